@@ -1,0 +1,198 @@
+/*
+ * oracle.c -- CPU oracle for C[MxN] = A[MxK] . B[KxN], FP16 inputs, FP32 output.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test-suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library; the two meet only through the seeded input arrays.
+ *
+ * What it computes (the plain definition of the product the lecture pages
+ * centre on):
+ *
+ *     R[i][j] = (float) sum_{k=0}^{K-1} (double) A[i*lda + k] * (double) B[k*ldb + j]
+ *
+ *   - "04_tensor_cores.py", demo 2 (block tensor-core GEMM) and "06_triton_style.py",
+ *     demos 1 and 4: every kernel on the pages is checked against the product of the
+ *     FP16 inputs widened to float64, which is exactly this sum.
+ *   - "04_tensor_cores.py", demo 1 observation 3: an FP16 x FP16 product has at most
+ *     11 + 11 significand bits, so each product below is exact in FP64; the only
+ *     rounding is in the FP64 running sum and in the single final cast to FP32.
+ *   - Summation order: increasing k, one running FP64 accumulator per output,
+ *     i-k-j loop order (rows in parallel), no blocking, no reordering.
+ *   - The final FP64 -> FP32 conversion is a plain C cast, i.e. IEEE round to
+ *     nearest, ties to even (the pages are silent; this is the plainest reading).
+ *   - K == 0 gives the empty sum 0 for every output; M == 0 or N == 0 writes nothing.
+ *
+ * FP16 values are decoded from their bit patterns by oracle_f16_to_f64(), written
+ * from the IEEE 754 binary16 definition (1 sign bit, 5 exponent bits with bias 15,
+ * 10 fraction bits; exponent 0 = zero/subnormal, exponent 31 = inf/NaN).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* IEEE 754 binary16 -> double, exact for every one of the 65536 patterns. */
+double oracle_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double mag;
+    if (expo == 0) {
+        /* zero or subnormal: 0.frac x 2^-14 */
+        mag = ldexp((double)frac, -24);
+    } else if (expo == 31) {
+        mag = frac ? NAN : INFINITY;
+    } else {
+        /* normal: 1.frac x 2^(expo-15) */
+        mag = ldexp((double)(1024 + frac), expo - 25);
+    }
+    return sign ? -mag : mag;
+}
+
+void oracle_decode_f16(const uint16_t *h, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_f16_to_f64(h[i]);
+}
+
+/* Decoding through a table built from oracle_f16_to_f64 keeps the triple loop plain
+ * while avoiding a ldexp per operand read. */
+static double g_f16_table[65536];
+static int g_f16_table_ready = 0;
+
+static const double *f16_table(void)
+{
+    if (!g_f16_table_ready) {
+        for (int i = 0; i < 65536; ++i)
+            g_f16_table[i] = oracle_f16_to_f64((uint16_t)i);
+        g_f16_table_ready = 1;
+    }
+    return g_f16_table;
+}
+
+static int check_args(const void *A, const void *B, const void *C, int64_t M, int64_t N,
+                      int64_t K, int64_t lda, int64_t ldb, int64_t ldc)
+{
+    if (M < 0 || N < 0 || K < 0) return 1;
+    if (lda < K || ldb < N || ldc < N) return 1;
+    if (M > 0 && N > 0 && !C) return 1;
+    if (M > 0 && K > 0 && !A) return 1;
+    if (N > 0 && K > 0 && !B) return 1;
+    return 0;
+}
+
+/*
+ * Rows [row0, row0 + nrows) of the FP64 sums, written to R (leading dimension ldr).
+ * This is the whole definition; the other entry points round or sample it.
+ */
+int oracle_gemm_rows_f64(const uint16_t *A, const uint16_t *B, double *R, int64_t M, int64_t N,
+                         int64_t K, int64_t lda, int64_t ldb, int64_t ldr, int64_t row0,
+                         int64_t nrows)
+{
+    if (check_args(A, B, R, M, N, K, lda, ldb, ldr)) return 1;
+    if (row0 < 0 || nrows < 0 || row0 + nrows > M) return 1;
+    const double *T = f16_table();
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = row0; i < row0 + nrows; ++i) {
+        double *r = R + (i - row0) * ldr;
+        for (int64_t j = 0; j < N; ++j) r[j] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double a = T[A[i * lda + k]];
+            const uint16_t *b = B + k * ldb;
+            for (int64_t j = 0; j < N; ++j) r[j] += a * T[b[j]];
+        }
+    }
+    return 0;
+}
+
+int oracle_gemm_f64(const uint16_t *A, const uint16_t *B, double *R, int64_t M, int64_t N,
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldr)
+{
+    return oracle_gemm_rows_f64(A, B, R, M, N, K, lda, ldb, ldr, 0, M);
+}
+
+/* Rows [row0, row0 + nrows) of the FP64 sums rounded once to FP32. */
+int oracle_gemm_rows_f32(const uint16_t *A, const uint16_t *B, float *C, int64_t M, int64_t N,
+                         int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t row0,
+                         int64_t nrows)
+{
+    if (check_args(A, B, C, M, N, K, lda, ldb, ldc)) return 1;
+    if (row0 < 0 || nrows < 0 || row0 + nrows > M) return 1;
+    const double *T = f16_table();
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+        if (!acc) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = row0; i < row0 + nrows; ++i) {
+            if (!acc) continue;
+            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double a = T[A[i * lda + k]];
+                const uint16_t *b = B + k * ldb;
+                for (int64_t j = 0; j < N; ++j) acc[j] += a * T[b[j]];
+            }
+            float *c = C + (i - row0) * ldc;
+            for (int64_t j = 0; j < N; ++j) c[j] = (float)acc[j];
+        }
+        free(acc);
+    }
+    return bad ? 2 : 0;
+}
+
+int oracle_gemm_f32(const uint16_t *A, const uint16_t *B, float *C, int64_t M, int64_t N,
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldc)
+{
+    return oracle_gemm_rows_f32(A, B, C, M, N, K, lda, ldb, ldc, 0, M);
+}
+
+/*
+ * Selected outputs (rows[t], cols[t]) for t < n: the same FP64 sum in the same
+ * order, for checking single elements of products too large to compute whole.
+ * out64 (may be NULL) receives the FP64 sums, out32 (may be NULL) the FP32 casts.
+ */
+int oracle_gemm_elems(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, const int64_t *rows, const int64_t *cols,
+                      int64_t n, double *out64, float *out32)
+{
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N || n < 0) return 1;
+    for (int64_t t = 0; t < n; ++t)
+        if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return 1;
+    const double *T = f16_table();
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t i = rows[t], j = cols[t];
+        double s = 0.0;
+        for (int64_t k = 0; k < K; ++k) s += T[A[i * lda + k]] * T[B[k * ldb + j]];
+        if (out64) out64[t] = s;
+        if (out32) out32[t] = (float)s;
+    }
+    return 0;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
