@@ -1,0 +1,141 @@
+/*
+ * tensor_core_tiled.h -- C ABI of the GB300 (sm_103a) FP16 -> FP32 tiled tensor-core GEMM.
+ *
+ * The operation is the blocked tensor-core matrix multiply that the lecture pages
+ * centre on: C[M x N] = A[M x K] . B[K x N] with FP16 inputs, FP32 accumulation and an
+ * FP32 result ("04_tensor_cores.py", function tc_matmul and demo 2: FP16 inputs, FP32
+ * accumulation), correct for any shape, ragged edges included ("06_triton_style.py",
+ * matmul_kernel and demo 1: out-of-range loads read as zero, out-of-range stores are
+ * skipped).  All matrices are row-major with explicit leading dimensions.
+ *
+ * Conventions shared by every entry point below:
+ *   - Pointers A, B, C are device-accessible addresses (cudaMalloc, torch CUDA tensors).
+ *     The caller owns all memory.  C must not overlap A or B.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All
+ *     work is enqueued on it; no call synchronises the host.
+ *   - C is overwritten (no beta term).  M == 0 or N == 0 is a no-op.  K == 0 writes zeros
+ *     (the empty sum) into the M x N block of C.
+ *   - Errors in the arguments are reported immediately through the return value and
+ *     nothing is enqueued.  Device-side errors (a pipeline wait that exceeded its time
+ *     limit) are recorded in a per-device error word read by gemm_f16_f32_get_error().
+ *   - Not thread-safe against concurrent first calls on the same device (the first call
+ *     per device caches device properties).
+ */
+#ifndef TENSOR_CORE_TILED_H
+#define TENSOR_CORE_TILED_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TCT_API __attribute__((visibility("default")))
+#else
+#define TCT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,        /* bad size, leading dimension, pointer or option */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not sm_103 (GB300)            */
+    GEMM_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed               */
+    GEMM_ERR_DEVICE_TIMEOUT = 4      /* a device pipeline wait exceeded its time limit  */
+} gemm_status;
+
+/*
+ * gemm_f16_f32 -- C = A . B, FP16 x FP16 -> FP32 accumulate -> FP32 C.
+ *   A   : FP16, M x K, row-major, element (i, k) at A[i*lda + k]; lda >= K.
+ *   B   : FP16, K x N, row-major, element (k, j) at B[k*ldb + j]; ldb >= N.
+ *   C   : FP32, M x N, row-major, element (i, j) at C[i*ldc + j]; ldc >= N.
+ *   M, N, K : 0 <= M, N, K < 2^31.
+ * Any alignment and any leading dimension are accepted.  When lda or ldb is not a
+ * multiple of 8 elements, or A or B is not 16-byte aligned, the operand is first copied
+ * on `stream` into a stream-ordered temporary (cudaMallocAsync/cudaFreeAsync) whose rows
+ * are 16-byte aligned.  The result does not depend on which path ran.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (negative or oversized dims, lda < K, ldb < N,
+ * ldc < N, NULL pointer with a non-empty extent), GEMM_ERR_UNSUPPORTED_DEVICE or
+ * GEMM_ERR_CUDA.
+ */
+TCT_API gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t M, int64_t N,
+                         int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void *stream);
+
+/*
+ * Tuning options for gemm_f16_f32_ex.  Zero in any field selects the library default.
+ *   group_m   : output tile rows per launch-order group ("06_triton_style.py",
+ *               matmul_kernel and demo 2: GROUP_M program order for L2 reuse); 1 gives
+ *               row-major tile order.  Range 1..256.
+ *   tile_n    : output tile width in columns: 128 or 256 (the tile height is 128).
+ *   stages    : shared-memory pipeline depth (2..the maximum that fits for tile_n).
+ *   max_ctas  : cap on the persistent grid (default: one CTA per SM).
+ *   timeout_ms: limit on any single device pipeline wait (default 2000 ms).
+ */
+typedef struct gemm_options {
+    int32_t group_m;
+    int32_t tile_n;
+    int32_t stages;
+    int32_t max_ctas;
+    int32_t timeout_ms;
+    int32_t reserved[3]; /* must be zero */
+} gemm_options;
+
+/* gemm_f16_f32 with explicit tuning options (opt may be NULL = all defaults). */
+TCT_API gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, int64_t N,
+                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void *stream,
+                            const gemm_options *opt);
+
+/*
+ * Launch plan the library would use for a problem (host only, no GPU needed when
+ * num_sms > 0 is given; num_sms <= 0 queries the current device).
+ */
+typedef struct gemm_plan {
+    int32_t tile_m, tile_n, tile_k; /* output tile and k-block                        */
+    int32_t stages;                 /* shared-memory pipeline depth                   */
+    int32_t group_m;                /* launch-order group height (tiles)              */
+    int32_t grid;                   /* persistent CTAs launched                       */
+    int64_t tiles;                  /* output tiles                                   */
+    int64_t waves;                  /* ceil(tiles / grid)                             */
+    double wave_efficiency;         /* M*N / (waves * grid * tile_m * tile_n)          */
+    int32_t smem_bytes;             /* dynamic shared memory per CTA                  */
+    int32_t pack_a, pack_b;         /* 1 if the operand would be repacked first       */
+} gemm_plan;
+
+TCT_API gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                              int32_t num_sms, const gemm_options *opt, gemm_plan *out);
+
+/*
+ * Launch-order map of the tile scheduler (host copy of the device function): linear tile
+ * index t -> (tile row, tile column) with GROUP_M grouping ("06_triton_style.py",
+ * matmul_kernel: groups of group_m tile rows, walked down the rows first).  Returns
+ * GEMM_ERR_INVALID_ARG when t is out of range or a count is not positive.
+ */
+TCT_API gemm_status gemm_tile_coord(int64_t t, int64_t num_m, int64_t num_n, int32_t group_m,
+                            int64_t *tile_row, int64_t *tile_col);
+
+/*
+ * Wave model ("02_gpu_execution_model.py", part 5, wave_utilization): tiles =
+ * ceil(M/tile_m)*ceil(N/tile_n), waves = ceil(tiles/slots), utilisation = tiles /
+ * (waves*slots).  Host only.
+ */
+TCT_API gemm_status gemm_wave_model(int64_t M, int64_t N, int64_t tile_m, int64_t tile_n, int64_t slots,
+                            int64_t *tiles, int64_t *waves, double *utilization);
+
+/*
+ * Reads and clears the device error word of the current device: GEMM_OK, or
+ * GEMM_ERR_DEVICE_TIMEOUT if a kernel launched since the last read gave up on a pipeline
+ * wait (its output is then incomplete).  Synchronises the current device first.
+ */
+TCT_API gemm_status gemm_f16_f32_get_error(void);
+
+/* Static description of a status code (never NULL). */
+TCT_API const char *gemm_status_string(int status);
+
+/* Library version string, e.g. "tensor_core_tiled 0.1 sm_103a". */
+TCT_API const char *gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TENSOR_CORE_TILED_H */

@@ -1,0 +1,184 @@
+"""Python binding of the GB300 FP16 -> FP32 tiled tensor-core GEMM (``libtensor_core_tiled.so``).
+
+Argument marshalling only: every step of the computation runs in the library's CUDA
+kernels.  The names mirror the C ABI in ``include/tensor_core_tiled.h``.  Importing this
+package does not load the library; the first call does, and raises ``GemmError`` if the
+library has not been built (``python -m tensor_core_tiled_gb300.build``) -- there is no
+fallback implementation.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtensor_core_tiled.so")
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_UNSUPPORTED_DEVICE = 2
+GEMM_ERR_CUDA = 3
+GEMM_ERR_DEVICE_TIMEOUT = 4
+
+# Every function the header declares (checked by the test-suite against the .so).
+EXPORTED = (
+    "gemm_f16_f32",
+    "gemm_f16_f32_ex",
+    "gemm_f16_f32_plan",
+    "gemm_tile_coord",
+    "gemm_wave_model",
+    "gemm_f16_f32_get_error",
+    "gemm_status_string",
+    "gemm_version",
+)
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})" if what else status_string(status))
+
+
+class GemmOptions(ctypes.Structure):
+    _fields_ = [("group_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 3)]
+
+
+class GemmPlan(ctypes.Structure):
+    _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("group_m", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("tiles", ctypes.c_int64), ("waves", ctypes.c_int64), ("wave_efficiency", ctypes.c_double),
+                ("smem_bytes", ctypes.c_int32), ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load():
+    """Load the shared library (once).  Raises GemmError if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise GemmError(GEMM_ERR_CUDA, f"{LIB_PATH} is not built; run tensor_core_tiled_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    lib.gemm_f16_f32.restype = ctypes.c_int
+    lib.gemm_f16_f32.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
+    lib.gemm_f16_f32_ex.restype = ctypes.c_int
+    lib.gemm_f16_f32_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, ctypes.POINTER(GemmOptions)]
+    lib.gemm_f16_f32_plan.restype = ctypes.c_int
+    lib.gemm_f16_f32_plan.argtypes = [i64, i64, i64, i64, i64, i32, ctypes.POINTER(GemmOptions),
+                                      ctypes.POINTER(GemmPlan)]
+    lib.gemm_tile_coord.restype = ctypes.c_int
+    lib.gemm_tile_coord.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    lib.gemm_wave_model.restype = ctypes.c_int
+    lib.gemm_wave_model.argtypes = [i64, i64, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                    ctypes.POINTER(ctypes.c_double)]
+    lib.gemm_f16_f32_get_error.restype = ctypes.c_int
+    lib.gemm_f16_f32_get_error.argtypes = []
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_status_string.argtypes = [ctypes.c_int]
+    lib.gemm_version.restype = ctypes.c_char_p
+    lib.gemm_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    try:
+        return load().gemm_status_string(int(status)).decode()
+    except GemmError:
+        return f"status {status}"
+
+
+def version():
+    return load().gemm_version().decode()
+
+
+def _options(group_m=0, tile_n=0, stages=0, max_ctas=0, timeout_ms=0):
+    o = GemmOptions()
+    o.group_m, o.tile_n, o.stages, o.max_ctas, o.timeout_ms = group_m, tile_n, stages, max_ctas, timeout_ms
+    return o
+
+
+def gemm_f16_f32(A, B, C, M, N, K, lda, ldb, ldc, stream=0):
+    """Raw C-ABI call with integer device pointers; returns the status code."""
+    return load().gemm_f16_f32(A, B, C, M, N, K, lda, ldb, ldc, stream or None)
+
+
+def gemm_f16_f32_ex(A, B, C, M, N, K, lda, ldb, ldc, stream=0, **options):
+    """Raw C-ABI call with tuning options (group_m, tile_n, stages, max_ctas, timeout_ms)."""
+    opt = _options(**options)
+    return load().gemm_f16_f32_ex(A, B, C, M, N, K, lda, ldb, ldc, stream or None, ctypes.byref(opt))
+
+
+def gemm_f16_f32_plan(M, N, K, lda=None, ldb=None, num_sms=0, **options):
+    """The launch plan (tile shape, stages, grid, waves) as a dict."""
+    opt = _options(**options)
+    pl = GemmPlan()
+    st = load().gemm_f16_f32_plan(M, N, K, K if lda is None else lda, N if ldb is None else ldb, num_sms,
+                                  ctypes.byref(opt), ctypes.byref(pl))
+    if st:
+        raise GemmError(st, "gemm_f16_f32_plan")
+    return {name: getattr(pl, name) for name, _ in GemmPlan._fields_}
+
+
+def gemm_tile_coord(t, num_m, num_n, group_m):
+    r, c = ctypes.c_int64(), ctypes.c_int64()
+    st = load().gemm_tile_coord(t, num_m, num_n, group_m, ctypes.byref(r), ctypes.byref(c))
+    if st:
+        raise GemmError(st, "gemm_tile_coord")
+    return r.value, c.value
+
+
+def gemm_wave_model(M, N, tile_m, tile_n, slots):
+    t, w, u = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_double()
+    st = load().gemm_wave_model(M, N, tile_m, tile_n, slots, ctypes.byref(t), ctypes.byref(w), ctypes.byref(u))
+    if st:
+        raise GemmError(st, "gemm_wave_model")
+    return t.value, w.value, u.value
+
+
+def gemm_f16_f32_get_error():
+    return load().gemm_f16_f32_get_error()
+
+
+def _current_stream_ptr(device):
+    import torch
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def matmul(A, B, C=None, stream=None, **options):
+    """C = A @ B for torch CUDA tensors: A (M x K) and B (K x N) float16 with unit column
+    stride, C (M x N) float32 (allocated if None).  Runs on ``stream`` (a torch.cuda.Stream)
+    or the current stream; raises GemmError on a non-zero status."""
+    import torch
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("A and B must be float16")
+    if not (A.is_cuda and B.is_cuda) or A.device != B.device:
+        raise ValueError("A and B must be CUDA tensors on one device")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if C.dtype != torch.float32 or tuple(C.shape) != (M, N) or C.device != A.device:
+        raise ValueError("C must be a float32 M x N tensor on A's device")
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if t.numel() and t.shape[1] > 1 and t.stride(1) != 1:
+            raise ValueError(f"{name} must be row-major (unit column stride)")
+    lda = A.stride(0) if M > 1 else max(K, 1)
+    ldb = B.stride(0) if K > 1 else max(N, 1)
+    ldc = C.stride(0) if M > 1 else max(N, 1)
+    s = stream.cuda_stream if stream is not None else _current_stream_ptr(A.device)
+    with torch.cuda.device(A.device):
+        if options:
+            st = gemm_f16_f32_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc, s, **options)
+        else:
+            st = gemm_f16_f32(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc, s)
+    if st:
+        raise GemmError(st, "gemm_f16_f32")
+    return C

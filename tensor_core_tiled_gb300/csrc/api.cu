@@ -1,0 +1,332 @@
+// api.cu -- the C ABI: argument validation, launch planning, TMA descriptor encoding and
+// the stream-ordered launch sequence (optional operand repack, then the GEMM kernel).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_internal.h"
+#include "tile_sched.h"
+#include "tensor_core_tiled.h"
+
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+constexpr int kDefaultGroupM = 8;
+constexpr int kDefaultTimeoutMs = 2000;
+constexpr int kMaxDevices = 64;
+// Relative per-tile tensor throughput used by the tile-width choice: a 128-wide tile
+// reads as many A bytes per MMA as a 256-wide one but does half the work with them.
+constexpr double kNarrowTileRate = 0.90;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int major = 0;
+    int minor = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+gemm_status device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        d.ready = true;
+    }
+    *out = d;
+    if (d.major != 10 || d.minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    return GEMM_OK;
+}
+
+gemm_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return GEMM_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    *fn = g_encode;
+    return GEMM_OK;
+}
+
+// 2-D FP16 tensor map over a row-major matrix of `rows` x `cols` with leading dimension
+// `ld` (elements), boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill.
+gemm_status encode_fp16_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld,
+                           uint32_t box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    gemm_status st = get_encoder(&enc);
+    if (st != GEMM_OK) return st;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+bool tma_ok(const void *p, int64_t ld) { return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && (ld % 8 == 0); }
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+gemm_status check_options(const gemm_options *opt)
+{
+    if (!opt) return GEMM_OK;
+    for (int i = 0; i < 3; ++i)
+        if (opt->reserved[i] != 0) return GEMM_ERR_INVALID_ARG;
+    if (opt->group_m < 0 || opt->group_m > 256) return GEMM_ERR_INVALID_ARG;
+    if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return GEMM_ERR_INVALID_ARG;
+    if (opt->stages < 0 || opt->max_ctas < 0 || opt->timeout_ms < 0) return GEMM_ERR_INVALID_ARG;
+    if (opt->stages != 0) {
+        const int tn = opt->tile_n ? opt->tile_n : 256;
+        if (tct::variant_smem_bytes(tn, opt->stages) < 0) return GEMM_ERR_INVALID_ARG;
+    }
+    return GEMM_OK;
+}
+
+gemm_status check_args(const void *A, const void *B, const float *C, int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc)
+{
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_ARG;
+    if (lda < K || ldb < N || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (lda > kMaxDim * 4 || ldb > kMaxDim * 4 || ldc > kMaxDim * 4) return GEMM_ERR_INVALID_ARG;
+    if (M > 0 && N > 0) {
+        if (!C || reinterpret_cast<uintptr_t>(C) % 4 != 0) return GEMM_ERR_INVALID_ARG;
+    }
+    if (M > 0 && N > 0 && K > 0) {
+        if (!A || reinterpret_cast<uintptr_t>(A) % 2 != 0) return GEMM_ERR_INVALID_ARG;
+        if (!B || reinterpret_cast<uintptr_t>(B) % 2 != 0) return GEMM_ERR_INVALID_ARG;
+    }
+    return GEMM_OK;
+}
+
+double wave_util(int64_t M, int64_t N, int64_t tm, int64_t tn, int64_t slots, int64_t *tiles_out,
+                 int64_t *waves_out)
+{
+    const int64_t tiles = tct::ceil_div(M, tm) * tct::ceil_div(N, tn);
+    const int64_t waves = tct::ceil_div(tiles, slots);
+    if (tiles_out) *tiles_out = tiles;
+    if (waves_out) *waves_out = waves;
+    return static_cast<double>(tiles) / static_cast<double>(waves * slots);
+}
+
+// Fraction of the SM-time of the launch spent on useful output elements.
+double useful_fraction(int64_t M, int64_t N, int64_t tn, int64_t sms)
+{
+    int64_t tiles = 0, waves = 0;
+    wave_util(M, N, kTileM, tn, sms, &tiles, &waves);
+    return static_cast<double>(M) * static_cast<double>(N) /
+           (static_cast<double>(waves) * sms * kTileM * tn);
+}
+
+gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int sms,
+                      const gemm_options *opt, const void *A, const void *B, gemm_plan *pl)
+{
+    std::memset(pl, 0, sizeof(*pl));
+    int tile_n = opt && opt->tile_n ? opt->tile_n : 0;
+    if (!tile_n) {
+        // Wave-quantisation-aware width ("02_gpu_execution_model.py", part 5): compare the
+        // useful share of SM-time of both widths, weighting the narrow tile's lower rate.
+        const double u256 = useful_fraction(M, N, 256, sms);
+        const double u128 = useful_fraction(M, N, 128, sms) * kNarrowTileRate;
+        tile_n = (u128 > u256) ? 128 : 256;
+    }
+    int stages = opt && opt->stages ? opt->stages : (tile_n == 256 ? 4 : 6);
+    const int smem = tct::variant_smem_bytes(tile_n, stages);
+    if (smem < 0) return GEMM_ERR_INVALID_ARG;
+    const int group_m = opt && opt->group_m ? opt->group_m : kDefaultGroupM;
+    int64_t tiles = 0, waves = 0;
+    const int64_t num_m = tct::ceil_div(M, kTileM), num_n = tct::ceil_div(N, tile_n);
+    tiles = num_m * num_n;
+    int64_t grid = tiles < sms ? tiles : sms;
+    if (opt && opt->max_ctas > 0 && grid > opt->max_ctas) grid = opt->max_ctas;
+    if (grid < 1) grid = 1;
+    waves = tct::ceil_div(tiles, grid);
+    pl->tile_m = kTileM;
+    pl->tile_n = tile_n;
+    pl->tile_k = kTileK;
+    pl->stages = stages;
+    pl->group_m = group_m;
+    pl->grid = static_cast<int32_t>(grid);
+    pl->tiles = tiles;
+    pl->waves = waves;
+    pl->wave_efficiency = tiles ? static_cast<double>(M) * N / (static_cast<double>(waves) * grid * kTileM * tile_n)
+                                : 0.0;
+    pl->smem_bytes = smem;
+    pl->pack_a = (K > 0 && !tma_ok(A, lda)) ? 1 : 0;
+    pl->pack_b = (K > 0 && !tma_ok(B, ldb)) ? 1 : 0;
+    return GEMM_OK;
+}
+
+gemm_status to_status(cudaError_t e) { return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int64_t ldc, void *stream, const gemm_options *opt)
+{
+    gemm_status st = check_args(A, B, C, M, N, K, lda, ldb, ldc);
+    if (st != GEMM_OK) return st;
+    st = check_options(opt);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceInfo dev;
+    st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return to_status(tct::launch_fill_zero(C, ldc, M, N, dev.sms, s));
+
+    gemm_plan pl;
+    st = make_plan(M, N, K, lda, ldb, dev.sms, opt, A, B, &pl);
+    if (st != GEMM_OK) return st;
+
+    // Operands whose rows do not start on 16-byte boundaries are copied first (TMA needs
+    // 16-byte aligned bases and row strides); the copy is stream-ordered.
+    const void *a_use = A, *b_use = B;
+    int64_t lda_use = lda, ldb_use = ldb;
+    void *ws = nullptr;
+    if (pl.pack_a || pl.pack_b) {
+        const int64_t lda_p = round_up(K, 8), ldb_p = round_up(N, 8);
+        const int64_t a_bytes = pl.pack_a ? round_up(M * lda_p * 2, 256) : 0;
+        const int64_t b_bytes = pl.pack_b ? round_up(K * ldb_p * 2, 256) : 0;
+        if (cudaMallocAsync(&ws, static_cast<size_t>(a_bytes + b_bytes), s) != cudaSuccess) return GEMM_ERR_CUDA;
+        uint8_t *w = static_cast<uint8_t *>(ws);
+        cudaError_t e = cudaSuccess;
+        if (pl.pack_a) {
+            e = tct::launch_pack(A, lda, w, lda_p, M, K, dev.sms, s);
+            a_use = w;
+            lda_use = lda_p;
+        }
+        if (e == cudaSuccess && pl.pack_b) {
+            e = tct::launch_pack(B, ldb, w + a_bytes, ldb_p, K, N, dev.sms, s);
+            b_use = w + a_bytes;
+            ldb_use = ldb_p;
+        }
+        if (e != cudaSuccess) {
+            cudaFreeAsync(ws, s);
+            return GEMM_ERR_CUDA;
+        }
+    }
+
+    CUtensorMap ta, tb;
+    st = encode_fp16_2d(&ta, a_use, M, K, lda_use, kTileM);
+    if (st == GEMM_OK) st = encode_fp16_2d(&tb, b_use, K, N, ldb_use, kTileK);
+    if (st == GEMM_OK) {
+        tct::KernelParams p;
+        p.C = C;
+        p.ldc = ldc;
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.K = static_cast<int32_t>(K);
+        p.num_m = static_cast<int32_t>(tct::ceil_div(M, kTileM));
+        p.num_n = static_cast<int32_t>(tct::ceil_div(N, pl.tile_n));
+        p.num_kb = static_cast<int32_t>(tct::ceil_div(K, kTileK));
+        p.num_tiles = static_cast<int32_t>(pl.tiles);
+        p.group_m = pl.group_m;
+        p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 1 : 0;
+        const int tmo = opt && opt->timeout_ms ? opt->timeout_ms : kDefaultTimeoutMs;
+        p.timeout_ns = static_cast<uint64_t>(tmo) * 1000000ull;
+        st = to_status(tct::launch_gemm(ta, tb, p, pl.tile_n, pl.stages, pl.grid, s));
+    }
+    if (ws) {
+        if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
+    }
+    return st;
+}
+
+gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                         int64_t lda, int64_t ldb, int64_t ldc, void *stream)
+{
+    return gemm_f16_f32_ex(A, B, C, M, N, K, lda, ldb, ldc, stream, nullptr);
+}
+
+gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int32_t num_sms,
+                              const gemm_options *opt, gemm_plan *out)
+{
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || lda < K || ldb < N)
+        return GEMM_ERR_INVALID_ARG;
+    gemm_status st = check_options(opt);
+    if (st != GEMM_OK) return st;
+    int sms = num_sms;
+    if (sms <= 0) {
+        DeviceInfo dev;
+        st = device_info(&dev);
+        if (st != GEMM_OK) return st;
+        sms = dev.sms;
+    }
+    // Alignment of the base pointers is unknown here: assume 16-byte aligned bases.
+    const void *aligned = reinterpret_cast<const void *>(uintptr_t{256});
+    return make_plan(M, N, K, lda, ldb, sms, opt, aligned, aligned, out);
+}
+
+gemm_status gemm_tile_coord(int64_t t, int64_t num_m, int64_t num_n, int32_t group_m, int64_t *tile_row,
+                            int64_t *tile_col)
+{
+    if (num_m <= 0 || num_n <= 0 || group_m <= 0 || t < 0 || !tile_row || !tile_col) return GEMM_ERR_INVALID_ARG;
+    if (num_m > kMaxDim || num_n > kMaxDim || num_m * num_n > kMaxDim || t >= num_m * num_n)
+        return GEMM_ERR_INVALID_ARG;
+    const tct::TileCoord c = tct::tile_coord(static_cast<int32_t>(t), static_cast<int32_t>(num_m),
+                                             static_cast<int32_t>(num_n), group_m);
+    *tile_row = c.m;
+    *tile_col = c.n;
+    return GEMM_OK;
+}
+
+gemm_status gemm_wave_model(int64_t M, int64_t N, int64_t tile_m, int64_t tile_n, int64_t slots, int64_t *tiles,
+                            int64_t *waves, double *utilization)
+{
+    if (M <= 0 || N <= 0 || tile_m <= 0 || tile_n <= 0 || slots <= 0) return GEMM_ERR_INVALID_ARG;
+    const double u = wave_util(M, N, tile_m, tile_n, slots, tiles, waves);
+    if (utilization) *utilization = u;
+    return GEMM_OK;
+}
+
+gemm_status gemm_f16_f32_get_error(void)
+{
+    unsigned w = 0;
+    if (tct::read_and_clear_error(&w) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (w == 0) return GEMM_OK;
+    return static_cast<gemm_status>(w & 0xffu);
+}
+
+const char *gemm_status_string(int status)
+{
+    switch (status) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103, GB300)";
+    case GEMM_ERR_CUDA: return "CUDA runtime or driver error";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    default: return "unknown status";
+    }
+}
+
+const char *gemm_version(void) { return "tensor_core_tiled 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,411 @@
+// gemm_sm103a.cu -- persistent, warp-specialised FP16 x FP16 -> FP32 GEMM for GB300 (sm_103a).
+//
+// C[M x N] = A[M x K] . B[K x N], all row-major, FP32 accumulation in tensor memory.
+// This is the blocked tensor-core matrix multiply of the lecture pages ("04_tensor_cores.py",
+// tc_matmul and demo 2; "06_triton_style.py", matmul_kernel), re-designed for the
+// 5th-generation tensor core instead of the mma.sync/ldmatrix and Triton realisations the
+// pages describe:
+//
+//   * Block tiling with a K loop: each CTA owns 128 x BN output tiles and walks K in
+//     64-element blocks ("04_tensor_cores.py", tc_matmul: BM x BN blocks, a BK loop).
+//   * Operand tiles reach shared memory through TMA with the 128-byte swizzle, the
+//     hardware form of the XOR swizzle of demo 2 (16-byte chunk index XOR row mod 8), so
+//     tensor-core reads of any 8 rows hit distinct banks.  A (K-major) and B (row-major,
+//     i.e. N-major) are consumed as stored: B needs no transposed copy.
+//   * A ring of STAGES shared-memory stages guarded by mbarriers, sized by the Little's-law
+//     argument of "04_tensor_cores.py" demo 4 (data in flight = consumption rate x latency,
+//     capped by the 227 KB of shared memory).
+//   * Warp specialisation (demo 4, observation 4: one producer issues TMA, consumers only
+//     compute): warp 0 issues TMA, warp 1 issues tcgen05.mma from one thread, warps 2..5
+//     drain the FP32 accumulators from TMEM.  Two TMEM accumulator buffers let the
+//     epilogue of one tile overlap the main loop of the next.
+//   * A persistent grid of at most one CTA per SM walks the tiles in GROUP_M launch order
+//     ("06_triton_style.py", matmul_kernel / demo 2) for L2 reuse.
+//   * Ragged shapes ("06_triton_style.py", matmul_kernel masks): TMA fills out-of-range
+//     operand elements with zeros (the masked load with other = 0) and the epilogue
+//     predicates every store on row < M and column < N (the masked store).
+//   * Every pipeline wait is bounded in wall time; on expiry the CTA records an error
+//     code in a device word, drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gemm_internal.h"
+#include "ptx_sm103a.cuh"
+#include "tile_sched.h"
+
+namespace tct {
+
+__device__ unsigned int g_error_word;
+
+template <int BN_, int STAGES_>
+struct Cfg {
+    static constexpr int BM = 128;
+    static constexpr int BN = BN_;
+    static constexpr int BK = 64;  // 64 FP16 = 128 bytes = one swizzle row
+    static constexpr int STAGES = STAGES_;
+    static constexpr int UMMA_K = 16;  // K of one kind::f16 MMA
+    static constexpr int A_STAGE = BM * BK * 2;
+    static constexpr int B_SUB = BK * 64 * 2;  // one 64-column TMA box of B
+    static constexpr int B_STAGE = BK * BN * 2;
+    static constexpr int STAGE_TX = A_STAGE + B_STAGE;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_BYTES = EPI_WARPS * 32 * 32 * 4;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SMEM_BYTES =
+        1024 + STAGES * (A_STAGE + B_STAGE) + EPI_BYTES + NUM_BARS * 8 + 16;
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256 in steps of 64");
+    static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
+    static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory");
+};
+
+enum WaitSite : unsigned {
+    SITE_PRODUCER_EMPTY = 1,
+    SITE_MMA_FULL = 2,
+    SITE_MMA_TMEM_EMPTY = 3,
+    SITE_EPI_TMEM_FULL = 4,
+};
+
+__device__ __forceinline__ void record_timeout(volatile int *abort_flag, unsigned site)
+{
+    atomicCAS(&g_error_word, 0u, (unsigned)GEMM_ERR_DEVICE_TIMEOUT_CODE | (site << 8));
+    *abort_flag = 1;
+    __threadfence_block();
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int *abort_flag, unsigned site)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++spins & 15u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                record_timeout(abort_flag, site);
+                return false;
+            }
+        }
+    }
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    gemm_f16_f32_tcgen05(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB, const KernelParams p)
+{
+    using Cf = Cfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte swizzle atoms must start on 1024-byte boundaries of the shared space.
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sA = smem;
+    uint8_t *sB = sA + STAGES * Cf::A_STAGE;
+    float *sEpi = reinterpret_cast<float *>(sB + STAGES * Cf::B_STAGE);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sEpi) + Cf::EPI_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cf::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), Cf::EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cf::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint64_t limit = p.timeout_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_parity[STAGES];
+            bool issued[STAGES];
+            for (int i = 0; i < STAGES; ++i) issued[i] = false, issued_parity[i] = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                const TileCoord c = tile_coord(t, p.num_m, p.num_n, p.group_m);
+                const int32_t m0 = c.m * Cf::BM;
+                const int32_t n0 = c.n * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_or_abort(empty_bar(s), ph ^ 1u, limit, abort_flag,
+                                       SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_TX);
+                    const int32_t k0 = kb * Cf::BK;
+                    tma_load_2d(smem_u32(sA + s * Cf::A_STAGE), &tmA, k0, m0, full_bar(s));
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(smem_u32(sB + s * Cf::B_STAGE + j * Cf::B_SUB), &tmB, n0 + 64 * j,
+                                    k0, full_bar(s));
+                    issued[s] = true;
+                    issued_parity[s] = ph;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let this CTA's loads land before shared memory is released.
+                for (int i = 0; i < STAGES; ++i)
+                    if (issued[i]) (void)mbar_wait(full_bar(i), issued_parity[i], limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(Cf::BM, BN, /*b_mn_major=*/true);
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool ok = true;
+            bool any_mma = false;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+                const int b = it & 1;
+                const uint32_t use = static_cast<uint32_t>(it >> 1);
+                if (!wait_or_abort(tempty_bar(b), (use & 1u) ^ 1u, limit, abort_flag,
+                                   SITE_MMA_TMEM_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_or_abort(full_bar(s), ph, limit, abort_flag, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sA + s * Cf::A_STAGE);
+                    const uint32_t b_base = smem_u32(sB + s * Cf::B_STAGE);
+#pragma unroll
+                    for (int kk = 0; kk < Cf::BK / Cf::UMMA_K; ++kk) {
+                        // A: K-major, 128-byte rows, 8-row groups 1024 B apart; a K step of
+                        // 16 elements is 32 bytes inside the swizzle row.
+                        const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                        // B: N-major, 64-column boxes B_SUB bytes apart (leading offset),
+                        // 8-row K groups 1024 B apart (stride offset); 16 K rows = 2048 B.
+                        const uint64_t bdesc = smem_desc_sw128(b_base + kk * 2048, Cf::B_SUB, 1024);
+                        tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    any_mma = true;
+                    tc_commit(empty_bar(s));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(tfull_bar(b));
+            }
+            if (!ok && any_mma) {
+                // Wait for this thread's MMAs before TMEM is released.
+                tc_commit(drain_bar);
+                (void)mbar_wait(drain_bar, 0, limit);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        float *stage = sEpi + (warp - 2) * 32 * 32;
+        const bool vec = p.vec_store != 0;
+        int it = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+            const int b = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            bool ok = wait_or_abort(tfull_bar(b), use & 1u, limit, abort_flag, SITE_EPI_TMEM_FULL);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const TileCoord c = tile_coord(t, p.num_m, p.num_n, p.group_m);
+            const int64_t row_base = static_cast<int64_t>(c.m) * Cf::BM + q * 32;
+            const int64_t col_base = static_cast<int64_t>(c.n) * BN;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(b * BN);
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + ch * 32, r);
+                tmem_wait_ld();
+                if (ch == BN / 32 - 1) {
+                    // Accumulator fully read: hand the buffer back to the MMA warp.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(b));
+                }
+                // Row `lane` of this 32 x 32 block into the staging buffer, 16-byte chunks
+                // XOR-swizzled by row so the transposed read below is conflict-free.
+                float4 *srow = reinterpret_cast<float4 *>(stage + lane * 32);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    srow[j ^ (lane & 7)] =
+                        make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
+                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                __syncwarp();
+                // Coalesced, predicated stores: 8 lanes cover one 128-byte row segment.
+                const int jj = lane & 7;
+                const int64_t gcol = col_base + ch * 32 + jj * 4;
+#pragma unroll
+                for (int rr0 = 0; rr0 < 32; rr0 += 4) {
+                    const int rr = rr0 + (lane >> 3);
+                    const float4 v = reinterpret_cast<const float4 *>(stage + rr * 32)[jj ^ (rr & 7)];
+                    const int64_t grow = row_base + rr;
+                    if (grow < p.M) {
+                        float *dst = p.C + grow * p.ldc + gcol;
+                        if (vec && gcol + 3 < p.N) {
+                            __stcs(reinterpret_cast<float4 *>(dst), v);
+                        } else {
+                            if (gcol + 0 < p.N) __stcs(dst + 0, v.x);
+                            if (gcol + 1 < p.N) __stcs(dst + 1, v.y);
+                            if (gcol + 2 < p.N) __stcs(dst + 2, v.z);
+                            if (gcol + 3 < p.N) __stcs(dst + 3, v.w);
+                        }
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- helper kernels
+
+// Row copy into a buffer whose rows start on 16-byte boundaries (TMA's stride rule).
+__global__ void pack_rows_f16(const uint16_t *__restrict__ src, int64_t ld_src,
+                              uint16_t *__restrict__ dst, int64_t ld_dst, int64_t rows, int64_t cols)
+{
+    const int64_t total = rows * cols;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / cols;
+        const int64_t c = i - r * cols;
+        dst[r * ld_dst + c] = src[r * ld_src + c];
+    }
+}
+
+// K == 0: the empty sum.
+__global__ void fill_zero_f32(float *__restrict__ C, int64_t ldc, int64_t rows, int64_t cols)
+{
+    const int64_t total = rows * cols;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / cols;
+        C[r * ldc + (i - r * cols)] = 0.0f;
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+template <int BN, int STAGES>
+static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const KernelParams &p,
+                                  int grid, cudaStream_t stream)
+{
+    using Cf = Cfg<BN, STAGES>;
+    auto kern = gemm_f16_f32_tcgen05<BN, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cf::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 192, Cf::SMEM_BYTES, stream>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+int variant_smem_bytes(int tile_n, int stages)
+{
+#define TCT_CASE(BN_, ST_) \
+    if (tile_n == BN_ && stages == ST_) return Cfg<BN_, ST_>::SMEM_BYTES;
+    TCT_VARIANTS(TCT_CASE)
+#undef TCT_CASE
+    return -1;
+}
+
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const KernelParams &p, int tile_n,
+                        int stages, int grid, cudaStream_t stream)
+{
+#define TCT_CASE(BN_, ST_) \
+    if (tile_n == BN_ && stages == ST_) return launch_variant<BN_, ST_>(ta, tb, p, grid, stream);
+    TCT_VARIANTS(TCT_CASE)
+#undef TCT_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pack(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows,
+                        int64_t cols, int num_sms, cudaStream_t stream)
+{
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int64_t total = rows * cols;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    pack_rows_f16<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(src), ld_src, static_cast<uint16_t *>(dst), ld_dst, rows, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_zero(float *C, int64_t ldc, int64_t rows, int64_t cols, int num_sms,
+                             cudaStream_t stream)
+{
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int64_t total = rows * cols;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    fill_zero_f32<<<static_cast<int>(blocks), 256, 0, stream>>>(C, ldc, rows, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_error(unsigned *out)
+{
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(out, g_error_word, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned));
+}
+
+}  // namespace tct

@@ -9,3 +9,15 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def tct_lib():
+    """The built C-ABI library (compiled in-tree if missing or stale)."""
+    from tensor_core_tiled_gb300 import build
+    import tensor_core_tiled_gb300 as tct
+    build.build()
+    return tct.load()

@@ -1,0 +1,138 @@
+"""CPU-side checks of the C ABI: the library loads and exports every declared symbol, and
+the host logic (argument validation, tile scheduler, wave model, planner) behaves as the
+lecture pages' figures require.  No test here launches a kernel."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import tensor_core_tiled_gb300 as tct
+from tests.golden import figures
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names.update(re.findall(r"TCT_API\s+[\w\s\*]+?\b(\w+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol(tct_lib):
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    assert declared == set(tct.EXPORTED)
+    for name in declared:
+        assert hasattr(tct_lib, name), name
+        assert ctypes.cast(getattr(tct_lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings(tct_lib):
+    assert "sm_103a" in tct.version()
+    for code in range(5):
+        assert tct.status_string(code)
+    assert tct.status_string(99) == "unknown status"
+
+
+def test_invalid_arguments_rejected_before_any_device_work(tct_lib):
+    p = 1 << 20  # never dereferenced: validation fails first
+    bad = [
+        (p, p, p, -1, 4, 4, 4, 4, 4),      # negative M
+        (p, p, p, 4, 4, 4, 3, 4, 4),       # lda < K
+        (p, p, p, 4, 4, 4, 4, 3, 4),       # ldb < N
+        (p, p, p, 4, 4, 4, 4, 4, 3),       # ldc < N
+        (0, p, p, 4, 4, 4, 4, 4, 4),       # NULL A
+        (p, 0, p, 4, 4, 4, 4, 4, 4),       # NULL B
+        (p, p, 0, 4, 4, 4, 4, 4, 4),       # NULL C
+        (p + 1, p, p, 4, 4, 4, 4, 4, 4),   # A not FP16-aligned
+        (p, p, p + 2, 4, 4, 4, 4, 4, 4),   # C not FP32-aligned
+        (p, p, p, 1 << 31, 4, 4, 4, 4, 4),  # M too large
+    ]
+    for args in bad:
+        assert tct.gemm_f16_f32(*args, 0) == tct.GEMM_ERR_INVALID_ARG, args
+    # empty output is a no-op that needs no device
+    assert tct.gemm_f16_f32(0, 0, 0, 0, 5, 7, 7, 5, 5, 0) == tct.GEMM_OK
+    assert tct.gemm_f16_f32(0, 0, 0, 5, 0, 7, 7, 0, 0, 0) == tct.GEMM_OK
+    # bad options
+    assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, tile_n=96) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, stages=9) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, group_m=-1) == tct.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("num_m,num_n", [(9, 9), (7, 14), (32, 16), (13, 5), (1, 40), (40, 1)])
+@pytest.mark.parametrize("group_m", [1, 2, 3, 4, 8, 16])
+def test_tile_order_is_a_bijection(tct_lib, num_m, num_n, group_m):
+    seen = set()
+    for t in range(num_m * num_n):
+        m, n = tct.gemm_tile_coord(t, num_m, num_n, group_m)
+        assert 0 <= m < num_m and 0 <= n < num_n
+        seen.add((m, n))
+    assert len(seen) == num_m * num_n
+
+
+def test_tile_order_row_major_and_grouped(tct_lib):
+    # group_m = 1 is row-major
+    assert [tct.gemm_tile_coord(t, 3, 4, 1) for t in range(5)] == [(0, 0), (0, 1), (0, 2), (0, 3), (1, 0)]
+    # inside a group the index walks down the rows first
+    assert [tct.gemm_tile_coord(t, 9, 9, 3) for t in range(4)] == [(0, 0), (1, 0), (2, 0), (0, 1)]
+    # the last group may be shorter than group_m
+    assert tct.gemm_tile_coord(9 * 8, 9, 9, 4) == (8, 0)
+    assert tct.gemm_tile_coord(9 * 8 + 1, 9, 9, 4) == (8, 1)
+
+
+def test_page_grouping_example_90_vs_54(tct_lib):
+    """9x9 output blocks, K = 9 blocks: the first 9 programs read 90 blocks in row-major
+    order and 54 with GROUP_M = 3 ("06_triton_style.py" demo 2)."""
+    fig = figures.load()
+
+    def blocks_read(group_m):
+        coords = [tct.gemm_tile_coord(t, 9, 9, group_m) for t in range(9)]
+        rows = {m for m, _ in coords}
+        cols = {n for _, n in coords}
+        return len(rows) * 9 + len(cols) * 9
+
+    assert blocks_read(1) == fig["group9_rowmajor_blocks"]
+    assert blocks_read(3) == fig["group9_grouped3_blocks"]
+
+
+def test_page_wave_quantisation_example(tct_lib):
+    """A100, 108 SMs, 256x128 tiles: n = 1792 -> 98 tiles in 1 wave, n = 1793 -> 120 tiles in
+    2 waves ("02_gpu_execution_model.py" part 5)."""
+    fig = figures.load()
+    sms = int(fig["wave_sms"])
+    t, w, u = tct.gemm_wave_model(1792, 1792, 256, 128, sms)
+    assert (t, w) == (fig["wave_1792_tiles"], fig["wave_1792_waves"])
+    assert u == pytest.approx(98 / 108)
+    t, w, u = tct.gemm_wave_model(1793, 1793, 256, 128, sms)
+    assert (t, w) == (fig["wave_1793_tiles"], fig["wave_1793_waves"])
+    assert u == pytest.approx(120 / 216)
+    with pytest.raises(tct.GemmError):
+        tct.gemm_wave_model(0, 5, 128, 128, 10)
+
+
+def test_planner_on_gb300_shapes(tct_lib):
+    sms = 152
+    p = tct.gemm_f16_f32_plan(8192, 8192, 8192, num_sms=sms)
+    assert (p["tile_m"], p["tile_n"], p["tile_k"]) == (128, 256, 64)
+    assert p["grid"] == sms and p["tiles"] == 64 * 32
+    assert p["waves"] == -(-2048 // sms)
+    assert p["pack_a"] == 0 and p["pack_b"] == 0
+    # the skinny, bandwidth-bound shape spreads over more SMs with the narrow tile
+    p = tct.gemm_f16_f32_plan(128, 16384, 16384, num_sms=sms)
+    assert p["tile_n"] == 128 and p["grid"] == 128
+    # ragged leading dimensions are repacked before TMA
+    p = tct.gemm_f16_f32_plan(17, 4097, 31, num_sms=sms)
+    assert p["pack_a"] == 1 and p["pack_b"] == 1
+    p = tct.gemm_f16_f32_plan(300, 200, 150, num_sms=sms)
+    assert p["pack_a"] == 1 and p["pack_b"] == 0
+    # explicit options are honoured
+    p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, tile_n=256, stages=3, group_m=16, max_ctas=100)
+    assert (p["tile_n"], p["stages"], p["group_m"], p["grid"]) == (256, 3, 16, 100)
+    # the shared-memory ring fits the 227 KB limit
+    for tn, st in ((256, 2), (256, 3), (256, 4), (128, 4), (128, 6)):
+        p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, tile_n=tn, stages=st)
+        assert 0 < p["smem_bytes"] <= 227 * 1024

@@ -1,0 +1,230 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Criteria (tests/parity.py): element-wise |C - R| <= 1e-3 * sqrt(K) * max(1, |R|) for N(0,1)
+FP16 inputs; bit-exact FP32 for integer-valued inputs in [-4, 4] (partial sums < 2^24).
+Small and medium shapes are compared whole; the full-size workloads on sampled outputs
+spread over every tile row/column class (first, last, interior) plus random positions.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import tensor_core_tiled_gb300 as tct
+from tensor_core_tiled_gb300 import inputs
+from tests.parity import bit_exact, within_tol, worst_ratio
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(tct_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+
+
+def dev16(x):
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.float16)
+
+
+def gpu_gemm(A, B, **opts):
+    C = tct.matmul(dev16(A), dev16(B), **opts)
+    torch.cuda.synchronize()
+    return C.cpu().numpy()
+
+
+def check_tol(A, B, C=None, **opts):
+    M, K = A.shape
+    if C is None:
+        C = gpu_gemm(A, B, **opts)
+    R = oracle.gemm_f32(A, B)
+    assert within_tol(C, R, K), f"worst |err|/tol = {worst_ratio(C, R, K):.3g}"
+    return C, R
+
+
+def test_square_256_seed0():
+    (M, N, K), A, B = inputs.workload("square256")[0]
+    C, R = check_tol(A, B)
+    err = np.abs(C.astype(np.float64) - oracle.gemm_f64(A, B)).max()
+    # FP32 accumulation error of a 256-term sum: small but not the FP64 result
+    assert 1e-7 < err < 1e-4
+
+
+@pytest.mark.parametrize("idx", range(len(inputs.RAGGED_SHAPES)))
+def test_ragged_normal(idx):
+    (M, N, K), A, B = inputs.workload("ragged")[idx]
+    check_tol(A, B)
+
+
+@pytest.mark.parametrize("idx", range(len(inputs.RAGGED_SHAPES)))
+def test_ragged_integer_bit_exact(idx):
+    (M, N, K), A, B = inputs.workload("ragged_int")[idx]
+    C = gpu_gemm(A, B)
+    assert bit_exact(C, oracle.gemm_f32(A, B))
+
+
+def test_mma_tile_16x8x16():
+    rng = np.random.default_rng(0)
+    worst = 0.0
+    for _ in range(20):
+        A = rng.standard_normal((16, 16)).astype(np.float16)
+        B = rng.standard_normal((16, 8)).astype(np.float16)
+        C, R = check_tol(A, B)
+        worst = max(worst, float(np.abs(C.astype(np.float64) - oracle.gemm_f64(A, B)).max()))
+    assert worst < 1e-5
+
+
+@pytest.mark.parametrize("shape", [(64, 64, 64), (128, 64, 96), (1, 1, 1), (17, 33, 65), (100, 70, 50),
+                                   (64, 64, 40), (128, 256, 64), (129, 257, 65), (255, 511, 127)])
+def test_edge_shapes(shape):
+    M, N, K = shape
+    rng = np.random.default_rng(3)
+    A, B = inputs.normal_pair(rng, M, N, K)
+    check_tol(A, B)
+
+
+def test_identity_and_permutation():
+    rng = np.random.default_rng(5)
+    n = 384
+    X = rng.standard_normal((n, 300)).astype(np.float16)
+    eye = np.eye(n, dtype=np.float16)
+    assert np.array_equal(gpu_gemm(eye, X), X.astype(np.float32))
+    Y = rng.standard_normal((200, n)).astype(np.float16)
+    assert np.array_equal(gpu_gemm(Y, eye), Y.astype(np.float32))
+    perm = rng.permutation(n)
+    P = np.zeros((n, n), np.float16)
+    P[np.arange(n), perm] = 1.0
+    assert np.array_equal(gpu_gemm(P, X), X[perm].astype(np.float32))
+    assert np.array_equal(gpu_gemm(Y, P), Y[:, np.argsort(perm)].astype(np.float32))
+
+
+def test_integer_bit_exact_multi_tile():
+    rng = np.random.default_rng(1)
+    A, B = inputs.integer_pair(rng, 1000, 1300, 2048)
+    C = gpu_gemm(A, B)
+    assert bit_exact(C, oracle.gemm_f32(A, B))
+
+
+def test_k_zero_and_empty_outputs():
+    A = torch.empty((5, 0), dtype=torch.float16, device="cuda")
+    B = torch.empty((0, 7), dtype=torch.float16, device="cuda")
+    C = torch.full((5, 7), 3.0, device="cuda")
+    tct.matmul(A, B, C)
+    torch.cuda.synchronize()
+    assert torch.all(C == 0)
+    C2 = torch.full((0, 7), 3.0, device="cuda")
+    tct.matmul(torch.empty((0, 4), dtype=torch.float16, device="cuda"),
+               torch.ones((4, 7), dtype=torch.float16, device="cuda"), C2)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M,N,K,pad_a,pad_b,pad_c,off", [
+    (300, 200, 150, 7, 5, 3, 0),
+    (129, 65, 33, 0, 0, 0, 1),
+    (256, 512, 128, 8, 16, 4, 0),
+    (17, 4097, 31, 1, 3, 9, 1),
+])
+def test_leading_dims_offsets_and_guard_zones(M, N, K, pad_a, pad_b, pad_c, off):
+    """lda > K, ldb > N, ldc > N, bases offset by one element (repack path), NaN guard zones
+    around C and in its gap columns: only the M x N block may change."""
+    rng = np.random.default_rng(17)
+    A, B = inputs.normal_pair(rng, M, N, K)
+    lda, ldb, ldc = K + pad_a, N + pad_b, N + pad_c
+    guard = 4096
+    a_buf = torch.zeros(off + M * lda + 8, dtype=torch.float16, device="cuda")
+    b_buf = torch.zeros(off + K * ldb + 8, dtype=torch.float16, device="cuda")
+    c_buf = torch.full((guard + M * ldc + guard,), float("nan"), dtype=torch.float32, device="cuda")
+    a_view = a_buf[off:off + M * lda].view(M, lda)
+    b_view = b_buf[off:off + K * ldb].view(K, ldb)
+    a_view[:, :K] = dev16(A)
+    b_view[:, :N] = dev16(B)
+    c_base = c_buf.data_ptr() + guard * 4
+    st = tct.gemm_f16_f32(a_view.data_ptr(), b_view.data_ptr(), c_base, M, N, K, lda, ldb, ldc,
+                          torch.cuda.current_stream().cuda_stream)
+    assert st == tct.GEMM_OK
+    torch.cuda.synchronize()
+    host = c_buf.cpu().numpy()
+    assert np.all(np.isnan(host[:guard])) and np.all(np.isnan(host[guard + M * ldc:]))
+    body = host[guard:guard + M * ldc].reshape(M, ldc)
+    assert np.all(np.isnan(body[:, N:]))
+    R = oracle.gemm_f32(A, B)
+    assert within_tol(body[:, :N], R, K)
+
+
+def test_repeat_runs_bitwise_identical():
+    rng = np.random.default_rng(21)
+    A, B = inputs.normal_pair(rng, 1000, 1100, 700)
+    dA, dB = dev16(A), dev16(B)
+    first = tct.matmul(dA, dB).cpu()
+    for _ in range(9):
+        again = tct.matmul(dA, dB).cpu()
+        assert torch.equal(first.view(torch.int32), again.view(torch.int32))
+
+
+@pytest.mark.parametrize("opts", [dict(group_m=1), dict(group_m=4), dict(group_m=16),
+                                  dict(tile_n=128), dict(tile_n=128, stages=4), dict(tile_n=256, stages=2),
+                                  dict(tile_n=256, stages=3), dict(max_ctas=7), dict(tile_n=128, group_m=3)])
+def test_variants_and_schedules_agree(opts):
+    """For a given tile width every pipeline depth, launch order and grid size gives the same
+    bits (the k order inside a tile never changes), and every variant passes the oracle."""
+    rng = np.random.default_rng(23)
+    M, N, K = 777, 1500, 515
+    A, B = inputs.normal_pair(rng, M, N, K)
+    dA, dB = dev16(A), dev16(B)
+    width = opts.get("tile_n") or tct.gemm_f16_f32_plan(M, N, K)["tile_n"]
+    ref = tct.matmul(dA, dB, tile_n=width)
+    C = tct.matmul(dA, dB, **opts)
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int32), ref.view(torch.int32))
+    assert within_tol(C.cpu().numpy(), oracle.gemm_f32(A, B), K)
+
+
+# ---- full-size workloads: sampled outputs -------------------------------------------------
+
+def _sample_positions(M, N, tile_m=128, tile_n=256, n_random=512, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {0, M - 1, min(M - 1, tile_m - 1), min(M - 1, tile_m), M // 2}
+    cols = {0, N - 1, min(N - 1, tile_n - 1), min(N - 1, tile_n), N // 2, min(N - 1, 127), min(N - 1, 128)}
+    rr = [r for r in rows for _ in cols]
+    cc = [c for _ in rows for c in cols]
+    rr += list(rng.integers(0, M, n_random))
+    cc += list(rng.integers(0, N, n_random))
+    return np.array(rr, np.int64), np.array(cc, np.int64)
+
+
+def check_sampled(A, B, C_dev, seed=0, extra_rows=()):
+    M, K = A.shape
+    N = B.shape[1]
+    rows, cols = _sample_positions(M, N, seed=seed)
+    _, want = oracle.gemm_elems(A, B, rows, cols)
+    got = C_dev[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
+    assert within_tol(got, want, K), f"worst ratio {worst_ratio(got, want, K):.3g}"
+    for r in extra_rows:
+        full = oracle.gemm_rows_f32(A, B, r, 1)[0]
+        assert within_tol(C_dev[r].cpu().numpy(), full, K)
+
+
+def test_square_4096_seed2_sampled():
+    (M, N, K), A, B = inputs.workload("square4096")[0]
+    C = tct.matmul(dev16(A), dev16(B))
+    torch.cuda.synchronize()
+    check_sampled(A, B, C, extra_rows=(0, 127, 128, 2047, 4095))
+
+
+def test_wave_sweep_seed3_sampled():
+    for (M, N, K), A, B in inputs.workload("wave_sweep"):
+        C = tct.matmul(dev16(A), dev16(B))
+        torch.cuda.synchronize()
+        check_sampled(A, B, C, extra_rows=(M - 1,))
+        del C
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2])
+def test_large_seed4_sampled(idx):
+    (M, N, K), A, B = inputs.workload(f"large:{idx}")[idx]
+    C = tct.matmul(dev16(A), dev16(B))
+    torch.cuda.synchronize()
+    check_sampled(A, B, C, extra_rows=(M - 1,))
