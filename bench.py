@@ -1,0 +1,419 @@
+"""Benchmark: FP16 -> FP32 GEMM throughput on GB300 through the library's C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
+
+A step is one C = A.B call on the 8192 x 8192 x 8192 workload (A, B drawn N(0,1) from
+seed 4, rounded to FP16).  The inputs (256 MiB) are larger than L2, so no flush is needed
+between steps.  Prints one JSON line (rank 0).  Under torchrun with N > 1 every rank runs
+its own replica on its own GPU (the problem does not need a collective); the time is the
+maximum over ranks and the value the aggregate throughput.
+
+--impl reference times the CPU oracle (the plain FP64-accumulating definition) on the
+host cores over a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = (8192, 8192, 8192)
+SEED = 4
+SECONDARY = (4096, 4096, 4096)
+METRIC = "FP16->FP32 GEMM TFLOP/s at 4096^3/8192^3; % of GB300 dense FP16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAK_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SOURCES = ("gemm_sm103a.cu", "ptx_sm103a.cuh", "tile_sched.h", "gemm_internal.h", "api.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target length of the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0.0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_PEAK_TFLOPS, None, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "tensor_core_tiled_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch():
+    """DRAM bytes (read + write) per launch of the main kernel from the committed ncu
+    summary, or None if absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "gemm_8192_dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background (timestamps in host time)."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self._stop = threading.Event()
+        self._thr = None
+
+    def _run(self):
+        try:
+            proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                     "--format=csv,noheader,nounits", "-lms", "50"],
+                                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        try:
+            for line in proc.stdout:
+                self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+                if self._stop.is_set():
+                    break
+        finally:
+            proc.terminate()
+            try:
+                proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                proc.kill()
+
+    def start(self):
+        self._thr = threading.Thread(target=self._run, daemon=True)
+        self._thr.start()
+        time.sleep(0.3)
+
+    def stop(self):
+        self._stop.set()
+        if self._thr:
+            self._thr.join(timeout=10)
+
+    def summary(self, t0, t1):
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not inside and self.samples:
+            nearest = min(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))
+            inside = [nearest[1]]
+            window = "nearest sample (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[1]) for s in inside if len(s) > 1 and num(s[1]) is not None]
+        mx = [num(s[2]) for s in inside if len(s) > 2 and num(s[2]) is not None]
+        pw = [num(s[3]) for s in inside if len(s) > 3 and num(s[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in inside:
+            for i, n in enumerate(names):
+                if len(s) > 5 + i and s[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons),
+                "samples": len(inside), "window": window}
+
+
+def make_inputs(M, N, K, seed):
+    import numpy as np
+    from tensor_core_tiled_gb300 import inputs
+    rng = np.random.default_rng(seed)
+    return inputs.normal_pair(rng, M, N, K)
+
+
+def _oracle_rate(A, B, rows=4):
+    """Rows per second of the oracle on this host (a short calibration run)."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.gemm_rows_f32(A, B, 0, rows)
+    return rows / max(time.perf_counter() - t0, 1e-9)
+
+
+def _oracle_sample(A, B, rows):
+    """Time the oracle on rows [0, rows) of the product; returns (seconds, flops)."""
+    import oracle
+    N, K = B.shape[1], A.shape[1]
+    t0 = time.perf_counter()
+    oracle.gemm_rows_f32(A, B, 0, rows)
+    return time.perf_counter() - t0, 2.0 * rows * N * K
+
+
+def _baseline_record(A, B, rows, secs, flops):
+    import oracle
+    M, K = A.shape
+    N = B.shape[1]
+    return {"value": flops / secs / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {M}x{N}x{K} seed-{SEED} product ({rows * N} outputs, "
+                      f"{flops / 1e9:.1f} GFLOP in {secs:.2f} s), FP64 accumulation, all host threads"}
+
+
+def cpu_baseline(A, B, target_seconds):
+    """The oracle as it stands, timed on a bounded sample: leading rows of the same product."""
+    rate = _oracle_rate(A, B)
+    rows = int(max(1, min(A.shape[0], rate * target_seconds)))
+    secs, flops = _oracle_sample(A, B, rows)
+    return _baseline_record(A, B, rows, secs, flops)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    M, N, K = WORKLOAD
+    A, B = make_inputs(M, N, K, SEED)
+    # each step: a bounded sample sized so that warm-up + steps take about cpu_seconds * 6
+    per_step = max(0.02, 6.0 * args.cpu_seconds / max(1, args.steps + args.warmup))
+    rate = _oracle_rate(A, B)
+    rows = int(max(1, min(M, rate * per_step)))
+    for _ in range(args.warmup):
+        _oracle_sample(A, B, rows)
+    secs = flops = 0.0
+    for _ in range(args.steps):
+        s, f = _oracle_sample(A, B, rows)
+        secs += s
+        flops += f
+    value = flops / secs / 1e12
+    rec = _baseline_record(A, B, rows, secs / args.steps, flops / args.steps)
+    rec["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": f"gemm_f16_f32 {M}x{N}x{K}, A and B N(0,1) FP16 "
+                                                        f"from seed {SEED}, FP32 output",
+                                            "M": M, "N": N, "K": K},
+            "cpu_baseline": rec,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import tensor_core_tiled_gb300 as tct
+    from tensor_core_tiled_gb300 import build as lib_build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        lib_build.build()
+    if dist:
+        dist.barrier()
+    tct.load()
+
+    M, N, K = WORKLOAD
+    A16, B16 = make_inputs(M, N, K, SEED)
+    hA = torch.from_numpy(A16.view(np.int16)).view(torch.float16).pin_memory()
+    hB = torch.from_numpy(B16.view(np.int16)).view(torch.float16).pin_memory()
+    dA = hA.to(dev)
+    dB = hB.to(dev)
+    dC = torch.empty((M, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    flops = 2.0 * M * N * K
+
+    def launch():
+        st = tct.gemm_f16_f32(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), M, N, K, K, N, N, sp)
+        if st:
+            raise tct.GemmError(st, "gemm_f16_f32")
+
+    for _ in range(max(3, args.warmup)):
+        launch()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    # ---- timed region: K launches, one event pair per launch on the launching stream
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for e0, e1 in evs:
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    if dist:
+        dist.barrier()
+    total_ms = g0.elapsed_time(g1)
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+
+    # max over ranks of the timed region
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+
+    # ---- end to end through the public call with host buffers: H2D of A and B from pinned
+    # memory, the GEMM, D2H of C into pinned memory, all inside the timed region.
+    hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        launch()
+        hC.copy_(dC, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = x0.elapsed_time(x1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    # ---- secondary workload: 4096^3 (inputs fit in L2, so L2 is flushed before each launch)
+    m2, n2, k2 = SECONDARY
+    sA, sB = make_inputs(m2, n2, k2, 2)
+    sA = torch.from_numpy(sA.view(np.int16)).view(torch.float16).to(dev)
+    sB = torch.from_numpy(sB.view(np.int16)).view(torch.float16).to(dev)
+    sC = torch.empty((m2, n2), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def launch2():
+        st = tct.gemm_f16_f32(sA.data_ptr(), sB.data_ptr(), sC.data_ptr(), m2, n2, k2, k2, n2, n2, sp)
+        if st:
+            raise tct.GemmError(st, "gemm_f16_f32")
+
+    for _ in range(5):
+        launch2()
+    sec = []
+    n_sec = max(5, min(args.steps, 100))
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_sec)]
+    for a, b in pairs:
+        flush.fill_(1.0)
+        a.record(stream)
+        launch2()
+        b.record(stream)
+    torch.cuda.synchronize()
+    sec = [a.elapsed_time(b) for a, b in pairs]
+    sec_ms = statistics.mean(sec)
+    sec_tflops = 2.0 * m2 * n2 * k2 / (sec_ms * 1e-3) / 1e12
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+
+    peak, peak_sustained, peak_src = peaks()
+    mean_launch = statistics.mean(launch_ms)
+    achieved = flops / (mean_launch * 1e-3) / 1e12
+    plan = tct.gemm_f16_f32_plan(M, N, K)
+    plan2 = tct.gemm_f16_f32_plan(m2, n2, k2)
+
+    line = None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": f"gemm_f16_f32 {M}x{N}x{K}, A and B N(0,1) FP16 from seed {SEED}, "
+                                   f"FP32 accumulate and output",
+                       "M": M, "N": N, "K": K, "accumulate": "f32", "parallelism": f"replicas x{world}",
+                       "l2": "inputs (256 MiB) larger than L2; no flush",
+                       "tile": [plan["tile_m"], plan["tile_n"], plan["tile_k"]], "stages": plan["stages"],
+                       "group_m": plan["group_m"], "grid": plan["grid"]},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak, "traffic": traffic_per_launch(),
+                         "peak_source": f"{peak_src}: bf16 burst (fp16 nominal rate equal)",
+                         "peak_sustained": peak_sustained,
+                         "frac_of_sustained": (achieved / peak_sustained) if peak_sustained else None,
+                         "kernel_ms_mean": mean_launch, "kernel_ms_min": min(launch_ms)},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(dA.numel() * 2 + dB.numel() * 2),
+                    "d2h_bytes_per_step": int(dC.numel() * 4), "steps": e2e_steps, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "secondary": {"workload": f"gemm_f16_f32 {m2}x{n2}x{k2}, seed 2, L2 flushed before each launch",
+                          "value": sec_tflops, "unit": UNIT, "frac": sec_tflops / peak,
+                          "ms_mean": sec_ms, "launches": n_sec,
+                          "tile": [plan2["tile_m"], plan2["tile_n"], plan2["tile_k"]], "waves": plan2["waves"]},
+            "kernel_hash": kernel_hash(),
+        }
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(A16, B16, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
