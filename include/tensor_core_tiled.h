@@ -122,6 +122,31 @@ TCT_API gemm_status gemm_wave_model(int64_t M, int64_t N, int64_t tile_m, int64_
                             int64_t *tiles, int64_t *waves, double *utilization);
 
 /*
+ * gemm_f16_f32_noalloc -- gemm_f16_f32 for callers that cannot allocate device memory.
+ * The lecture pages have no counterpart to this entry point; it exists for callers whose
+ * device memory is owned by another allocator (a framework's caching pool, a server that
+ * reserves the whole GPU at start-up), where a new driver allocation mid-run can fail or
+ * stall, and for callers whose interface forbids using the CUDA allocator (an operator or
+ * plugin API that provides only the input and output buffers).
+ *   Arguments, layouts and results are those of gemm_f16_f32; the caller still provides A,
+ *   B and C.  The call makes no cudaMalloc/cudaFree or other allocating call.  The only
+ *   scratch it can need -- the aligned copy of A and/or B made when lda or ldb is not a
+ *   multiple of 8 or a base is not 16-byte aligned -- lives in one library-owned device
+ *   array of GEMM_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library keeps
+ *   until the process exits.  GEMM_ERR_INVALID_ARG is returned, before any work is
+ *   enqueued, when the repacked operands would need more than that (M * roundup(K, 8) * 2
+ *   bytes for A plus K * roundup(N, 8) * 2 bytes for B, each rounded up to 256).
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *   with that device current; make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents (nothing in it
+ *   needs to start at zero): calls that may run at the same time on the GPU (different
+ *   streams without ordering between them) race on it and must be serialised by the caller.
+ */
+#define GEMM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+TCT_API gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float *C, int64_t M, int64_t N,
+                                         int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void *stream);
+
+/*
  * Reads and clears the device error word of the current device: GEMM_OK, or
  * GEMM_ERR_DEVICE_TIMEOUT if a kernel launched since the last read gave up on a pipeline
  * wait (its output is then incomplete).  Synchronises the current device first.

@@ -22,6 +22,7 @@ GEMM_ERR_DEVICE_TIMEOUT = 4
 EXPORTED = (
     "gemm_f16_f32",
     "gemm_f16_f32_ex",
+    "gemm_f16_f32_noalloc",
     "gemm_f16_f32_plan",
     "gemm_tile_coord",
     "gemm_wave_model",
@@ -64,6 +65,8 @@ def load():
     i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
     lib.gemm_f16_f32.restype = ctypes.c_int
     lib.gemm_f16_f32.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
+    lib.gemm_f16_f32_noalloc.restype = ctypes.c_int
+    lib.gemm_f16_f32_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
     lib.gemm_f16_f32_ex.restype = ctypes.c_int
     lib.gemm_f16_f32_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, ctypes.POINTER(GemmOptions)]
     lib.gemm_f16_f32_plan.restype = ctypes.c_int
@@ -104,6 +107,14 @@ def _options(group_m=0, tile_n=0, stages=0, max_ctas=0, timeout_ms=0):
 def gemm_f16_f32(A, B, C, M, N, K, lda, ldb, ldc, stream=0):
     """Raw C-ABI call with integer device pointers; returns the status code."""
     return load().gemm_f16_f32(A, B, C, M, N, K, lda, ldb, ldc, stream or None)
+
+
+def gemm_f16_f32_noalloc(A, B, C, M, N, K, lda, ldb, ldc, stream=0):
+    """Raw C-ABI call of the allocation-free entry point (library-owned scratch array)."""
+    return load().gemm_f16_f32_noalloc(A, B, C, M, N, K, lda, ldb, ldc, stream or None)
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 def gemm_f16_f32_ex(A, B, C, M, N, K, lda, ldb, ldc, stream=0, **options):

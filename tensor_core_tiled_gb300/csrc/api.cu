@@ -330,3 +330,103 @@ const char *gemm_status_string(int status)
 const char *gemm_version(void) { return "tensor_core_tiled 0.1 sm_103a"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free variant
+//
+// Some callers cannot call cudaMalloc: their device memory belongs to another allocator (a
+// framework's caching pool, or a server that reserves the whole GPU when it starts), so a
+// fresh driver allocation in the middle of a run can fail or stall, or their calling
+// context (an operator/plugin interface that hands over only input and output buffers)
+// forbids touching the CUDA allocator.  gemm_f16_f32_noalloc serves them: the only
+// scratch the GEMM path can need -- the 16-byte-aligned copy of operands whose rows are
+// not aligned for TMA -- lives in this fixed, library-owned device array instead of a
+// cudaMallocAsync block.
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device.
+// In host code the array's name is only a host-side stand-in, so kernels must be given
+// this address, never the symbol itself.
+gemm_status noalloc_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GEMM_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float *C, int64_t M, int64_t N,
+                                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void *stream)
+{
+    gemm_status st = check_args(A, B, C, M, N, K, lda, ldb, ldc);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    // Scratch needed for the repacked operands, checked against the fixed array first.
+    const bool pack_a = K > 0 && !tma_ok(A, lda);
+    const bool pack_b = K > 0 && !tma_ok(B, ldb);
+    const int64_t lda_p = round_up(K, 8), ldb_p = round_up(N, 8);
+    const int64_t a_bytes = pack_a ? round_up(M * lda_p * 2, 256) : 0;
+    const int64_t b_bytes = pack_b ? round_up(K * ldb_p * 2, 256) : 0;
+    if (a_bytes + b_bytes > static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_BYTES)) return GEMM_ERR_INVALID_ARG;
+
+    DeviceInfo dev;
+    st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return to_status(tct::launch_fill_zero(C, ldc, M, N, dev.sms, s));
+
+    gemm_plan pl;
+    st = make_plan(M, N, K, lda, ldb, dev.sms, nullptr, A, B, &pl);
+    if (st != GEMM_OK) return st;
+
+    const void *a_use = A, *b_use = B;
+    int64_t lda_use = lda, ldb_use = ldb;
+    if (pack_a || pack_b) {
+        void *scratch = nullptr;
+        st = noalloc_scratch(&scratch);
+        if (st != GEMM_OK) return st;
+        uint8_t *w = static_cast<uint8_t *>(scratch);
+        // Every element the GEMM reads is written here first; nothing needs clearing.
+        if (pack_a) {
+            if (tct::launch_pack(A, lda, w, lda_p, M, K, dev.sms, s) != cudaSuccess) return GEMM_ERR_CUDA;
+            a_use = w;
+            lda_use = lda_p;
+        }
+        if (pack_b) {
+            if (tct::launch_pack(B, ldb, w + a_bytes, ldb_p, K, N, dev.sms, s) != cudaSuccess) return GEMM_ERR_CUDA;
+            b_use = w + a_bytes;
+            ldb_use = ldb_p;
+        }
+    }
+
+    CUtensorMap ta, tb;
+    st = encode_fp16_2d(&ta, a_use, M, K, lda_use, kTileM);
+    if (st == GEMM_OK) st = encode_fp16_2d(&tb, b_use, K, N, ldb_use, kTileK);
+    if (st != GEMM_OK) return st;
+    tct::KernelParams p;
+    p.C = C;
+    p.ldc = ldc;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.num_m = static_cast<int32_t>(tct::ceil_div(M, kTileM));
+    p.num_n = static_cast<int32_t>(tct::ceil_div(N, pl.tile_n));
+    p.num_kb = static_cast<int32_t>(tct::ceil_div(K, kTileK));
+    p.num_tiles = static_cast<int32_t>(pl.tiles);
+    p.group_m = pl.group_m;
+    p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 1 : 0;
+    p.timeout_ns = static_cast<uint64_t>(kDefaultTimeoutMs) * 1000000ull;
+    return to_status(tct::launch_gemm(ta, tb, p, pl.tile_n, pl.stages, pl.grid, s));
+}
