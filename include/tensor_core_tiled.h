@@ -66,10 +66,11 @@ TCT_API gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t
  *   group_m   : output tile rows per launch-order group ("06_triton_style.py",
  *               matmul_kernel and demo 2: GROUP_M program order for L2 reuse); 1 gives
  *               row-major tile order.  Range 1..256.
- *   tile_n    : output tile width in columns: 128 or 256 (the tile height is 128).
- *   stages    : shared-memory pipeline depth (2..the maximum that fits for tile_n).
- *   max_ctas  : cap on the persistent grid (default: one CTA per SM).
+ *   tile_n    : output tile width in columns: 128 or 256.
+ *   stages    : shared-memory pipeline depth (a compiled depth for the chosen tile).
+ *   max_ctas  : cap on the persistent grid in CTAs (default: every co-resident CTA).
  *   timeout_ms: limit on any single device pipeline wait (default 2000 ms).
+ *   cta_group : 1 = one CTA per 128-row tile, 2 = a CTA pair per 256-row tile.
  */
 typedef struct gemm_options {
     int32_t group_m;
@@ -77,7 +78,8 @@ typedef struct gemm_options {
     int32_t stages;
     int32_t max_ctas;
     int32_t timeout_ms;
-    int32_t reserved[3]; /* must be zero */
+    int32_t cta_group;
+    int32_t reserved[2]; /* must be zero */
 } gemm_options;
 
 /* gemm_f16_f32 with explicit tuning options (opt may be NULL = all defaults). */
@@ -99,6 +101,7 @@ typedef struct gemm_plan {
     double wave_efficiency;         /* M*N / (waves * grid * tile_m * tile_n)          */
     int32_t smem_bytes;             /* dynamic shared memory per CTA                  */
     int32_t pack_a, pack_b;         /* 1 if the operand would be repacked first       */
+    int32_t cta_group;              /* CTAs sharing one tile (1 or 2)                 */
 } gemm_plan;
 
 TCT_API gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,

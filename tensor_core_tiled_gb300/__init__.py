@@ -40,15 +40,16 @@ class GemmError(RuntimeError):
 
 class GemmOptions(ctypes.Structure):
     _fields_ = [("group_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 3)]
+                ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32), ("cta_group", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 class GemmPlan(ctypes.Structure):
     _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("group_m", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("tiles", ctypes.c_int64), ("waves", ctypes.c_int64), ("wave_efficiency", ctypes.c_double),
-                ("smem_bytes", ctypes.c_int32), ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32)]
+                ("smem_bytes", ctypes.c_int32), ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32),
+                ("cta_group", ctypes.c_int32)]
 
 
 _lib = None
@@ -98,9 +99,10 @@ def version():
     return load().gemm_version().decode()
 
 
-def _options(group_m=0, tile_n=0, stages=0, max_ctas=0, timeout_ms=0):
+def _options(group_m=0, tile_n=0, stages=0, max_ctas=0, timeout_ms=0, cta_group=0):
     o = GemmOptions()
     o.group_m, o.tile_n, o.stages, o.max_ctas, o.timeout_ms = group_m, tile_n, stages, max_ctas, timeout_ms
+    o.cta_group = cta_group
     return o
 
 
@@ -118,7 +120,7 @@ NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 def gemm_f16_f32_ex(A, B, C, M, N, K, lda, ldb, ldc, stream=0, **options):
-    """Raw C-ABI call with tuning options (group_m, tile_n, stages, max_ctas, timeout_ms)."""
+    """Raw C-ABI call with tuning options (group_m, tile_n, stages, max_ctas, timeout_ms, cta_group)."""
     opt = _options(**options)
     return load().gemm_f16_f32_ex(A, B, C, M, N, K, lda, ldb, ldc, stream or None, ctypes.byref(opt))
 

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "gemm_internal.h"
@@ -21,15 +22,30 @@ constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 constexpr int kDefaultGroupM = 8;
 constexpr int kDefaultTimeoutMs = 2000;
 constexpr int kMaxDevices = 64;
-// Relative per-tile tensor throughput used by the tile-width choice: a 128-wide tile
-// reads as many A bytes per MMA as a 256-wide one but does half the work with them.
-constexpr double kNarrowTileRate = 0.90;
+
+// Kernel variants the planner chooses between, with the relative per-tile throughput
+// each reached on GB300 with every SM busy (8192^3 and 4096^3, same clocks): the pair
+// 256 x 256 tile moves the fewest operand bytes into shared memory per FLOP; the
+// 128-column tiles are much slower per tile and only pay off when they fill SMs that a
+// wider tile would leave idle (skinny M or N).  The planner weighs these against wave
+// quantisation.
+struct Candidate {
+    int cta_group, tile_n, stages;
+    double rate;
+};
+constexpr Candidate kCandidates[] = {
+    {2, 256, 6, 1.00},
+    {1, 256, 4, 0.85},
+    {1, 128, 6, 0.70},
+    {2, 128, 8, 0.57},
+};
 
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int major = 0;
     int minor = 0;
+    int pair_clusters = 0;  // co-resident CTA pairs of the pair kernels (0 = not queried)
 };
 
 std::mutex g_mu;
@@ -95,14 +111,21 @@ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 gemm_status check_options(const gemm_options *opt)
 {
     if (!opt) return GEMM_OK;
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < 2; ++i)
         if (opt->reserved[i] != 0) return GEMM_ERR_INVALID_ARG;
     if (opt->group_m < 0 || opt->group_m > 256) return GEMM_ERR_INVALID_ARG;
     if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return GEMM_ERR_INVALID_ARG;
+    if (opt->cta_group < 0 || opt->cta_group > 2) return GEMM_ERR_INVALID_ARG;
     if (opt->stages < 0 || opt->max_ctas < 0 || opt->timeout_ms < 0) return GEMM_ERR_INVALID_ARG;
     if (opt->stages != 0) {
-        const int tn = opt->tile_n ? opt->tile_n : 256;
-        if (tct::variant_smem_bytes(tn, opt->stages) < 0) return GEMM_ERR_INVALID_ARG;
+        // some compiled variant must match every field that is set
+        bool any = false;
+        for (int cg = 1; cg <= 2; ++cg)
+            for (int tn = 128; tn <= 256; tn += 128) {
+                if ((opt->cta_group && opt->cta_group != cg) || (opt->tile_n && opt->tile_n != tn)) continue;
+                if (tct::variant_smem_bytes(cg, tn, opt->stages) > 0) any = true;
+            }
+        if (!any) return GEMM_ERR_INVALID_ARG;
     }
     return GEMM_OK;
 }
@@ -133,52 +156,79 @@ double wave_util(int64_t M, int64_t N, int64_t tm, int64_t tn, int64_t slots, in
     return static_cast<double>(tiles) / static_cast<double>(waves * slots);
 }
 
-// Fraction of the SM-time of the launch spent on useful output elements.
-double useful_fraction(int64_t M, int64_t N, int64_t tn, int64_t sms)
+// Fraction of the launch's tile slots (waves x slots x tile area) holding useful outputs.
+double useful_fraction(int64_t M, int64_t N, int64_t tm, int64_t tn, int64_t slots)
 {
     int64_t tiles = 0, waves = 0;
-    wave_util(M, N, kTileM, tn, sms, &tiles, &waves);
+    wave_util(M, N, tm, tn, slots, &tiles, &waves);
     return static_cast<double>(M) * static_cast<double>(N) /
-           (static_cast<double>(waves) * sms * kTileM * tn);
+           (static_cast<double>(waves) * slots * tm * tn);
 }
 
-gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int sms,
+// Wave-quantisation-aware choice among the compiled variants ("02_gpu_execution_model.py",
+// part 5: tiles, waves = ceil(tiles / slots), utilisation), weighted by each variant's rate.
+// pair_slots: co-resident CTA pairs (from the device, or sms / 2 when planning offline).
+gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int sms, int pair_slots,
                       const gemm_options *opt, const void *A, const void *B, gemm_plan *pl)
 {
     std::memset(pl, 0, sizeof(*pl));
-    int tile_n = opt && opt->tile_n ? opt->tile_n : 0;
-    if (!tile_n) {
-        // Wave-quantisation-aware width ("02_gpu_execution_model.py", part 5): compare the
-        // useful share of SM-time of both widths, weighting the narrow tile's lower rate.
-        const double u256 = useful_fraction(M, N, 256, sms);
-        const double u128 = useful_fraction(M, N, 128, sms) * kNarrowTileRate;
-        tile_n = (u128 > u256) ? 128 : 256;
+    const int want_cg = opt ? opt->cta_group : 0;
+    const int want_tn = opt ? opt->tile_n : 0;
+    const int want_st = opt ? opt->stages : 0;
+    int64_t cap = opt && opt->max_ctas > 0 ? opt->max_ctas : 0;
+    const Candidate *best = nullptr;
+    double best_score = -1.0;
+    for (const Candidate &c : kCandidates) {
+        if ((want_cg && want_cg != c.cta_group) || (want_tn && want_tn != c.tile_n)) continue;
+        if (want_st && tct::variant_smem_bytes(c.cta_group, c.tile_n, want_st) < 0) continue;
+        int64_t slots = c.cta_group == 2 ? pair_slots : sms;
+        if (cap > 0) slots = std::min<int64_t>(slots, std::max<int64_t>(1, cap / c.cta_group));
+        if (slots < 1) continue;
+        const double score = useful_fraction(M, N, 128 * c.cta_group, c.tile_n, slots) * c.rate;
+        if (score > best_score) {
+            best_score = score;
+            best = &c;
+        }
     }
-    int stages = opt && opt->stages ? opt->stages : (tile_n == 256 ? 4 : 6);
-    const int smem = tct::variant_smem_bytes(tile_n, stages);
+    if (!best) return GEMM_ERR_INVALID_ARG;
+    const int cg = best->cta_group, tile_n = best->tile_n;
+    const int stages = want_st ? want_st : best->stages;
+    const int smem = tct::variant_smem_bytes(cg, tile_n, stages);
     if (smem < 0) return GEMM_ERR_INVALID_ARG;
-    const int group_m = opt && opt->group_m ? opt->group_m : kDefaultGroupM;
-    int64_t tiles = 0, waves = 0;
-    const int64_t num_m = tct::ceil_div(M, kTileM), num_n = tct::ceil_div(N, tile_n);
-    tiles = num_m * num_n;
-    int64_t grid = tiles < sms ? tiles : sms;
-    if (opt && opt->max_ctas > 0 && grid > opt->max_ctas) grid = opt->max_ctas;
-    if (grid < 1) grid = 1;
-    waves = tct::ceil_div(tiles, grid);
-    pl->tile_m = kTileM;
+    const int tile_m = kTileM * cg;
+    const int64_t tiles = tct::ceil_div(M, tile_m) * tct::ceil_div(N, tile_n);
+    int64_t units = cg == 2 ? pair_slots : sms;  // persistent CTAs (or pairs)
+    if (cap > 0) units = std::min<int64_t>(units, std::max<int64_t>(1, cap / cg));
+    units = std::max<int64_t>(1, std::min<int64_t>(units, tiles));
+    const int64_t waves = tct::ceil_div(tiles, units);
+    pl->tile_m = tile_m;
     pl->tile_n = tile_n;
     pl->tile_k = kTileK;
     pl->stages = stages;
-    pl->group_m = group_m;
-    pl->grid = static_cast<int32_t>(grid);
+    pl->group_m = opt && opt->group_m ? opt->group_m : kDefaultGroupM;
+    pl->grid = static_cast<int32_t>(units * cg);
     pl->tiles = tiles;
     pl->waves = waves;
-    pl->wave_efficiency = tiles ? static_cast<double>(M) * N / (static_cast<double>(waves) * grid * kTileM * tile_n)
-                                : 0.0;
+    pl->wave_efficiency = static_cast<double>(M) * N / (static_cast<double>(waves) * units * tile_m * tile_n);
     pl->smem_bytes = smem;
     pl->pack_a = (K > 0 && !tma_ok(A, lda)) ? 1 : 0;
     pl->pack_b = (K > 0 && !tma_ok(B, ldb)) ? 1 : 0;
+    pl->cta_group = cg;
     return GEMM_OK;
+}
+
+// Co-resident CTA pairs on the current device for the pair kernels (queried once).
+int device_pair_slots(DeviceInfo *dev)
+{
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return dev->sms / 2;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_dev[d].pair_clusters == 0) {
+        const int n = tct::variant_max_clusters(2, 256, 6);
+        g_dev[d].pair_clusters = n > 0 ? n : std::max(1, g_dev[d].sms / 2);
+    }
+    dev->pair_clusters = g_dev[d].pair_clusters;
+    return dev->pair_clusters;
 }
 
 gemm_status to_status(cudaError_t e) { return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA; }
@@ -202,7 +252,7 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
     if (K == 0) return to_status(tct::launch_fill_zero(C, ldc, M, N, dev.sms, s));
 
     gemm_plan pl;
-    st = make_plan(M, N, K, lda, ldb, dev.sms, opt, A, B, &pl);
+    st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), opt, A, B, &pl);
     if (st != GEMM_OK) return st;
 
     // Operands whose rows do not start on 16-byte boundaries are copied first (TMA needs
@@ -243,7 +293,7 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
         p.M = static_cast<int32_t>(M);
         p.N = static_cast<int32_t>(N);
         p.K = static_cast<int32_t>(K);
-        p.num_m = static_cast<int32_t>(tct::ceil_div(M, kTileM));
+        p.num_m = static_cast<int32_t>(tct::ceil_div(M, pl.tile_m));
         p.num_n = static_cast<int32_t>(tct::ceil_div(N, pl.tile_n));
         p.num_kb = static_cast<int32_t>(tct::ceil_div(K, kTileK));
         p.num_tiles = static_cast<int32_t>(pl.tiles);
@@ -251,7 +301,7 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
         p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 1 : 0;
         const int tmo = opt && opt->timeout_ms ? opt->timeout_ms : kDefaultTimeoutMs;
         p.timeout_ns = static_cast<uint64_t>(tmo) * 1000000ull;
-        st = to_status(tct::launch_gemm(ta, tb, p, pl.tile_n, pl.stages, pl.grid, s));
+        st = to_status(tct::launch_gemm(ta, tb, p, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
     }
     if (ws) {
         if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
@@ -273,16 +323,17 @@ gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int6
         return GEMM_ERR_INVALID_ARG;
     gemm_status st = check_options(opt);
     if (st != GEMM_OK) return st;
-    int sms = num_sms;
+    int sms = num_sms, pairs = num_sms / 2;
     if (sms <= 0) {
         DeviceInfo dev;
         st = device_info(&dev);
         if (st != GEMM_OK) return st;
         sms = dev.sms;
+        pairs = device_pair_slots(&dev);
     }
     // Alignment of the base pointers is unknown here: assume 16-byte aligned bases.
     const void *aligned = reinterpret_cast<const void *>(uintptr_t{256});
-    return make_plan(M, N, K, lda, ldb, sms, opt, aligned, aligned, out);
+    return make_plan(M, N, K, lda, ldb, sms, pairs, opt, aligned, aligned, out);
 }
 
 gemm_status gemm_tile_coord(int64_t t, int64_t num_m, int64_t num_n, int32_t group_m, int64_t *tile_row,
@@ -388,7 +439,7 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
     if (K == 0) return to_status(tct::launch_fill_zero(C, ldc, M, N, dev.sms, s));
 
     gemm_plan pl;
-    st = make_plan(M, N, K, lda, ldb, dev.sms, nullptr, A, B, &pl);
+    st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), nullptr, A, B, &pl);
     if (st != GEMM_OK) return st;
 
     const void *a_use = A, *b_use = B;
@@ -421,12 +472,12 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
-    p.num_m = static_cast<int32_t>(tct::ceil_div(M, kTileM));
+    p.num_m = static_cast<int32_t>(tct::ceil_div(M, pl.tile_m));
     p.num_n = static_cast<int32_t>(tct::ceil_div(N, pl.tile_n));
     p.num_kb = static_cast<int32_t>(tct::ceil_div(K, kTileK));
     p.num_tiles = static_cast<int32_t>(pl.tiles);
     p.group_m = pl.group_m;
     p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 1 : 0;
     p.timeout_ns = static_cast<uint64_t>(kDefaultTimeoutMs) * 1000000ull;
-    return to_status(tct::launch_gemm(ta, tb, p, pl.tile_n, pl.stages, pl.grid, s));
+    return to_status(tct::launch_gemm(ta, tb, p, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
 }

@@ -22,19 +22,30 @@ struct KernelParams {
     uint64_t timeout_ns;
 };
 
-// Compiled (tile_n, stages) variants of the main kernel.  Shared memory per stage is
-// 16 KB (A) + tile_n * 128 B (B); the epilogue staging takes 16 KB more.
+// Compiled (cta_group, tile_n, stages) variants of the main kernel.  cta_group 1: 128 x
+// tile_n tiles, one CTA each; per stage 16 KB of A + tile_n * 128 B of B.  cta_group 2:
+// 256 x tile_n tiles on a CTA pair; per CTA and stage 16 KB of A + tile_n * 64 B of B.
+// The epilogue staging takes 16 KB more.
 #define TCT_VARIANTS(X) \
-    X(256, 2)           \
-    X(256, 3)           \
-    X(256, 4)           \
-    X(128, 4)           \
-    X(128, 6)
+    X(1, 256, 2)        \
+    X(1, 256, 3)        \
+    X(1, 256, 4)        \
+    X(1, 128, 4)        \
+    X(1, 128, 6)        \
+    X(2, 256, 3)        \
+    X(2, 256, 4)        \
+    X(2, 256, 5)        \
+    X(2, 256, 6)        \
+    X(2, 128, 6)        \
+    X(2, 128, 8)
 
-int variant_smem_bytes(int tile_n, int stages);
+int variant_smem_bytes(int cta_group, int tile_n, int stages);
 
-cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const KernelParams &p, int tile_n,
-                        int stages, int grid, cudaStream_t stream);
+// Co-resident clusters of the variant on the current device (-1 if the query fails).
+int variant_max_clusters(int cta_group, int tile_n, int stages);
+
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const KernelParams &p, int cta_group,
+                        int tile_n, int stages, int grid, cudaStream_t stream);
 
 cudaError_t launch_pack(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows,
                         int64_t cols, int num_sms, cudaStream_t stream);

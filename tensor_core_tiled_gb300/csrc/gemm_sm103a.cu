@@ -6,8 +6,12 @@
 // 5th-generation tensor core instead of the mma.sync/ldmatrix and Triton realisations the
 // pages describe:
 //
-//   * Block tiling with a K loop: each CTA owns 128 x BN output tiles and walks K in
+//   * Block tiling with a K loop: each tile is (128 * CG) x BN outputs, K is walked in
 //     64-element blocks ("04_tensor_cores.py", tc_matmul: BM x BN blocks, a BK loop).
+//     CG = 1: one CTA per tile.  CG = 2: a CTA pair (cluster of 2) shares one 256-row tile;
+//     each CTA loads its own 128 rows of A and half of the tile's B columns, the even CTA
+//     issues M = 256 MMAs that read both CTAs' shared memory, and each CTA's TMEM receives
+//     its 128 rows -- half the B bytes per SM of the CG = 1 form for the same work.
 //   * Operand tiles reach shared memory through TMA with the 128-byte swizzle, the
 //     hardware form of the XOR swizzle of demo 2 (16-byte chunk index XOR row mod 8), so
 //     tensor-core reads of any 8 rows hit distinct banks.  A (K-major) and B (row-major,
@@ -19,8 +23,8 @@
 //     compute): warp 0 issues TMA, warp 1 issues tcgen05.mma from one thread, warps 2..5
 //     drain the FP32 accumulators from TMEM.  Two TMEM accumulator buffers let the
 //     epilogue of one tile overlap the main loop of the next.
-//   * A persistent grid of at most one CTA per SM walks the tiles in GROUP_M launch order
-//     ("06_triton_style.py", matmul_kernel / demo 2) for L2 reuse.
+//   * A persistent grid walks the tiles in GROUP_M launch order ("06_triton_style.py",
+//     matmul_kernel / demo 2) for L2 reuse.
 //   * Ragged shapes ("06_triton_style.py", matmul_kernel masks): TMA fills out-of-range
 //     operand elements with zeros (the masked load with other = 0) and the epilogue
 //     predicates every store on row < M and column < N (the masked store).
@@ -39,24 +43,28 @@ namespace tct {
 
 __device__ unsigned int g_error_word;
 
-template <int BN_, int STAGES_>
+template <int CG_, int BN_, int STAGES_>
 struct Cfg {
-    static constexpr int BM = 128;
-    static constexpr int BN = BN_;
-    static constexpr int BK = 64;  // 64 FP16 = 128 bytes = one swizzle row
+    static constexpr int CG = CG_;            // CTAs per tile (1 or 2)
+    static constexpr int BM = 128;            // tile rows held by one CTA
+    static constexpr int BN = BN_;            // tile columns (the MMA's N)
+    static constexpr int BN_CTA = BN_ / CG_;  // B columns loaded by one CTA
+    static constexpr int BK = 64;             // 64 FP16 = 128 bytes = one swizzle row
     static constexpr int STAGES = STAGES_;
-    static constexpr int UMMA_K = 16;  // K of one kind::f16 MMA
+    static constexpr int UMMA_K = 16;         // K of one kind::f16 MMA
     static constexpr int A_STAGE = BM * BK * 2;
     static constexpr int B_SUB = BK * 64 * 2;  // one 64-column TMA box of B
-    static constexpr int B_STAGE = BK * BN * 2;
-    static constexpr int STAGE_TX = A_STAGE + B_STAGE;
+    static constexpr int B_BOXES = BN_CTA / 64;
+    static constexpr int B_STAGE = BK * BN_CTA * 2;
+    static constexpr int STAGE_TX = CG * (A_STAGE + B_STAGE);  // bytes counted on one full barrier
     static constexpr int EPI_WARPS = 4;
     static constexpr int EPI_BYTES = EPI_WARPS * 32 * 32 * 4;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM_BYTES =
         1024 + STAGES * (A_STAGE + B_STAGE) + EPI_BYTES + NUM_BARS * 8 + 16;
-    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256 in steps of 64");
+    static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per tile");
+    static_assert(BN_CTA % 64 == 0 && BN <= 256, "B columns per CTA must be whole 64-column boxes");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory");
 };
@@ -66,6 +74,7 @@ enum WaitSite : unsigned {
     SITE_MMA_FULL = 2,
     SITE_MMA_TMEM_EMPTY = 3,
     SITE_EPI_TMEM_FULL = 4,
+    SITE_PRODUCER_TAIL = 5,
 };
 
 __device__ __forceinline__ void record_timeout(volatile int *abort_flag, unsigned site)
@@ -75,15 +84,25 @@ __device__ __forceinline__ void record_timeout(volatile int *abort_flag, unsigne
     __threadfence_block();
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
+template <bool kCluster>
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
+{
+    if constexpr (kCluster)
+        return mbar_try_wait_cluster(bar, parity);
+    else
+        return mbar_try_wait(bar, parity);
+}
+
+// Bounded wait that also gives up as soon as another role of this CTA has aborted.
+template <bool kCluster>
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                               volatile int *abort_flag, unsigned site)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait<kCluster>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     uint32_t spins = 0;
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_wait<kCluster>(bar, parity)) return true;
         if ((++spins & 15u) == 0u) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > limit_ns) {
@@ -94,12 +113,63 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
     }
 }
 
-template <int BN, int STAGES>
+// One accumulator buffer (this warp's 32 TMEM lanes x BN columns) to global memory.
+// `release` is called by lane 0 once every column has been read from TMEM.
+template <int BN, typename Release>
+__device__ __forceinline__ void store_accumulator(uint32_t t_row, int64_t row_base, int64_t col_base,
+                                                  const KernelParams &p, float *stage, int lane, bool vec,
+                                                  Release release)
+{
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + ch * 32, r);
+        tmem_wait_ld();
+        if (ch == BN / 32 - 1) {
+            // Accumulator fully read: hand the buffer back to the MMA issuer.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release();
+        }
+        // Row `lane` of this 32 x 32 block into the staging buffer, 16-byte chunks
+        // XOR-swizzled by row so the transposed read below is conflict-free.
+        float4 *srow = reinterpret_cast<float4 *>(stage + lane * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            srow[j ^ (lane & 7)] =
+                make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
+                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        __syncwarp();
+        // Coalesced, predicated stores: 8 lanes cover one 128-byte row segment.
+        const int jj = lane & 7;
+        const int64_t gcol = col_base + ch * 32 + jj * 4;
+#pragma unroll
+        for (int rr0 = 0; rr0 < 32; rr0 += 4) {
+            const int rr = rr0 + (lane >> 3);
+            const float4 v = reinterpret_cast<const float4 *>(stage + rr * 32)[jj ^ (rr & 7)];
+            const int64_t grow = row_base + rr;
+            if (grow < p.M) {
+                float *dst = p.C + grow * p.ldc + gcol;
+                if (vec && gcol + 3 < p.N) {
+                    __stcs(reinterpret_cast<float4 *>(dst), v);
+                } else {
+                    if (gcol + 0 < p.N) __stcs(dst + 0, v.x);
+                    if (gcol + 1 < p.N) __stcs(dst + 1, v.y);
+                    if (gcol + 2 < p.N) __stcs(dst + 2, v.z);
+                    if (gcol + 3 < p.N) __stcs(dst + 3, v.w);
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
+template <int CG, int BN, int STAGES>
 __global__ void __launch_bounds__(192, 1)
     gemm_f16_f32_tcgen05(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, const KernelParams p)
 {
-    using Cf = Cfg<BN, STAGES>;
+    using Cf = Cfg<CG, BN, STAGES>;
+    constexpr bool kPair = CG == 2;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms must start on 1024-byte boundaries of the shared space.
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -119,6 +189,10 @@ __global__ void __launch_bounds__(192, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // CTA rank inside the pair (0 = the CTA that issues the MMAs) and the tile walk.
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const int first_tile = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int tile_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -127,7 +201,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), Cf::EPI_WARPS);
+            mbar_init(tempty_bar(b), Cf::EPI_WARPS * CG);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -138,11 +212,17 @@ __global__ void __launch_bounds__(192, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), Cf::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(smem_u32(tmem_slot), Cf::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), Cf::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();  // peer barriers initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t limit = p.timeout_ns;
@@ -156,23 +236,34 @@ __global__ void __launch_bounds__(192, 1)
             bool issued[STAGES];
             for (int i = 0; i < STAGES; ++i) issued[i] = false, issued_parity[i] = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int t = first_tile; ok && t < p.num_tiles; t += tile_step) {
                 const TileCoord c = tile_coord(t, p.num_m, p.num_n, p.group_m);
-                const int32_t m0 = c.m * Cf::BM;
-                const int32_t n0 = c.n * BN;
+                const int32_t m0 = c.m * (Cf::BM * CG) + static_cast<int32_t>(rank) * Cf::BM;
+                const int32_t n0 = c.n * BN + static_cast<int32_t>(rank) * Cf::BN_CTA;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_or_abort(empty_bar(s), ph ^ 1u, limit, abort_flag,
-                                       SITE_PRODUCER_EMPTY)) {
+                    if (!wait_or_abort<kPair>(empty_bar(s), ph ^ 1u, limit, abort_flag,
+                                              SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_TX);
                     const int32_t k0 = kb * Cf::BK;
-                    tma_load_2d(smem_u32(sA + s * Cf::A_STAGE), &tmA, k0, m0, full_bar(s));
+                    if constexpr (kPair) {
+                        // Both CTAs' bytes are counted on the even CTA's full barrier.
+                        const uint32_t fb = map_to_cta(full_bar(s), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_TX);
+                        tma_load_2d_pair(smem_u32(sA + s * Cf::A_STAGE), &tmA, k0, m0, fb);
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d(smem_u32(sB + s * Cf::B_STAGE + j * Cf::B_SUB), &tmB, n0 + 64 * j,
-                                    k0, full_bar(s));
+                        for (int j = 0; j < Cf::B_BOXES; ++j)
+                            tma_load_2d_pair(smem_u32(sB + s * Cf::B_STAGE + j * Cf::B_SUB), &tmB,
+                                             n0 + 64 * j, k0, fb);
+                    } else {
+                        mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_TX);
+                        tma_load_2d(smem_u32(sA + s * Cf::A_STAGE), &tmA, k0, m0, full_bar(s));
+#pragma unroll
+                        for (int j = 0; j < Cf::B_BOXES; ++j)
+                            tma_load_2d(smem_u32(sB + s * Cf::B_STAGE + j * Cf::B_SUB), &tmB, n0 + 64 * j,
+                                        k0, full_bar(s));
+                    }
                     issued[s] = true;
                     issued_parity[s] = ph;
                     if (++s == STAGES) {
@@ -181,7 +272,22 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
-            if (!ok) {
+            if (ok) {
+                // Tail: wait until the MMAs have released every stage, so that no arrival is
+                // still on its way to this CTA's shared memory when it exits.
+                for (int i = 0; i < STAGES; ++i) {
+                    if (!wait_or_abort<kPair>(empty_bar(s), ph ^ 1u, limit, abort_flag, SITE_PRODUCER_TAIL))
+                        break;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            } else if (kPair && rank != 0) {
+                // This CTA's loads signal the peer's barrier: give them time to land.
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 2000000ull) __nanosleep(1000);
+            } else {
                 // Let this CTA's loads land before shared memory is released.
                 for (int i = 0; i < STAGES; ++i)
                     if (issued[i]) (void)mbar_wait(full_bar(i), issued_parity[i], limit);
@@ -190,25 +296,25 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(Cf::BM, BN, /*b_mn_major=*/true);
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(Cf::BM * CG, BN, /*b_mn_major=*/true);
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
             bool ok = true;
             bool any_mma = false;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+            for (int t = first_tile; ok && t < p.num_tiles; t += tile_step, ++it) {
                 const int b = it & 1;
                 const uint32_t use = static_cast<uint32_t>(it >> 1);
-                if (!wait_or_abort(tempty_bar(b), (use & 1u) ^ 1u, limit, abort_flag,
-                                   SITE_MMA_TMEM_EMPTY)) {
+                if (!wait_or_abort<kPair>(tempty_bar(b), (use & 1u) ^ 1u, limit, abort_flag,
+                                          SITE_MMA_TMEM_EMPTY)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_or_abort(full_bar(s), ph, limit, abort_flag, SITE_MMA_FULL)) {
+                    if (!wait_or_abort<kPair>(full_bar(s), ph, limit, abort_flag, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
@@ -223,21 +329,34 @@ __global__ void __launch_bounds__(192, 1)
                         // B: N-major, 64-column boxes B_SUB bytes apart (leading offset),
                         // 8-row K groups 1024 B apart (stride offset); 16 K rows = 2048 B.
                         const uint64_t bdesc = smem_desc_sw128(b_base + kk * 2048, Cf::B_SUB, 1024);
-                        tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                        if constexpr (kPair)
+                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, acc);
+                        else
+                            tc_mma_f16(d_tmem, adesc, bdesc, idesc, acc);
                     }
                     any_mma = true;
-                    tc_commit(empty_bar(s));
+                    if constexpr (kPair)
+                        tc_commit_pair_multicast(empty_bar(s), 0x3);
+                    else
+                        tc_commit(empty_bar(s));
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(tfull_bar(b));
+                if constexpr (kPair)
+                    tc_commit_pair_multicast(tfull_bar(b), 0x3);
+                else
+                    tc_commit(tfull_bar(b));
             }
             if (!ok && any_mma) {
                 // Wait for this thread's MMAs before TMEM is released.
-                tc_commit(drain_bar);
+                if constexpr (kPair)
+                    tc_commit_pair_multicast(drain_bar, 0x1);
+                else
+                    tc_commit(drain_bar);
                 (void)mbar_wait(drain_bar, 0, limit);
             }
         }
@@ -248,68 +367,40 @@ __global__ void __launch_bounds__(192, 1)
         float *stage = sEpi + (warp - 2) * 32 * 32;
         const bool vec = p.vec_store != 0;
         int it = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+        for (int t = first_tile; t < p.num_tiles; t += tile_step, ++it) {
             const int b = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
-            bool ok = wait_or_abort(tfull_bar(b), use & 1u, limit, abort_flag, SITE_EPI_TMEM_FULL);
+            bool ok = wait_or_abort<kPair>(tfull_bar(b), use & 1u, limit, abort_flag, SITE_EPI_TMEM_FULL);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             const TileCoord c = tile_coord(t, p.num_m, p.num_n, p.group_m);
-            const int64_t row_base = static_cast<int64_t>(c.m) * Cf::BM + q * 32;
+            const int64_t row_base = static_cast<int64_t>(c.m) * (Cf::BM * CG) +
+                                     static_cast<int64_t>(rank) * Cf::BM + q * 32;
             const int64_t col_base = static_cast<int64_t>(c.n) * BN;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(b * BN);
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + ch * 32, r);
-                tmem_wait_ld();
-                if (ch == BN / 32 - 1) {
-                    // Accumulator fully read: hand the buffer back to the MMA warp.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty_bar(b));
-                }
-                // Row `lane` of this 32 x 32 block into the staging buffer, 16-byte chunks
-                // XOR-swizzled by row so the transposed read below is conflict-free.
-                float4 *srow = reinterpret_cast<float4 *>(stage + lane * 32);
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    srow[j ^ (lane & 7)] =
-                        make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
-                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                __syncwarp();
-                // Coalesced, predicated stores: 8 lanes cover one 128-byte row segment.
-                const int jj = lane & 7;
-                const int64_t gcol = col_base + ch * 32 + jj * 4;
-#pragma unroll
-                for (int rr0 = 0; rr0 < 32; rr0 += 4) {
-                    const int rr = rr0 + (lane >> 3);
-                    const float4 v = reinterpret_cast<const float4 *>(stage + rr * 32)[jj ^ (rr & 7)];
-                    const int64_t grow = row_base + rr;
-                    if (grow < p.M) {
-                        float *dst = p.C + grow * p.ldc + gcol;
-                        if (vec && gcol + 3 < p.N) {
-                            __stcs(reinterpret_cast<float4 *>(dst), v);
-                        } else {
-                            if (gcol + 0 < p.N) __stcs(dst + 0, v.x);
-                            if (gcol + 1 < p.N) __stcs(dst + 1, v.y);
-                            if (gcol + 2 < p.N) __stcs(dst + 2, v.z);
-                            if (gcol + 3 < p.N) __stcs(dst + 3, v.w);
-                        }
-                    }
-                }
-                __syncwarp();
+            if constexpr (kPair) {
+                const uint32_t te = map_to_cta(tempty_bar(b), 0);
+                store_accumulator<BN>(t_row, row_base, col_base, p, stage, lane, vec,
+                                      [&] { mbar_arrive_cluster(te); });
+            } else {
+                const uint32_t te = tempty_bar(b);
+                store_accumulator<BN>(t_row, row_base, col_base, p, stage, lane, vec, [&] { mbar_arrive(te); });
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();  // the pair's MMAs and remote arrivals are done
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem_base, Cf::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, Cf::TMEM_COLS);
     }
 }
 
@@ -341,33 +432,82 @@ __global__ void fill_zero_f32(float *__restrict__ C, int64_t ldc, int64_t rows, 
 
 // ---------------------------------------------------------------- host side
 
-template <int BN, int STAGES>
+template <int CG, int BN, int STAGES>
+static cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute *attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<CG, BN, STAGES>::SMEM_BYTES;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int CG, int BN, int STAGES>
 static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const KernelParams &p,
                                   int grid, cudaStream_t stream)
 {
-    using Cf = Cfg<BN, STAGES>;
-    auto kern = gemm_f16_f32_tcgen05<BN, STAGES>;
+    auto kern = gemm_f16_f32_tcgen05<CG, BN, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cf::SMEM_BYTES);
+                                         Cfg<CG, BN, STAGES>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 192, Cf::SMEM_BYTES, stream>>>(ta, tb, p);
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = launch_config<CG, BN, STAGES>(grid, stream, attr);
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-int variant_smem_bytes(int tile_n, int stages)
+// Clusters of this variant that can be resident at once on the current device.
+template <int CG, int BN, int STAGES>
+static int max_clusters_variant()
 {
-#define TCT_CASE(BN_, ST_) \
-    if (tile_n == BN_ && stages == ST_) return Cfg<BN_, ST_>::SMEM_BYTES;
+    auto kern = gemm_f16_f32_tcgen05<CG, BN, STAGES>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<CG, BN, STAGES>::SMEM_BYTES) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = launch_config<CG, BN, STAGES>(2048, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    return n;
+}
+
+int variant_smem_bytes(int cta_group, int tile_n, int stages)
+{
+#define TCT_CASE(CG_, BN_, ST_) \
+    if (cta_group == CG_ && tile_n == BN_ && stages == ST_) return Cfg<CG_, BN_, ST_>::SMEM_BYTES;
     TCT_VARIANTS(TCT_CASE)
 #undef TCT_CASE
     return -1;
 }
 
-cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const KernelParams &p, int tile_n,
-                        int stages, int grid, cudaStream_t stream)
+int variant_max_clusters(int cta_group, int tile_n, int stages)
 {
-#define TCT_CASE(BN_, ST_) \
-    if (tile_n == BN_ && stages == ST_) return launch_variant<BN_, ST_>(ta, tb, p, grid, stream);
+#define TCT_CASE(CG_, BN_, ST_) \
+    if (cta_group == CG_ && tile_n == BN_ && stages == ST_) return max_clusters_variant<CG_, BN_, ST_>();
+    TCT_VARIANTS(TCT_CASE)
+#undef TCT_CASE
+    return -1;
+}
+
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const KernelParams &p, int cta_group,
+                        int tile_n, int stages, int grid, cudaStream_t stream)
+{
+#define TCT_CASE(CG_, BN_, ST_)                             \
+    if (cta_group == CG_ && tile_n == BN_ && stages == ST_) \
+        return launch_variant<CG_, BN_, ST_>(ta, tb, p, grid, stream);
     TCT_VARIANTS(TCT_CASE)
 #undef TCT_CASE
     return cudaErrorInvalidValue;

@@ -61,6 +61,7 @@ def test_invalid_arguments_rejected_before_any_device_work(tct_lib):
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, tile_n=96) == tct.GEMM_ERR_INVALID_ARG
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, stages=9) == tct.GEMM_ERR_INVALID_ARG
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, group_m=-1) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, cta_group=3) == tct.GEMM_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("num_m,num_n", [(9, 9), (7, 14), (32, 16), (13, 5), (1, 40), (40, 1)])
@@ -117,13 +118,18 @@ def test_page_wave_quantisation_example(tct_lib):
 def test_planner_on_gb300_shapes(tct_lib):
     sms = 152
     p = tct.gemm_f16_f32_plan(8192, 8192, 8192, num_sms=sms)
-    assert (p["tile_m"], p["tile_n"], p["tile_k"]) == (128, 256, 64)
-    assert p["grid"] == sms and p["tiles"] == 64 * 32
-    assert p["waves"] == -(-2048 // sms)
+    # the CTA-pair 256x256 tile: 32 x 32 tiles over 76 pairs
+    assert (p["cta_group"], p["tile_m"], p["tile_n"], p["tile_k"]) == (2, 256, 256, 64)
+    assert p["grid"] == sms and p["tiles"] == 32 * 32
+    assert p["waves"] == -(-1024 // (sms // 2))
     assert p["pack_a"] == 0 and p["pack_b"] == 0
-    # the skinny, bandwidth-bound shape spreads over more SMs with the narrow tile
+    # 4096^3: 4 waves of 256x256 pair tiles (84% filled) still beat the narrower tiles'
+    # fuller waves at their lower per-tile rate
+    p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms)
+    assert (p["cta_group"], p["tile_n"], p["waves"]) == (2, 256, 4)
+    # the skinny, bandwidth-bound shape spreads over more SMs with the narrow 1-CTA tile
     p = tct.gemm_f16_f32_plan(128, 16384, 16384, num_sms=sms)
-    assert p["tile_n"] == 128 and p["grid"] == 128
+    assert (p["cta_group"], p["tile_n"], p["grid"]) == (1, 128, 128)
     # ragged leading dimensions are repacked before TMA
     p = tct.gemm_f16_f32_plan(17, 4097, 31, num_sms=sms)
     assert p["pack_a"] == 1 and p["pack_b"] == 1
@@ -132,7 +138,13 @@ def test_planner_on_gb300_shapes(tct_lib):
     # explicit options are honoured
     p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, tile_n=256, stages=3, group_m=16, max_ctas=100)
     assert (p["tile_n"], p["stages"], p["group_m"], p["grid"]) == (256, 3, 16, 100)
-    # the shared-memory ring fits the 227 KB limit
-    for tn, st in ((256, 2), (256, 3), (256, 4), (128, 4), (128, 6)):
-        p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, tile_n=tn, stages=st)
+    p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, cta_group=1, tile_n=256)
+    assert (p["cta_group"], p["tile_m"], p["stages"], p["grid"]) == (1, 128, 4, 152)
+    # every compiled variant's shared-memory ring fits the 227 KB limit
+    for cg, tn, st in ((1, 256, 2), (1, 256, 3), (1, 256, 4), (1, 128, 4), (1, 128, 6),
+                       (2, 256, 3), (2, 256, 4), (2, 256, 5), (2, 256, 6), (2, 128, 6), (2, 128, 8)):
+        p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, cta_group=cg, tile_n=tn, stages=st)
+        assert (p["cta_group"], p["tile_n"], p["stages"]) == (cg, tn, st)
         assert 0 < p["smem_bytes"] <= 227 * 1024
+    with pytest.raises(tct.GemmError):
+        tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, cta_group=2, stages=2)

@@ -164,22 +164,56 @@ def test_repeat_runs_bitwise_identical():
         assert torch.equal(first.view(torch.int32), again.view(torch.int32))
 
 
-@pytest.mark.parametrize("opts", [dict(group_m=1), dict(group_m=4), dict(group_m=16),
-                                  dict(tile_n=128), dict(tile_n=128, stages=4), dict(tile_n=256, stages=2),
-                                  dict(tile_n=256, stages=3), dict(max_ctas=7), dict(tile_n=128, group_m=3)])
+VARIANT_OPTS = [
+    dict(cta_group=1, tile_n=256, stages=2), dict(cta_group=1, tile_n=256, stages=3),
+    dict(cta_group=1, tile_n=256, stages=4, group_m=1), dict(cta_group=1, tile_n=128, stages=4),
+    dict(cta_group=1, tile_n=128, stages=6, group_m=3), dict(cta_group=1, tile_n=256, max_ctas=7),
+    dict(cta_group=2, tile_n=256, stages=3), dict(cta_group=2, tile_n=256, stages=4, group_m=16),
+    dict(cta_group=2, tile_n=256, stages=5), dict(cta_group=2, tile_n=256, stages=6, group_m=1),
+    dict(cta_group=2, tile_n=128, stages=6), dict(cta_group=2, tile_n=128, stages=8, group_m=4),
+    dict(cta_group=2, tile_n=256, max_ctas=6), dict(cta_group=2, tile_n=128, max_ctas=2),
+]
+
+
+@pytest.mark.parametrize("opts", VARIANT_OPTS)
 def test_variants_and_schedules_agree(opts):
-    """For a given tile width every pipeline depth, launch order and grid size gives the same
-    bits (the k order inside a tile never changes), and every variant passes the oracle."""
+    """For a given CTA grouping and tile width, every pipeline depth, launch order and grid
+    size gives the same bits (the k order inside a tile never changes); every variant
+    passes the oracle."""
     rng = np.random.default_rng(23)
     M, N, K = 777, 1500, 515
     A, B = inputs.normal_pair(rng, M, N, K)
     dA, dB = dev16(A), dev16(B)
-    width = opts.get("tile_n") or tct.gemm_f16_f32_plan(M, N, K)["tile_n"]
-    ref = tct.matmul(dA, dB, tile_n=width)
+    ref = tct.matmul(dA, dB, cta_group=opts["cta_group"], tile_n=opts["tile_n"])
     C = tct.matmul(dA, dB, **opts)
     torch.cuda.synchronize()
     assert torch.equal(C.view(torch.int32), ref.view(torch.int32))
     assert within_tol(C.cpu().numpy(), oracle.gemm_f32(A, B), K)
+
+
+def test_pair_and_single_cta_tiles_agree():
+    rng = np.random.default_rng(29)
+    M, N, K = 1000, 1024, 1000
+    A, B = inputs.normal_pair(rng, M, N, K)
+    dA, dB = dev16(A), dev16(B)
+    one = tct.matmul(dA, dB, cta_group=1, tile_n=256)
+    two = tct.matmul(dA, dB, cta_group=2, tile_n=256)
+    torch.cuda.synchronize()
+    R = oracle.gemm_f32(A, B)
+    assert within_tol(one.cpu().numpy(), R, K) and within_tol(two.cpu().numpy(), R, K)
+
+
+@pytest.mark.parametrize("cta_group,tile_n", [(1, 128), (1, 256), (2, 128), (2, 256)])
+def test_every_variant_on_ragged_and_integer_inputs(cta_group, tile_n):
+    for (M, N, K), A, B in inputs.workload("ragged"):
+        C = gpu_gemm(A, B, cta_group=cta_group, tile_n=tile_n)
+        assert within_tol(C, oracle.gemm_f32(A, B), K), (M, N, K)
+    for (M, N, K), A, B in inputs.workload("ragged_int"):
+        C = gpu_gemm(A, B, cta_group=cta_group, tile_n=tile_n)
+        assert bit_exact(C, oracle.gemm_f32(A, B)), (M, N, K)
+    rng = np.random.default_rng(33)
+    A, B = inputs.integer_pair(rng, 700, 900, 1100)
+    assert bit_exact(gpu_gemm(A, B, cta_group=cta_group, tile_n=tile_n), oracle.gemm_f32(A, B))
 
 
 # ---- full-size workloads: sampled outputs -------------------------------------------------
