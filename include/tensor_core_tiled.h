@@ -52,8 +52,11 @@ typedef enum gemm_status {
  *   M, N, K : 0 <= M, N, K < 2^31.
  * Any alignment and any leading dimension are accepted.  When lda or ldb is not a
  * multiple of 8 elements, or A or B is not 16-byte aligned, the operand is first copied
- * on `stream` into a stream-ordered temporary (cudaMallocAsync/cudaFreeAsync) whose rows
- * are 16-byte aligned.  The result does not depend on which path ran.
+ * on `stream` into a stream-ordered temporary whose rows are 16-byte aligned.  Temporaries
+ * (these copies and the stream-K partial tiles, see gemm_options) come from a library-owned
+ * stream-ordered memory pool per device (cudaMallocFromPoolAsync / cudaFreeAsync on
+ * `stream`) that keeps freed memory for reuse until the process exits.  The result does
+ * not depend on which path ran.
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (negative or oversized dims, lda < K, ldb < N,
  * ldc < N, NULL pointer with a non-empty extent), GEMM_ERR_UNSUPPORTED_DEVICE or
  * GEMM_ERR_CUDA.
@@ -71,6 +74,11 @@ TCT_API gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t
  *   max_ctas  : cap on the persistent grid in CTAs (default: every co-resident CTA).
  *   timeout_ms: limit on any single device pipeline wait (default 2000 ms).
  *   cta_group : 1 = one CTA per 128-row tile, 2 = a CTA pair per 256-row tile.
+ *   stream_k  : 1 = whole tiles only; 2 = split each tile of the last, partial wave into
+ *               two k-halves on two units whenever that wave fills at most half the units
+ *               (the second half goes through a stream-ordered workspace and is added by the
+ *               first half's unit, always in the same order, so results are reproducible);
+ *               0 = let the planner decide.
  */
 typedef struct gemm_options {
     int32_t group_m;
@@ -79,7 +87,8 @@ typedef struct gemm_options {
     int32_t max_ctas;
     int32_t timeout_ms;
     int32_t cta_group;
-    int32_t reserved[2]; /* must be zero */
+    int32_t stream_k;
+    int32_t reserved[1]; /* must be zero */
 } gemm_options;
 
 /* gemm_f16_f32 with explicit tuning options (opt may be NULL = all defaults). */
@@ -102,6 +111,9 @@ typedef struct gemm_plan {
     int32_t smem_bytes;             /* dynamic shared memory per CTA                  */
     int32_t pack_a, pack_b;         /* 1 if the operand would be repacked first       */
     int32_t cta_group;              /* CTAs sharing one tile (1 or 2)                 */
+    int32_t units;                  /* persistent work units (CTAs or CTA pairs)      */
+    int32_t stream_k_tiles;         /* tiles whose k-loop is split in two halves      */
+    double effective_waves;         /* tile-times per unit: whole waves + split share */
 } gemm_plan;
 
 TCT_API gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -115,6 +127,28 @@ TCT_API gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t l
  */
 TCT_API gemm_status gemm_tile_coord(int64_t t, int64_t num_m, int64_t num_n, int32_t group_m,
                             int64_t *tile_row, int64_t *tile_col);
+
+/*
+ * One work item of a persistent unit (a CTA, or a CTA pair when cta_group is 2): k-blocks
+ * [kb0, kb1) of linear tile `tile`.  mode 0: store the tile to C.  A tile of the last,
+ * partial wave may be split into two k-halves: mode 1 (its owner, the first half) adds the
+ * second half, read from workspace slot `part`, then stores to C; mode 2 writes the second
+ * half to slot `part` for the owner.
+ */
+typedef struct gemm_work {
+    int32_t tile, kb0, kb1;
+    int32_t mode;
+    int32_t part; /* -1 when mode == 0 */
+} gemm_work;
+
+/*
+ * Work item `idx` of unit `unit` in the plan the library would use for (M, N, K) on num_sms
+ * SMs (host only).  Returns GEMM_ERR_INVALID_ARG when the unit has no such item.  Every
+ * (tile, k-block) pair belongs to exactly one item of one unit.
+ */
+TCT_API gemm_status gemm_f16_f32_work_item(int64_t M, int64_t N, int64_t K, int32_t num_sms,
+                                           const gemm_options *opt, int32_t unit, int32_t idx,
+                                           gemm_work *out);
 
 /*
  * Wave model ("02_gpu_execution_model.py", part 5, wave_utilization): tiles =

@@ -24,6 +24,7 @@ EXPORTED = (
     "gemm_f16_f32_ex",
     "gemm_f16_f32_noalloc",
     "gemm_f16_f32_plan",
+    "gemm_f16_f32_work_item",
     "gemm_tile_coord",
     "gemm_wave_model",
     "gemm_f16_f32_get_error",
@@ -41,7 +42,7 @@ class GemmError(RuntimeError):
 class GemmOptions(ctypes.Structure):
     _fields_ = [("group_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32), ("cta_group", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("stream_k", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 class GemmPlan(ctypes.Structure):
@@ -49,8 +50,16 @@ class GemmPlan(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("group_m", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("tiles", ctypes.c_int64), ("waves", ctypes.c_int64), ("wave_efficiency", ctypes.c_double),
                 ("smem_bytes", ctypes.c_int32), ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32),
-                ("cta_group", ctypes.c_int32)]
+                ("cta_group", ctypes.c_int32), ("units", ctypes.c_int32), ("stream_k_tiles", ctypes.c_int32),
+                ("effective_waves", ctypes.c_double)]
 
+
+class GemmWork(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int32), ("kb0", ctypes.c_int32), ("kb1", ctypes.c_int32), ("mode", ctypes.c_int32),
+                ("part", ctypes.c_int32)]
+
+
+WORK_STORE, WORK_FIXUP, WORK_PARTIAL = 0, 1, 2
 
 _lib = None
 
@@ -73,6 +82,9 @@ def load():
     lib.gemm_f16_f32_plan.restype = ctypes.c_int
     lib.gemm_f16_f32_plan.argtypes = [i64, i64, i64, i64, i64, i32, ctypes.POINTER(GemmOptions),
                                       ctypes.POINTER(GemmPlan)]
+    lib.gemm_f16_f32_work_item.restype = ctypes.c_int
+    lib.gemm_f16_f32_work_item.argtypes = [i64, i64, i64, i32, ctypes.POINTER(GemmOptions), i32, i32,
+                                           ctypes.POINTER(GemmWork)]
     lib.gemm_tile_coord.restype = ctypes.c_int
     lib.gemm_tile_coord.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.gemm_wave_model.restype = ctypes.c_int
@@ -99,10 +111,10 @@ def version():
     return load().gemm_version().decode()
 
 
-def _options(group_m=0, tile_n=0, stages=0, max_ctas=0, timeout_ms=0, cta_group=0):
+def _options(group_m=0, tile_n=0, stages=0, max_ctas=0, timeout_ms=0, cta_group=0, stream_k=0):
     o = GemmOptions()
     o.group_m, o.tile_n, o.stages, o.max_ctas, o.timeout_ms = group_m, tile_n, stages, max_ctas, timeout_ms
-    o.cta_group = cta_group
+    o.cta_group, o.stream_k = cta_group, stream_k
     return o
 
 
@@ -120,7 +132,8 @@ NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 def gemm_f16_f32_ex(A, B, C, M, N, K, lda, ldb, ldc, stream=0, **options):
-    """Raw C-ABI call with tuning options (group_m, tile_n, stages, max_ctas, timeout_ms, cta_group)."""
+    """Raw C-ABI call with tuning options (group_m, tile_n, stages, max_ctas, timeout_ms, cta_group,
+    stream_k)."""
     opt = _options(**options)
     return load().gemm_f16_f32_ex(A, B, C, M, N, K, lda, ldb, ldc, stream or None, ctypes.byref(opt))
 
@@ -134,6 +147,18 @@ def gemm_f16_f32_plan(M, N, K, lda=None, ldb=None, num_sms=0, **options):
     if st:
         raise GemmError(st, "gemm_f16_f32_plan")
     return {name: getattr(pl, name) for name, _ in GemmPlan._fields_}
+
+
+def gemm_f16_f32_work_item(M, N, K, num_sms, unit, idx, **options):
+    """Work item idx of a persistent unit as a dict, or None when the unit has no more."""
+    opt = _options(**options)
+    w = GemmWork()
+    st = load().gemm_f16_f32_work_item(M, N, K, num_sms, ctypes.byref(opt), unit, idx, ctypes.byref(w))
+    if st == GEMM_ERR_INVALID_ARG:
+        return None
+    if st:
+        raise GemmError(st, "gemm_f16_f32_work_item")
+    return {name: getattr(w, name) for name, _ in GemmWork._fields_}
 
 
 def gemm_tile_coord(t, num_m, num_n, group_m):

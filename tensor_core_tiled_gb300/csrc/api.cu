@@ -33,6 +33,18 @@ struct Candidate {
     int cta_group, tile_n, stages;
     double rate;
 };
+// Time model of one launch (seconds), for choosing between plans.  Per-SM tensor rate at a
+// typical loaded clock (8192 FP16 FLOP per clock per SM x 1.9 GHz), HBM copy bandwidth, L2
+// bandwidth for the split tiles' parts, and the exposed cost of a split tile's fix-up.
+constexpr double kSmFlops = 8192.0 * 1.9e9;
+constexpr double kHbmBytesPerSec = 6.5e12;
+constexpr double kL2BytesPerSec = 20e12;
+// Measured on GB300: the second half's write, its transfer to the owner and the owner's
+// store are serial after the halves finish, about two tile epilogues plus a flag handoff.
+constexpr double kFixupSec = 12e-6;
+// A tile is only split in two when each half has at least this many k-blocks.
+constexpr int64_t kMinSplitIters = 4;
+
 constexpr Candidate kCandidates[] = {
     {2, 256, 6, 1.00},
     {1, 256, 4, 0.85},
@@ -46,6 +58,7 @@ struct DeviceInfo {
     int major = 0;
     int minor = 0;
     int pair_clusters = 0;  // co-resident CTA pairs of the pair kernels (0 = not queried)
+    cudaMemPool_t pool = nullptr;  // stream-ordered temporaries (repacks, stream-K partials)
 };
 
 std::mutex g_mu;
@@ -67,6 +80,34 @@ gemm_status device_info(DeviceInfo *out)
     }
     *out = d;
     if (d.major != 10 || d.minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    return GEMM_OK;
+}
+
+// The library's stream-ordered memory pool on the current device.  It keeps freed memory
+// for reuse (release threshold = unlimited), so a temporary of the same size on the next
+// call costs no new physical mapping; the memory is returned when the process exits.
+gemm_status device_pool(cudaMemPool_t *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.pool) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return GEMM_ERR_CUDA;
+        uint64_t keep = UINT64_MAX;
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return GEMM_ERR_CUDA;
+        }
+        d.pool = pool;
+    }
+    *out = d.pool;
     return GEMM_OK;
 }
 
@@ -111,8 +152,8 @@ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 gemm_status check_options(const gemm_options *opt)
 {
     if (!opt) return GEMM_OK;
-    for (int i = 0; i < 2; ++i)
-        if (opt->reserved[i] != 0) return GEMM_ERR_INVALID_ARG;
+    if (opt->reserved[0] != 0) return GEMM_ERR_INVALID_ARG;
+    if (opt->stream_k < 0 || opt->stream_k > 2) return GEMM_ERR_INVALID_ARG;
     if (opt->group_m < 0 || opt->group_m > 256) return GEMM_ERR_INVALID_ARG;
     if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return GEMM_ERR_INVALID_ARG;
     if (opt->cta_group < 0 || opt->cta_group > 2) return GEMM_ERR_INVALID_ARG;
@@ -156,38 +197,86 @@ double wave_util(int64_t M, int64_t N, int64_t tm, int64_t tn, int64_t slots, in
     return static_cast<double>(tiles) / static_cast<double>(waves * slots);
 }
 
-// Fraction of the launch's tile slots (waves x slots x tile area) holding useful outputs.
-double useful_fraction(int64_t M, int64_t N, int64_t tm, int64_t tn, int64_t slots)
+struct Split {
+    int64_t units, tiles, waves, dp_tiles, split_tiles;
+    double time, eff_waves;
+};
+
+// Work split and modelled time of one variant.  Whole waves of tiles go data-parallel; the
+// last, partial wave either runs as whole tiles (a full extra wave of time, "02_gpu_execution
+// _model.py" part 5) or, when at most half the units would be busy in it, has each of its
+// tiles split into two k-halves on two units (half a wave, plus the owner's add of the other
+// half).  Memory time assumes HBM bandwidth in proportion to the share of busy units.
+Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stages, double rate, int64_t units,
+                  int want_sk)
 {
-    int64_t tiles = 0, waves = 0;
-    wave_util(M, N, tm, tn, slots, &tiles, &waves);
-    return static_cast<double>(M) * static_cast<double>(N) /
-           (static_cast<double>(waves) * slots * tm * tn);
+    Split sp{};
+    const int64_t tile_m = kTileM * cg;
+    const int64_t tiles = tct::ceil_div(M, tile_m) * tct::ceil_div(N, tile_n);
+    const int64_t kb = std::max<int64_t>(1, tct::ceil_div(K, kTileK));
+    units = std::max<int64_t>(1, units);
+    const double tile_sec = 2.0 * tile_m * tile_n * static_cast<double>(kb * kTileK) / (cg * kSmFlops * rate);
+    const double tile_bytes = 4.0 * tile_m * tile_n;
+    const double bytes = 2.0 * M * K + 2.0 * K * N + 4.0 * M * N;
+    // whole tiles only, on at most one unit per tile
+    const int64_t dp_units = std::min<int64_t>(units, tiles);
+    const int64_t waves = tct::ceil_div(tiles, dp_units);
+    const double busy = static_cast<double>(dp_units) / units;
+    const double t_dp = std::max(waves * tile_sec, bytes / (kHbmBytesPerSec * busy));
+    sp.units = dp_units;
+    sp.tiles = tiles;
+    sp.waves = waves;
+    sp.dp_tiles = tiles;
+    sp.split_tiles = 0;
+    sp.time = t_dp;
+    sp.eff_waves = static_cast<double>(waves);
+    const int64_t full = tiles / units, rest = tiles - full * units;
+    const bool can_split = rest > 0 && 2 * rest <= units && kb / 2 >= (want_sk == 2 ? 1 : kMinSplitIters) &&
+                           want_sk != 1 && tct::variant_split_ok(cg, tile_n, stages);
+    if (can_split) {
+        const double ew = full + 0.5;
+        const double busy_split = static_cast<double>(2 * rest) / units;
+        const double t_tail_mem = (full > 0 ? bytes * full / tiles / kHbmBytesPerSec : 0.0) +
+                                  bytes * rest / tiles / (kHbmBytesPerSec * busy_split);
+        const double t_sp = std::max(ew * tile_sec, t_tail_mem) + kFixupSec +
+                            2.0 * rest * tile_bytes / kL2BytesPerSec;
+        if (want_sk == 2 || t_sp < t_dp) {
+            sp.units = units;
+            sp.waves = tct::ceil_div(tiles, units);
+            sp.dp_tiles = full * units;
+            sp.split_tiles = rest;
+            sp.time = t_sp;
+            sp.eff_waves = ew;
+        }
+    }
+    return sp;
 }
 
-// Wave-quantisation-aware choice among the compiled variants ("02_gpu_execution_model.py",
-// part 5: tiles, waves = ceil(tiles / slots), utilisation), weighted by each variant's rate.
+// Choice among the compiled variants by modelled time: wave quantisation, the per-tile rate
+// of each variant, and HBM time for bandwidth-bound shapes.
 // pair_slots: co-resident CTA pairs (from the device, or sms / 2 when planning offline).
 gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int sms, int pair_slots,
-                      const gemm_options *opt, const void *A, const void *B, gemm_plan *pl)
+                      const gemm_options *opt, const void *A, const void *B, gemm_plan *pl, bool allow_split = true)
 {
     std::memset(pl, 0, sizeof(*pl));
     const int want_cg = opt ? opt->cta_group : 0;
     const int want_tn = opt ? opt->tile_n : 0;
     const int want_st = opt ? opt->stages : 0;
-    int64_t cap = opt && opt->max_ctas > 0 ? opt->max_ctas : 0;
+    const int want_sk = allow_split ? (opt ? opt->stream_k : 0) : 1;
+    const int64_t cap = opt && opt->max_ctas > 0 ? opt->max_ctas : 0;
     const Candidate *best = nullptr;
-    double best_score = -1.0;
+    Split best_sp{};
     for (const Candidate &c : kCandidates) {
         if ((want_cg && want_cg != c.cta_group) || (want_tn && want_tn != c.tile_n)) continue;
         if (want_st && tct::variant_smem_bytes(c.cta_group, c.tile_n, want_st) < 0) continue;
-        int64_t slots = c.cta_group == 2 ? pair_slots : sms;
-        if (cap > 0) slots = std::min<int64_t>(slots, std::max<int64_t>(1, cap / c.cta_group));
-        if (slots < 1) continue;
-        const double score = useful_fraction(M, N, 128 * c.cta_group, c.tile_n, slots) * c.rate;
-        if (score > best_score) {
-            best_score = score;
+        int64_t units = c.cta_group == 2 ? pair_slots : sms;
+        if (cap > 0) units = std::min<int64_t>(units, std::max<int64_t>(1, cap / c.cta_group));
+        if (units < 1) continue;
+        const int st = want_st ? want_st : c.stages;
+        const Split sp = model_split(M, N, K, c.cta_group, c.tile_n, st, c.rate, units, want_sk);
+        if (!best || sp.time < best_sp.time) {
             best = &c;
+            best_sp = sp;
         }
     }
     if (!best) return GEMM_ERR_INVALID_ARG;
@@ -196,25 +285,79 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
     const int smem = tct::variant_smem_bytes(cg, tile_n, stages);
     if (smem < 0) return GEMM_ERR_INVALID_ARG;
     const int tile_m = kTileM * cg;
-    const int64_t tiles = tct::ceil_div(M, tile_m) * tct::ceil_div(N, tile_n);
-    int64_t units = cg == 2 ? pair_slots : sms;  // persistent CTAs (or pairs)
-    if (cap > 0) units = std::min<int64_t>(units, std::max<int64_t>(1, cap / cg));
-    units = std::max<int64_t>(1, std::min<int64_t>(units, tiles));
-    const int64_t waves = tct::ceil_div(tiles, units);
     pl->tile_m = tile_m;
     pl->tile_n = tile_n;
     pl->tile_k = kTileK;
     pl->stages = stages;
     pl->group_m = opt && opt->group_m ? opt->group_m : kDefaultGroupM;
-    pl->grid = static_cast<int32_t>(units * cg);
-    pl->tiles = tiles;
-    pl->waves = waves;
-    pl->wave_efficiency = static_cast<double>(M) * N / (static_cast<double>(waves) * units * tile_m * tile_n);
+    pl->grid = static_cast<int32_t>(best_sp.units * cg);
+    pl->tiles = best_sp.tiles;
+    pl->waves = best_sp.waves;
+    pl->wave_efficiency = static_cast<double>(M) * N /
+                          (static_cast<double>(best_sp.waves) * best_sp.units * tile_m * tile_n);
     pl->smem_bytes = smem;
     pl->pack_a = (K > 0 && !tma_ok(A, lda)) ? 1 : 0;
     pl->pack_b = (K > 0 && !tma_ok(B, ldb)) ? 1 : 0;
     pl->cta_group = cg;
+    pl->units = static_cast<int32_t>(best_sp.units);
+    pl->stream_k_tiles = static_cast<int32_t>(best_sp.split_tiles);
+    pl->effective_waves = best_sp.eff_waves;
     return GEMM_OK;
+}
+
+// Kernel parameters for a plan (the caller sets `workspace` when stream-K is used).
+tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t N, int64_t K, int64_t ldc,
+                              int timeout_ms)
+{
+    tct::KernelParams p;
+    p.C = C;
+    p.ldc = ldc;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.num_m = static_cast<int32_t>(tct::ceil_div(M, pl.tile_m));
+    p.num_n = static_cast<int32_t>(tct::ceil_div(N, pl.tile_n));
+    p.num_kb = static_cast<int32_t>(tct::ceil_div(K, kTileK));
+    p.num_tiles = static_cast<int32_t>(pl.tiles);
+    p.group_m = pl.group_m;
+    p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 1 : 0;
+    p.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
+    p.units = pl.units;
+    p.dp_tiles = static_cast<int32_t>(pl.tiles - pl.stream_k_tiles);
+    p.split_tiles = pl.stream_k_tiles;
+    p.workspace = nullptr;
+    p.flags = nullptr;
+    return p;
+}
+
+// Split-tile workspace: one part (the second k-half) per split tile, then one flag per split
+// tile and CTA rank.
+int64_t split_parts_bytes(const gemm_plan &pl)
+{
+    if (pl.stream_k_tiles <= 0) return 0;
+    return static_cast<int64_t>(pl.stream_k_tiles) * pl.tile_m * pl.tile_n * 4;
+}
+
+int64_t split_flags_bytes(const gemm_plan &pl)
+{
+    if (pl.stream_k_tiles <= 0) return 0;
+    return round_up(static_cast<int64_t>(pl.stream_k_tiles) * pl.cta_group * 4, 256);
+}
+
+// 2-D FP32 tensor map over the split parts: rows of tile_n floats, boxes of tile_n x 32.
+gemm_status encode_parts(CUtensorMap *m, const float *base, int64_t rows, int tile_n)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    gemm_status st = get_encoder(&enc);
+    if (st != GEMM_OK) return st;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(tile_n), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(tile_n) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(tile_n), 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 // Co-resident CTA pairs on the current device for the pair kernels (queried once).
@@ -256,15 +399,22 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
     if (st != GEMM_OK) return st;
 
     // Operands whose rows do not start on 16-byte boundaries are copied first (TMA needs
-    // 16-byte aligned bases and row strides); the copy is stream-ordered.
+    // 16-byte aligned bases and row strides); the copy is stream-ordered.  The same
+    // stream-ordered block holds the stream-K partial tiles.
     const void *a_use = A, *b_use = B;
     int64_t lda_use = lda, ldb_use = ldb;
+    const int64_t lda_p = round_up(K, 8), ldb_p = round_up(N, 8);
+    const int64_t a_bytes = pl.pack_a ? round_up(M * lda_p * 2, 256) : 0;
+    const int64_t b_bytes = pl.pack_b ? round_up(K * ldb_p * 2, 256) : 0;
+    const int64_t w_bytes = split_parts_bytes(pl), f_bytes = split_flags_bytes(pl);
     void *ws = nullptr;
-    if (pl.pack_a || pl.pack_b) {
-        const int64_t lda_p = round_up(K, 8), ldb_p = round_up(N, 8);
-        const int64_t a_bytes = pl.pack_a ? round_up(M * lda_p * 2, 256) : 0;
-        const int64_t b_bytes = pl.pack_b ? round_up(K * ldb_p * 2, 256) : 0;
-        if (cudaMallocAsync(&ws, static_cast<size_t>(a_bytes + b_bytes), s) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (a_bytes + b_bytes + w_bytes + f_bytes > 0) {
+        cudaMemPool_t pool = nullptr;
+        st = device_pool(&pool);
+        if (st != GEMM_OK) return st;
+        if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes + w_bytes + f_bytes), pool, s) !=
+            cudaSuccess)
+            return GEMM_ERR_CUDA;
         uint8_t *w = static_cast<uint8_t *>(ws);
         cudaError_t e = cudaSuccess;
         if (pl.pack_a) {
@@ -277,6 +427,8 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
             b_use = w + a_bytes;
             ldb_use = ldb_p;
         }
+        if (e == cudaSuccess && f_bytes)  // the split tiles' flags start lowered
+            e = cudaMemsetAsync(w + a_bytes + b_bytes + w_bytes, 0, static_cast<size_t>(f_bytes), s);
         if (e != cudaSuccess) {
             cudaFreeAsync(ws, s);
             return GEMM_ERR_CUDA;
@@ -287,21 +439,18 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
     st = encode_fp16_2d(&ta, a_use, M, K, lda_use, kTileM);
     if (st == GEMM_OK) st = encode_fp16_2d(&tb, b_use, K, N, ldb_use, kTileK);
     if (st == GEMM_OK) {
-        tct::KernelParams p;
-        p.C = C;
-        p.ldc = ldc;
-        p.M = static_cast<int32_t>(M);
-        p.N = static_cast<int32_t>(N);
-        p.K = static_cast<int32_t>(K);
-        p.num_m = static_cast<int32_t>(tct::ceil_div(M, pl.tile_m));
-        p.num_n = static_cast<int32_t>(tct::ceil_div(N, pl.tile_n));
-        p.num_kb = static_cast<int32_t>(tct::ceil_div(K, kTileK));
-        p.num_tiles = static_cast<int32_t>(pl.tiles);
-        p.group_m = pl.group_m;
-        p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 1 : 0;
         const int tmo = opt && opt->timeout_ms ? opt->timeout_ms : kDefaultTimeoutMs;
-        p.timeout_ns = static_cast<uint64_t>(tmo) * 1000000ull;
-        st = to_status(tct::launch_gemm(ta, tb, p, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
+        tct::KernelParams p = make_params(pl, C, M, N, K, ldc, tmo);
+        CUtensorMap tp;
+        std::memset(&tp, 0, sizeof(tp));
+        if (w_bytes) {
+            uint8_t *w = static_cast<uint8_t *>(ws) + a_bytes + b_bytes;
+            p.workspace = reinterpret_cast<float *>(w);
+            p.flags = reinterpret_cast<unsigned int *>(w + w_bytes);
+            st = encode_parts(&tp, p.workspace, static_cast<int64_t>(pl.stream_k_tiles) * pl.tile_m, pl.tile_n);
+        }
+        if (st == GEMM_OK)
+            st = to_status(tct::launch_gemm(ta, tb, tp, p, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
     }
     if (ws) {
         if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
@@ -334,6 +483,29 @@ gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int6
     // Alignment of the base pointers is unknown here: assume 16-byte aligned bases.
     const void *aligned = reinterpret_cast<const void *>(uintptr_t{256});
     return make_plan(M, N, K, lda, ldb, sms, pairs, opt, aligned, aligned, out);
+}
+
+gemm_status gemm_f16_f32_work_item(int64_t M, int64_t N, int64_t K, int32_t num_sms, const gemm_options *opt,
+                                   int32_t unit, int32_t idx, gemm_work *out)
+{
+    if (!out || num_sms <= 0 || unit < 0 || idx < 0) return GEMM_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_ARG;
+    gemm_status st = check_options(opt);
+    if (st != GEMM_OK) return st;
+    const void *aligned = reinterpret_cast<const void *>(uintptr_t{256});
+    gemm_plan pl;
+    st = make_plan(M, N, K, K, N, num_sms, num_sms / 2, opt, aligned, aligned, &pl);
+    if (st != GEMM_OK) return st;
+    if (unit >= pl.units) return GEMM_ERR_INVALID_ARG;
+    const tct::KernelParams p = make_params(pl, nullptr, M, N, K, N, kDefaultTimeoutMs);
+    tct::WorkItem w;
+    if (!tct::work_item(p, unit, idx, w)) return GEMM_ERR_INVALID_ARG;
+    out->tile = w.tile;
+    out->kb0 = w.kb0;
+    out->kb1 = w.kb1;
+    out->mode = w.mode;
+    out->part = w.part;
+    return GEMM_OK;
 }
 
 gemm_status gemm_tile_coord(int64_t t, int64_t num_m, int64_t num_n, int32_t group_m, int64_t *tile_row,
@@ -439,7 +611,8 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
     if (K == 0) return to_status(tct::launch_fill_zero(C, ldc, M, N, dev.sms, s));
 
     gemm_plan pl;
-    st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), nullptr, A, B, &pl);
+    st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), nullptr, A, B, &pl,
+                   /*allow_split=*/false);
     if (st != GEMM_OK) return st;
 
     const void *a_use = A, *b_use = B;
@@ -466,18 +639,8 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
     st = encode_fp16_2d(&ta, a_use, M, K, lda_use, kTileM);
     if (st == GEMM_OK) st = encode_fp16_2d(&tb, b_use, K, N, ldb_use, kTileK);
     if (st != GEMM_OK) return st;
-    tct::KernelParams p;
-    p.C = C;
-    p.ldc = ldc;
-    p.M = static_cast<int32_t>(M);
-    p.N = static_cast<int32_t>(N);
-    p.K = static_cast<int32_t>(K);
-    p.num_m = static_cast<int32_t>(tct::ceil_div(M, pl.tile_m));
-    p.num_n = static_cast<int32_t>(tct::ceil_div(N, pl.tile_n));
-    p.num_kb = static_cast<int32_t>(tct::ceil_div(K, kTileK));
-    p.num_tiles = static_cast<int32_t>(pl.tiles);
-    p.group_m = pl.group_m;
-    p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 1 : 0;
-    p.timeout_ns = static_cast<uint64_t>(kDefaultTimeoutMs) * 1000000ull;
-    return to_status(tct::launch_gemm(ta, tb, p, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
+    const tct::KernelParams p = make_params(pl, C, M, N, K, ldc, kDefaultTimeoutMs);
+    CUtensorMap tp;  // no split tiles on this path
+    std::memset(&tp, 0, sizeof(tp));
+    return to_status(tct::launch_gemm(ta, tb, tp, p, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
 }

@@ -20,7 +20,66 @@ struct KernelParams {
     int32_t group_m;
     int32_t vec_store;  // 1 when C is 16-byte aligned and ldc % 4 == 0
     uint64_t timeout_ns;
+    // Work split.  `units` CTAs (cta_group 1) or CTA pairs (cta_group 2) first take whole
+    // tiles 0 .. dp_tiles-1 (tile u + i * units goes to unit u).  The last split_tiles tiles
+    // (the partial last wave; 2 * split_tiles <= units) are each split into two halves of
+    // the k-loop: unit j does the first half of tail tile j and owns it, unit split_tiles + j
+    // the second half, which it writes to workspace slot j (tile_rows x tile_n FP32) before
+    // raising flag[j * cta_group + rank]; the owner then adds that part to its own and
+    // stores the tile.
+    int32_t units;
+    int32_t dp_tiles;
+    int32_t split_tiles;
+    float *workspace;
+    unsigned int *flags;
 };
+
+enum WorkMode : int32_t {
+    WORK_STORE = 0,    // store the accumulator to C
+    WORK_FIXUP = 1,    // add the part in workspace slot `part`, then store to C
+    WORK_PARTIAL = 2,  // store the accumulator to workspace slot `part`, raise its flag
+};
+
+// One piece of work of a unit: k-blocks [kb0, kb1) of linear tile `tile`.
+struct WorkItem {
+    int32_t tile;
+    int32_t kb0, kb1;
+    int32_t mode;
+    int32_t part;  // workspace slot (split tiles), else -1
+};
+
+// The idx-th work item of unit u (false when the unit has no more).
+#if defined(__CUDACC__)
+__host__ __device__
+#endif
+inline bool work_item(const KernelParams &p, int32_t u, int32_t idx, WorkItem &it)
+{
+    // whole tiles u, u + units, ... below dp_tiles
+    const int32_t waves = u < p.dp_tiles ? (p.dp_tiles - 1 - u) / p.units + 1 : 0;
+    it.part = -1;
+    if (idx < waves) {
+        it.tile = u + idx * p.units;
+        it.kb0 = 0;
+        it.kb1 = p.num_kb;
+        it.mode = WORK_STORE;
+        return true;
+    }
+    if (idx != waves || u >= 2 * p.split_tiles) return false;
+    const int32_t j = u < p.split_tiles ? u : u - p.split_tiles;
+    const int32_t half = p.num_kb / 2;
+    it.tile = p.dp_tiles + j;
+    it.part = j;
+    if (u < p.split_tiles) {
+        it.kb0 = 0;
+        it.kb1 = half;
+        it.mode = WORK_FIXUP;
+    } else {
+        it.kb0 = half;
+        it.kb1 = p.num_kb;
+        it.mode = WORK_PARTIAL;
+    }
+    return true;
+}
 
 // Compiled (cta_group, tile_n, stages) variants of the main kernel.  cta_group 1: 128 x
 // tile_n tiles, one CTA each; per stage 16 KB of A + tile_n * 128 B of B.  cta_group 2:
@@ -41,11 +100,15 @@ struct KernelParams {
 
 int variant_smem_bytes(int cta_group, int tile_n, int stages);
 
+// 1 if the variant's stage buffers can hold a split tile's other half in its epilogue.
+int variant_split_ok(int cta_group, int tile_n, int stages);
+
 // Co-resident clusters of the variant on the current device (-1 if the query fails).
 int variant_max_clusters(int cta_group, int tile_n, int stages);
 
-cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const KernelParams &p, int cta_group,
-                        int tile_n, int stages, int grid, cudaStream_t stream);
+// tp: 2-D FP32 map of the split-tile parts (box tile_n x 32), unused when split_tiles == 0.
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const KernelParams &p,
+                        int cta_group, int tile_n, int stages, int grid, cudaStream_t stream);
 
 cudaError_t launch_pack(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows,
                         int64_t cols, int num_sms, cudaStream_t stream);

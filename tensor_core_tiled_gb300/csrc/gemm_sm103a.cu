@@ -59,7 +59,10 @@ struct Cfg {
     static constexpr int STAGE_TX = CG * (A_STAGE + B_STAGE);  // bytes counted on one full barrier
     static constexpr int EPI_WARPS = 4;
     static constexpr int EPI_BYTES = EPI_WARPS * 32 * 32 * 4;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int NUM_BARS = 2 * STAGES + 6 + EPI_WARPS;
+    // A split tile's part (32 rows x BN FP32 per epilogue warp) is loaded into the stage
+    // buffers, which are idle by then; only variants with room for it split tiles.
+    static constexpr bool SPLIT_OK = STAGES * (A_STAGE + B_STAGE) >= EPI_WARPS * 32 * BN * 4;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM_BYTES =
         1024 + STAGES * (A_STAGE + B_STAGE) + EPI_BYTES + NUM_BARS * 8 + 16;
@@ -75,6 +78,7 @@ enum WaitSite : unsigned {
     SITE_MMA_TMEM_EMPTY = 3,
     SITE_EPI_TMEM_FULL = 4,
     SITE_PRODUCER_TAIL = 5,
+    SITE_EPI_PARTS = 6,
 };
 
 __device__ __forceinline__ void record_timeout(volatile int *abort_flag, unsigned site)
@@ -113,12 +117,25 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
     }
 }
 
+// Destination of one accumulator: element (r, c) of the tile goes to base[r * ld + c] for
+// r < rows and c < cols (coordinates relative to `base`); `vec` allows 16-byte stores,
+// `streaming` marks stores that are not read again.  When `part` is set, element (r, c) of
+// this warp's 32 rows of the split tile's other half, staged in shared memory as 32 rows
+// of BN floats, is added before the store.
+struct TileDst {
+    float *base;
+    int64_t ld;
+    int64_t rows, cols;
+    bool vec;
+    bool streaming;
+    const float *part;
+};
+
 // One accumulator buffer (this warp's 32 TMEM lanes x BN columns) to global memory.
 // `release` is called by lane 0 once every column has been read from TMEM.
 template <int BN, typename Release>
-__device__ __forceinline__ void store_accumulator(uint32_t t_row, int64_t row_base, int64_t col_base,
-                                                  const KernelParams &p, float *stage, int lane, bool vec,
-                                                  Release release)
+__device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst &d, int64_t row_base,
+                                                  int64_t col_base, float *stage, int lane, Release release)
 {
     for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t r[32];
@@ -145,17 +162,27 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, int64_t row_ba
 #pragma unroll
         for (int rr0 = 0; rr0 < 32; rr0 += 4) {
             const int rr = rr0 + (lane >> 3);
-            const float4 v = reinterpret_cast<const float4 *>(stage + rr * 32)[jj ^ (rr & 7)];
+            float4 v = reinterpret_cast<const float4 *>(stage + rr * 32)[jj ^ (rr & 7)];
+            if (d.part) {
+                const float4 a = *reinterpret_cast<const float4 *>(d.part + rr * BN + ch * 32 + jj * 4);
+                v.x += a.x;
+                v.y += a.y;
+                v.z += a.z;
+                v.w += a.w;
+            }
             const int64_t grow = row_base + rr;
-            if (grow < p.M) {
-                float *dst = p.C + grow * p.ldc + gcol;
-                if (vec && gcol + 3 < p.N) {
-                    __stcs(reinterpret_cast<float4 *>(dst), v);
+            if (grow < d.rows) {
+                float *dst = d.base + grow * d.ld + gcol;
+                if (d.vec && gcol + 3 < d.cols) {
+                    if (d.streaming)
+                        __stcs(reinterpret_cast<float4 *>(dst), v);
+                    else
+                        __stcg(reinterpret_cast<float4 *>(dst), v);
                 } else {
-                    if (gcol + 0 < p.N) __stcs(dst + 0, v.x);
-                    if (gcol + 1 < p.N) __stcs(dst + 1, v.y);
-                    if (gcol + 2 < p.N) __stcs(dst + 2, v.z);
-                    if (gcol + 3 < p.N) __stcs(dst + 3, v.w);
+                    if (gcol + 0 < d.cols) __stcs(dst + 0, v.x);
+                    if (gcol + 1 < d.cols) __stcs(dst + 1, v.y);
+                    if (gcol + 2 < d.cols) __stcs(dst + 2, v.z);
+                    if (gcol + 3 < d.cols) __stcs(dst + 3, v.w);
                 }
             }
         }
@@ -163,10 +190,27 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, int64_t row_ba
     }
 }
 
+// Waits until *flag is raised (by another CTA), bounded like the pipeline waits.
+__device__ __forceinline__ bool wait_flag(const unsigned int *flag, uint64_t limit_ns, volatile int *abort_flag)
+{
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (flag_acquire_gpu(flag) == 0u) {
+        if ((++spins & 15u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                record_timeout(abort_flag, SITE_EPI_PARTS);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
 template <int CG, int BN, int STAGES>
 __global__ void __launch_bounds__(192, 1)
-    gemm_f16_f32_tcgen05(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB, const KernelParams p)
+    gemm_f16_f32_tcgen05(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmP, const KernelParams p)
 {
     using Cf = Cfg<CG, BN, STAGES>;
     constexpr bool kPair = CG == 2;
@@ -186,13 +230,14 @@ __global__ void __launch_bounds__(192, 1)
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    const uint32_t part_bar = bar0 + 8u * (2 * STAGES + 5);  // epilogue warps done with a part
+    auto pload_bar = [&](int e) { return bar0 + 8u * (2 * STAGES + 6 + e); };  // part load, warp e
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // CTA rank inside the pair (0 = the CTA that issues the MMAs) and the tile walk.
+    // CTA rank inside the pair (0 = the CTA that issues the MMAs) and this CTA's work unit.
     const uint32_t rank = kPair ? cluster_ctarank() : 0u;
-    const int first_tile = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int tile_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -204,6 +249,8 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(tempty_bar(b), Cf::EPI_WARPS * CG);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(part_bar, Cf::EPI_WARPS);
+        for (int e = 0; e < Cf::EPI_WARPS; ++e) mbar_init(pload_bar(e), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -236,11 +283,12 @@ __global__ void __launch_bounds__(192, 1)
             bool issued[STAGES];
             for (int i = 0; i < STAGES; ++i) issued[i] = false, issued_parity[i] = 0;
             bool ok = true;
-            for (int t = first_tile; ok && t < p.num_tiles; t += tile_step) {
-                const TileCoord c = tile_coord(t, p.num_m, p.num_n, p.group_m);
+            WorkItem w;
+            for (int idx = 0; ok && work_item(p, unit, idx, w); ++idx) {
+                const TileCoord c = tile_coord(w.tile, p.num_m, p.num_n, p.group_m);
                 const int32_t m0 = c.m * (Cf::BM * CG) + static_cast<int32_t>(rank) * Cf::BM;
                 const int32_t n0 = c.n * BN + static_cast<int32_t>(rank) * Cf::BN_CTA;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_or_abort<kPair>(empty_bar(s), ph ^ 1u, limit, abort_flag,
                                               SITE_PRODUCER_EMPTY)) {
                         ok = false;
@@ -303,7 +351,8 @@ __global__ void __launch_bounds__(192, 1)
             int it = 0;
             bool ok = true;
             bool any_mma = false;
-            for (int t = first_tile; ok && t < p.num_tiles; t += tile_step, ++it) {
+            WorkItem w;
+            for (; ok && work_item(p, unit, it, w); ++it) {
                 const int b = it & 1;
                 const uint32_t use = static_cast<uint32_t>(it >> 1);
                 if (!wait_or_abort<kPair>(tempty_bar(b), (use & 1u) ^ 1u, limit, abort_flag,
@@ -313,7 +362,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_or_abort<kPair>(full_bar(s), ph, limit, abort_flag, SITE_MMA_FULL)) {
                         ok = false;
                         break;
@@ -329,7 +378,7 @@ __global__ void __launch_bounds__(192, 1)
                         // B: N-major, 64-column boxes B_SUB bytes apart (leading offset),
                         // 8-row K groups 1024 B apart (stride offset); 16 K rows = 2048 B.
                         const uint64_t bdesc = smem_desc_sw128(b_base + kk * 2048, Cf::B_SUB, 1024);
-                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                        const uint32_t acc = (kb != w.kb0 || kk != 0) ? 1u : 0u;
                         if constexpr (kPair)
                             tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, acc);
                         else
@@ -365,28 +414,65 @@ __global__ void __launch_bounds__(192, 1)
         // ------------------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         float *stage = sEpi + (warp - 2) * 32 * 32;
-        const bool vec = p.vec_store != 0;
         int it = 0;
-        for (int t = first_tile; t < p.num_tiles; t += tile_step, ++it) {
+        WorkItem w;
+        for (; work_item(p, unit, it, w); ++it) {
             const int b = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             bool ok = wait_or_abort<kPair>(tfull_bar(b), use & 1u, limit, abort_flag, SITE_EPI_TMEM_FULL);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const TileCoord c = tile_coord(t, p.num_m, p.num_n, p.group_m);
-            const int64_t row_base = static_cast<int64_t>(c.m) * (Cf::BM * CG) +
-                                     static_cast<int64_t>(rank) * Cf::BM + q * 32;
-            const int64_t col_base = static_cast<int64_t>(c.n) * BN;
+            const TileCoord c = tile_coord(w.tile, p.num_m, p.num_n, p.group_m);
+            const int64_t lane_rows = static_cast<int64_t>(rank) * Cf::BM + q * 32;  // tile-local
+            constexpr int64_t kTileElems = static_cast<int64_t>(Cf::BM * CG) * BN;
+            TileDst d{p.C, p.ldc, p.M, p.N, p.vec_store != 0, true, nullptr};
+            int64_t row_base = static_cast<int64_t>(c.m) * (Cf::BM * CG) + lane_rows;
+            int64_t col_base = static_cast<int64_t>(c.n) * BN;
+            if (w.mode == WORK_PARTIAL) {
+                // second half of a split tile for its owner: the whole tile, tile-local rows
+                d = TileDst{p.workspace + w.part * kTileElems, BN, Cf::BM * CG, BN, true, false, nullptr};
+                row_base = lane_rows;
+                col_base = 0;
+            } else if (w.mode == WORK_FIXUP) {
+                if constexpr (Cf::SPLIT_OK) {
+                    // The other half, once its unit has published it, comes in by TMA: this
+                    // warp's 32 rows into the (idle) stage buffers, then it is added below.
+                    ok = wait_flag(p.flags + w.part * CG + rank, limit, abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    float *part = reinterpret_cast<float *>(sA) + (warp - 2) * 32 * BN;
+                    const uint32_t pb = pload_bar(warp - 2);
+                    if (lane == 0) {
+                        fence_proxy_async_all();
+                        mbar_arrive_expect_tx(pb, 32 * BN * 4);
+                        tma_load_2d(smem_u32(part), &tmP, 0,
+                                    static_cast<int32_t>(w.part * (Cf::BM * CG) + lane_rows), pb);
+                    }
+                    ok = wait_or_abort<false>(pb, 0u, limit, abort_flag, SITE_EPI_PARTS);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    d.part = part;
+                }
+            }
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(b * BN);
             if constexpr (kPair) {
                 const uint32_t te = map_to_cta(tempty_bar(b), 0);
-                store_accumulator<BN>(t_row, row_base, col_base, p, stage, lane, vec,
-                                      [&] { mbar_arrive_cluster(te); });
+                store_accumulator<BN>(t_row, d, row_base, col_base, stage, lane, [&] { mbar_arrive_cluster(te); });
             } else {
                 const uint32_t te = tempty_bar(b);
-                store_accumulator<BN>(t_row, row_base, col_base, p, stage, lane, vec, [&] { mbar_arrive(te); });
+                store_accumulator<BN>(t_row, d, row_base, col_base, stage, lane, [&] { mbar_arrive(te); });
+            }
+            if (w.mode == WORK_PARTIAL) {
+                // Publish this CTA's rows of the part to the owner once all four warps have
+                // written theirs (a unit writes at most one part, so the barrier's first phase).
+                __threadfence();
+                fence_proxy_async_all();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(part_bar);
+                if (warp == 2 && lane == 0 && wait_or_abort<false>(part_bar, 0u, limit, abort_flag, SITE_EPI_PARTS))
+                    flag_release_gpu(p.flags + w.part * CG + rank, 1u);
             }
         }
     }
@@ -407,15 +493,26 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------- helper kernels
 
 // Row copy into a buffer whose rows start on 16-byte boundaries (TMA's stride rule).
+// Each thread moves 8 consecutive elements of one row: 8 two-byte loads (the source rows
+// may start anywhere) and one 16-byte store; blockIdx.y walks the rows.
 __global__ void pack_rows_f16(const uint16_t *__restrict__ src, int64_t ld_src,
                               uint16_t *__restrict__ dst, int64_t ld_dst, int64_t rows, int64_t cols)
 {
-    const int64_t total = rows * cols;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / cols;
-        const int64_t c = i - r * cols;
-        dst[r * ld_dst + c] = src[r * ld_src + c];
+    const int64_t c8 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+    if (c8 >= cols) return;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const uint16_t *s = src + r * ld_src + c8;
+        uint16_t *d = dst + r * ld_dst + c8;
+        if (c8 + 8 <= cols) {
+            uint4 v;
+            v.x = static_cast<uint32_t>(s[0]) | (static_cast<uint32_t>(s[1]) << 16);
+            v.y = static_cast<uint32_t>(s[2]) | (static_cast<uint32_t>(s[3]) << 16);
+            v.z = static_cast<uint32_t>(s[4]) | (static_cast<uint32_t>(s[5]) << 16);
+            v.w = static_cast<uint32_t>(s[6]) | (static_cast<uint32_t>(s[7]) << 16);
+            *reinterpret_cast<uint4 *>(d) = v;
+        } else {
+            for (int64_t i = 0; i < cols - c8; ++i) d[i] = s[i];
+        }
     }
 }
 
@@ -450,8 +547,8 @@ static cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunc
 }
 
 template <int CG, int BN, int STAGES>
-static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const KernelParams &p,
-                                  int grid, cudaStream_t stream)
+static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp,
+                                  const KernelParams &p, int grid, cudaStream_t stream)
 {
     auto kern = gemm_f16_f32_tcgen05<CG, BN, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -459,7 +556,8 @@ static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, 
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config<CG, BN, STAGES>(grid, stream, attr);
-    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+    if (p.split_tiles > 0 && !Cfg<CG, BN, STAGES>::SPLIT_OK) return cudaErrorInvalidValue;
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tp, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -502,12 +600,21 @@ int variant_max_clusters(int cta_group, int tile_n, int stages)
     return -1;
 }
 
-cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const KernelParams &p, int cta_group,
-                        int tile_n, int stages, int grid, cudaStream_t stream)
+int variant_split_ok(int cta_group, int tile_n, int stages)
+{
+#define TCT_CASE(CG_, BN_, ST_) \
+    if (cta_group == CG_ && tile_n == BN_ && stages == ST_) return Cfg<CG_, BN_, ST_>::SPLIT_OK ? 1 : 0;
+    TCT_VARIANTS(TCT_CASE)
+#undef TCT_CASE
+    return 0;
+}
+
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const KernelParams &p,
+                        int cta_group, int tile_n, int stages, int grid, cudaStream_t stream)
 {
 #define TCT_CASE(CG_, BN_, ST_)                             \
     if (cta_group == CG_ && tile_n == BN_ && stages == ST_) \
-        return launch_variant<CG_, BN_, ST_>(ta, tb, p, grid, stream);
+        return launch_variant<CG_, BN_, ST_>(ta, tb, tp, p, grid, stream);
     TCT_VARIANTS(TCT_CASE)
 #undef TCT_CASE
     return cudaErrorInvalidValue;
@@ -516,13 +623,13 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Kern
 cudaError_t launch_pack(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows,
                         int64_t cols, int num_sms, cudaStream_t stream)
 {
+    (void)num_sms;
     if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const int64_t total = rows * cols;
-    int64_t blocks = (total + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
-    if (blocks > cap) blocks = cap;
-    pack_rows_f16<<<static_cast<int>(blocks), 256, 0, stream>>>(
-        static_cast<const uint16_t *>(src), ld_src, static_cast<uint16_t *>(dst), ld_dst, rows, cols);
+    const int64_t chunks = (cols + 7) / 8;
+    const unsigned gx = static_cast<unsigned>((chunks + 127) / 128);
+    const unsigned gy = static_cast<unsigned>(rows < 8192 ? rows : 8192);
+    pack_rows_f16<<<dim3(gx, gy, 1), 128, 0, stream>>>(static_cast<const uint16_t *>(src), ld_src,
+                                                         static_cast<uint16_t *>(dst), ld_dst, rows, cols);
     return cudaGetLastError();
 }
 

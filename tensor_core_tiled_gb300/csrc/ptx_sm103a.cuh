@@ -263,6 +263,26 @@ __device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t 
         : "memory");
 }
 
+// ---------------------------------------------------------------- cross-CTA flags
+
+// Orders this thread's generic-proxy memory accesses with its async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_all()
+{
+    asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+__device__ __forceinline__ void flag_release_gpu(unsigned int *flag, unsigned int v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int flag_acquire_gpu(const unsigned int *flag)
+{
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading- and

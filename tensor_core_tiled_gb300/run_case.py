@@ -1,7 +1,8 @@
 """Runs the GEMM on one shape a few times and prints the per-launch device time.
 
   python -m tensor_core_tiled_gb300.run_case --m 6144 --n 6144 --k 6144 [--launches 3]
-      [--warmup 2] [--tile-n 256] [--stages 4] [--group-m 8] [--max-ctas 0]
+      [--warmup 2] [--cta-group 2] [--tile-n 256] [--stages 6] [--group-m 8] [--max-ctas 0]
+      [--stream-k 0|1|2] [--flush-l2]
 
 Inputs are N(0,1) FP16 drawn on the device (no host generation), so the command is quick
 to start; it is meant for profiling one kernel on a chosen shape and for tuning sweeps.
@@ -25,6 +26,8 @@ def main():
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--group-m", type=int, default=0)
     ap.add_argument("--max-ctas", type=int, default=0)
+    ap.add_argument("--cta-group", type=int, default=0)
+    ap.add_argument("--stream-k", type=int, default=0, help="1 = whole tiles only, 2 = split the last wave")
     ap.add_argument("--flush-l2", action="store_true", help="write 512 MiB between launches")
     args = ap.parse_args()
 
@@ -33,7 +36,8 @@ def main():
     B = torch.randn(args.k, args.n, device="cuda", generator=g).half()
     C = torch.empty(args.m, args.n, device="cuda")
     flush = torch.empty(128 << 20, device="cuda") if args.flush_l2 else None
-    opts = dict(tile_n=args.tile_n, stages=args.stages, group_m=args.group_m, max_ctas=args.max_ctas)
+    opts = dict(tile_n=args.tile_n, stages=args.stages, group_m=args.group_m, max_ctas=args.max_ctas,
+                cta_group=args.cta_group, stream_k=args.stream_k)
     opts = {k: v for k, v in opts.items() if v}
     for _ in range(args.warmup):
         tct.matmul(A, B, C, **opts)

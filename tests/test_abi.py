@@ -118,18 +118,23 @@ def test_page_wave_quantisation_example(tct_lib):
 def test_planner_on_gb300_shapes(tct_lib):
     sms = 152
     p = tct.gemm_f16_f32_plan(8192, 8192, 8192, num_sms=sms)
-    # the CTA-pair 256x256 tile: 32 x 32 tiles over 76 pairs
+    # the CTA-pair 256x256 tile: 32 x 32 tiles over 76 pairs, 13 whole waves, the last 36
+    # tiles each split into two k-halves on 72 of the 76 pairs
     assert (p["cta_group"], p["tile_m"], p["tile_n"], p["tile_k"]) == (2, 256, 256, 64)
-    assert p["grid"] == sms and p["tiles"] == 32 * 32
+    assert p["grid"] == sms and p["tiles"] == 32 * 32 and p["units"] == sms // 2
     assert p["waves"] == -(-1024 // (sms // 2))
+    assert p["stream_k_tiles"] == 1024 - 13 * 76
+    assert p["effective_waves"] == pytest.approx(13.5)
     assert p["pack_a"] == 0 and p["pack_b"] == 0
-    # 4096^3: 4 waves of 256x256 pair tiles (84% filled) still beat the narrower tiles'
-    # fuller waves at their lower per-tile rate
+    # 4096^3: 3.5 waves of 256x256 pair tiles instead of 4 whole waves
     p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms)
-    assert (p["cta_group"], p["tile_n"], p["waves"]) == (2, 256, 4)
-    # the skinny, bandwidth-bound shape spreads over more SMs with the narrow 1-CTA tile
+    assert (p["cta_group"], p["tile_n"], p["waves"], p["stream_k_tiles"]) == (2, 256, 4, 256 - 3 * 76)
+    p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, stream_k=1)
+    assert p["stream_k_tiles"] == 0 and p["effective_waves"] == 4
+    # the skinny, bandwidth-bound shape keeps at least 128 of the 152 SMs streaming B
     p = tct.gemm_f16_f32_plan(128, 16384, 16384, num_sms=sms)
-    assert (p["cta_group"], p["tile_n"], p["grid"]) == (1, 128, 128)
+    busy = p["cta_group"] * min(p["units"], p["tiles"] * (2 if p["stream_k_tiles"] else 1))
+    assert busy >= 128
     # ragged leading dimensions are repacked before TMA
     p = tct.gemm_f16_f32_plan(17, 4097, 31, num_sms=sms)
     assert p["pack_a"] == 1 and p["pack_b"] == 1
@@ -148,3 +153,46 @@ def test_planner_on_gb300_shapes(tct_lib):
         assert 0 < p["smem_bytes"] <= 227 * 1024
     with pytest.raises(tct.GemmError):
         tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, cta_group=2, stages=2)
+
+
+@pytest.mark.parametrize("shape,opts", [
+    ((8192, 8192, 8192), {}), ((4096, 4096, 4096), {}), ((4096, 4096, 4096), {"stream_k": 1}),
+    ((128, 16384, 16384), {}), ((1000, 1100, 700), {"stream_k": 2}), ((777, 1500, 515), {"stream_k": 2, "cta_group": 1}),
+    ((300, 200, 150), {"stream_k": 2}), ((1, 1000, 640), {"stream_k": 2, "cta_group": 1, "tile_n": 128}),
+    ((2000, 3000, 5000), {"stream_k": 2, "max_ctas": 50}), ((1792, 1792, 1792), {}), ((6144, 6144, 6144), {}),
+])
+def test_work_items_cover_every_k_block_once(tct_lib, shape, opts):
+    """The library's own work split: each (tile, k-block) pair of the plan belongs to exactly
+    one work item of one unit; every split tile has exactly one owner (first k-half, mode 1)
+    and one writer of its second half (mode 2), sharing one workspace slot."""
+    M, N, K = shape
+    sms = 152
+    p = tct.gemm_f16_f32_plan(M, N, K, num_sms=sms, **opts)
+    kb = -(-K // 64)
+    seen = {}
+    owners, writers = {}, {}
+    for u in range(p["units"]):
+        idx = 0
+        while True:
+            it = tct.gemm_f16_f32_work_item(M, N, K, sms, u, idx, **opts)
+            if it is None:
+                break
+            tile, kb0, kb1, mode, part = it["tile"], it["kb0"], it["kb1"], it["mode"], it["part"]
+            assert 0 <= tile < p["tiles"] and 0 <= kb0 < kb1 <= kb
+            if mode == tct.WORK_STORE:
+                assert (kb0, kb1) == (0, kb) and part == -1
+            else:
+                assert tile >= p["tiles"] - p["stream_k_tiles"]
+                book = owners if mode == tct.WORK_FIXUP else writers
+                assert tile not in book
+                book[tile] = (u, part, kb0, kb1)
+            for k in range(kb0, kb1):
+                assert (tile, k) not in seen
+                seen[(tile, k)] = u
+            idx += 1
+    assert len(seen) == p["tiles"] * kb
+    assert set(owners) == set(writers) and len(owners) == p["stream_k_tiles"]
+    for tile, (u, part, kb0, kb1) in owners.items():
+        wu, wpart, wkb0, wkb1 = writers[tile]
+        assert wu != u and wpart == part and kb0 == 0 and kb1 == wkb0 and wkb1 == kb
+    assert sorted(v[1] for v in owners.values()) == list(range(p["stream_k_tiles"]))

@@ -177,15 +177,15 @@ VARIANT_OPTS = [
 
 @pytest.mark.parametrize("opts", VARIANT_OPTS)
 def test_variants_and_schedules_agree(opts):
-    """For a given CTA grouping and tile width, every pipeline depth, launch order and grid
-    size gives the same bits (the k order inside a tile never changes); every variant
-    passes the oracle."""
+    """For a given CTA grouping and tile width, with whole tiles only, every pipeline depth,
+    launch order and grid size gives the same bits (the k order inside a tile never
+    changes); every variant passes the oracle."""
     rng = np.random.default_rng(23)
     M, N, K = 777, 1500, 515
     A, B = inputs.normal_pair(rng, M, N, K)
     dA, dB = dev16(A), dev16(B)
-    ref = tct.matmul(dA, dB, cta_group=opts["cta_group"], tile_n=opts["tile_n"])
-    C = tct.matmul(dA, dB, **opts)
+    ref = tct.matmul(dA, dB, cta_group=opts["cta_group"], tile_n=opts["tile_n"], stream_k=1)
+    C = tct.matmul(dA, dB, stream_k=1, **opts)
     torch.cuda.synchronize()
     assert torch.equal(C.view(torch.int32), ref.view(torch.int32))
     assert within_tol(C.cpu().numpy(), oracle.gemm_f32(A, B), K)
@@ -214,6 +214,47 @@ def test_every_variant_on_ragged_and_integer_inputs(cta_group, tile_n):
     rng = np.random.default_rng(33)
     A, B = inputs.integer_pair(rng, 700, 900, 1100)
     assert bit_exact(gpu_gemm(A, B, cta_group=cta_group, tile_n=tile_n), oracle.gemm_f32(A, B))
+
+
+STREAM_K_CASES = [
+    ((1000, 1100, 700), dict(stream_k=2)),
+    ((777, 1500, 515), dict(stream_k=2, cta_group=1, tile_n=256)),
+    ((777, 1000, 515), dict(stream_k=2, cta_group=1, tile_n=128)),
+    ((300, 200, 150), dict(stream_k=2)),
+    ((129, 65, 33 * 64), dict(stream_k=2, cta_group=1)),
+    ((2000, 3000, 5000), dict(stream_k=2, max_ctas=150)),
+    ((2000, 3000, 5000), dict(stream_k=2, cta_group=1, tile_n=256, max_ctas=140)),
+    ((1, 1000, 640), dict(stream_k=2, cta_group=1, tile_n=128)),
+    ((4096, 4096, 1000), dict(stream_k=2, cta_group=2, tile_n=256)),
+]
+
+
+@pytest.mark.parametrize("shape,opts", STREAM_K_CASES)
+def test_stream_k_split(shape, opts):
+    """Tiles whose k-loop is split into two halves on two units: the second half through the
+    workspace and the owner's add give the oracle's result, bit-exact on integer inputs, and
+    the same bits on every run."""
+    M, N, K = shape
+    plan = tct.gemm_f16_f32_plan(M, N, K, **opts)
+    assert plan["stream_k_tiles"] > 0
+    rng = np.random.default_rng(41)
+    A, B = inputs.normal_pair(rng, M, N, K)
+    dA, dB = dev16(A), dev16(B)
+    C = tct.matmul(dA, dB, **opts)
+    again = tct.matmul(dA, dB, **opts)
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int32), again.view(torch.int32))
+    assert within_tol(C.cpu().numpy(), oracle.gemm_f32(A, B), K)
+    Ai, Bi = inputs.integer_pair(rng, M, N, K)
+    assert bit_exact(gpu_gemm(Ai, Bi, **opts), oracle.gemm_f32(Ai, Bi))
+
+
+def test_stream_k_and_whole_tiles_agree_on_integers():
+    rng = np.random.default_rng(43)
+    A, B = inputs.integer_pair(rng, 2048, 2304, 3000)
+    whole = gpu_gemm(A, B, stream_k=1)
+    split = gpu_gemm(A, B, stream_k=2)
+    assert bit_exact(whole, split) and bit_exact(split, oracle.gemm_f32(A, B))
 
 
 # ---- full-size workloads: sampled outputs -------------------------------------------------
