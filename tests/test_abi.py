@@ -126,10 +126,13 @@ def test_planner_on_gb300_shapes(tct_lib):
     assert p["stream_k_tiles"] == 1024 - 13 * 76
     assert p["effective_waves"] == pytest.approx(13.5)
     assert p["pack_a"] == 0 and p["pack_b"] == 0
-    # 4096^3: 3.5 waves of 256x256 pair tiles instead of 4 whole waves
+    # 4096^3: splitting the 28 tail tiles would cost more than the half tile it saves (the
+    # k-loop is short), so 4 whole waves; with 4x the k-loop the split pays
     p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms)
-    assert (p["cta_group"], p["tile_n"], p["waves"], p["stream_k_tiles"]) == (2, 256, 4, 256 - 3 * 76)
-    p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, stream_k=1)
+    assert (p["cta_group"], p["tile_n"], p["waves"], p["stream_k_tiles"]) == (2, 256, 4, 0)
+    p = tct.gemm_f16_f32_plan(4096, 4096, 16384, num_sms=sms)
+    assert p["stream_k_tiles"] == 256 - 3 * 76 and p["effective_waves"] == 3.5
+    p = tct.gemm_f16_f32_plan(4096, 4096, 16384, num_sms=sms, stream_k=1)
     assert p["stream_k_tiles"] == 0 and p["effective_waves"] == 4
     # the skinny, bandwidth-bound shape keeps at least 128 of the 152 SMs streaming B
     p = tct.gemm_f16_f32_plan(128, 16384, 16384, num_sms=sms)
