@@ -79,6 +79,11 @@ TCT_API gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t
  *               (the second half goes through a stream-ordered workspace and is added by the
  *               first half's unit, always in the same order, so results are reproducible);
  *               0 = let the planner decide.
+ *   fault_inject: test hook for the device-side timeout path; 0 in normal use.  Bit 0: the
+ *               unit computing the second k-half of a split tile never publishes it, so the
+ *               tile's owner waits until timeout_ms runs out, records
+ *               GEMM_ERR_DEVICE_TIMEOUT (read by gemm_f16_f32_get_error) and returns without
+ *               storing that tile.  Nothing faults, traps or hangs; later calls are unaffected.
  */
 typedef struct gemm_options {
     int32_t group_m;
@@ -88,7 +93,7 @@ typedef struct gemm_options {
     int32_t timeout_ms;
     int32_t cta_group;
     int32_t stream_k;
-    int32_t reserved[1]; /* must be zero */
+    int32_t fault_inject;
 } gemm_options;
 
 /* gemm_f16_f32 with explicit tuning options (opt may be NULL = all defaults). */

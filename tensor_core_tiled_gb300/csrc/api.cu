@@ -152,7 +152,7 @@ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 gemm_status check_options(const gemm_options *opt)
 {
     if (!opt) return GEMM_OK;
-    if (opt->reserved[0] != 0) return GEMM_ERR_INVALID_ARG;
+    if (opt->fault_inject < 0 || opt->fault_inject > 1) return GEMM_ERR_INVALID_ARG;
     if (opt->stream_k < 0 || opt->stream_k > 2) return GEMM_ERR_INVALID_ARG;
     if (opt->group_m < 0 || opt->group_m > 256) return GEMM_ERR_INVALID_ARG;
     if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return GEMM_ERR_INVALID_ARG;
@@ -327,6 +327,7 @@ tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t 
     p.split_tiles = pl.stream_k_tiles;
     p.workspace = nullptr;
     p.flags = nullptr;
+    p.fault_inject = 0;
     return p;
 }
 
@@ -441,6 +442,7 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
     if (st == GEMM_OK) {
         const int tmo = opt && opt->timeout_ms ? opt->timeout_ms : kDefaultTimeoutMs;
         tct::KernelParams p = make_params(pl, C, M, N, K, ldc, tmo);
+        p.fault_inject = opt ? opt->fault_inject : 0;
         CUtensorMap tp;
         std::memset(&tp, 0, sizeof(tp));
         if (w_bytes) {

@@ -32,6 +32,7 @@ struct KernelParams {
     int32_t split_tiles;
     float *workspace;
     unsigned int *flags;
+    int32_t fault_inject;  // bit 0: never publish a split tile's second half (timeout test)
 };
 
 enum WorkMode : int32_t {

@@ -471,7 +471,8 @@ __global__ void __launch_bounds__(192, 1)
                 fence_proxy_async_all();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(part_bar);
-                if (warp == 2 && lane == 0 && wait_or_abort<false>(part_bar, 0u, limit, abort_flag, SITE_EPI_PARTS))
+                if (warp == 2 && lane == 0 && wait_or_abort<false>(part_bar, 0u, limit, abort_flag, SITE_EPI_PARTS) &&
+                    !(p.fault_inject & 1))
                     flag_release_gpu(p.flags + w.part * CG + rank, 1u);
             }
         }
