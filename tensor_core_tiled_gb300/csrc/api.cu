@@ -417,17 +417,16 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
             cudaSuccess)
             return GEMM_ERR_CUDA;
         uint8_t *w = static_cast<uint8_t *>(ws);
-        cudaError_t e = cudaSuccess;
         if (pl.pack_a) {
-            e = tct::launch_pack(A, lda, w, lda_p, M, K, dev.sms, s);
             a_use = w;
             lda_use = lda_p;
         }
-        if (e == cudaSuccess && pl.pack_b) {
-            e = tct::launch_pack(B, ldb, w + a_bytes, ldb_p, K, N, dev.sms, s);
+        if (pl.pack_b) {
             b_use = w + a_bytes;
             ldb_use = ldb_p;
         }
+        cudaError_t e = tct::launch_pack2(pl.pack_a ? A : nullptr, lda, w, lda_p, M, K, pl.pack_b ? B : nullptr, ldb,
+                                          w + a_bytes, ldb_p, K, N, s);
         if (e == cudaSuccess && f_bytes)  // the split tiles' flags start lowered
             e = cudaMemsetAsync(w + a_bytes + b_bytes + w_bytes, 0, static_cast<size_t>(f_bytes), s);
         if (e != cudaSuccess) {
@@ -625,13 +624,14 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
         if (st != GEMM_OK) return st;
         uint8_t *w = static_cast<uint8_t *>(scratch);
         // Every element the GEMM reads is written here first; nothing needs clearing.
+        if (tct::launch_pack2(pack_a ? A : nullptr, lda, w, lda_p, M, K, pack_b ? B : nullptr, ldb, w + a_bytes,
+                              ldb_p, K, N, s) != cudaSuccess)
+            return GEMM_ERR_CUDA;
         if (pack_a) {
-            if (tct::launch_pack(A, lda, w, lda_p, M, K, dev.sms, s) != cudaSuccess) return GEMM_ERR_CUDA;
             a_use = w;
             lda_use = lda_p;
         }
         if (pack_b) {
-            if (tct::launch_pack(B, ldb, w + a_bytes, ldb_p, K, N, dev.sms, s) != cudaSuccess) return GEMM_ERR_CUDA;
             b_use = w + a_bytes;
             ldb_use = ldb_p;
         }

@@ -111,8 +111,11 @@ int variant_max_clusters(int cta_group, int tile_n, int stages);
 cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const KernelParams &p,
                         int cta_group, int tile_n, int stages, int grid, cudaStream_t stream);
 
-cudaError_t launch_pack(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows,
-                        int64_t cols, int num_sms, cudaStream_t stream);
+// Copies up to two FP16 operands (a NULL src skips one) into buffers with 16-byte aligned rows,
+// in one launch.
+cudaError_t launch_pack2(const void *src0, int64_t ld_src0, void *dst0, int64_t ld_dst0, int64_t rows0, int64_t cols0,
+                         const void *src1, int64_t ld_src1, void *dst1, int64_t ld_dst1, int64_t rows1, int64_t cols1,
+                         cudaStream_t stream);
 
 cudaError_t launch_fill_zero(float *C, int64_t ldc, int64_t rows, int64_t cols, int num_sms,
                              cudaStream_t stream);

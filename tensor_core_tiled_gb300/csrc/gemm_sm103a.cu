@@ -493,27 +493,36 @@ __global__ void __launch_bounds__(192, 1)
 
 // ---------------------------------------------------------------- helper kernels
 
-// Row copy into a buffer whose rows start on 16-byte boundaries (TMA's stride rule).
-// Each thread moves 8 consecutive elements of one row: 8 two-byte loads (the source rows
-// may start anywhere) and one 16-byte store; blockIdx.y walks the rows.
-__global__ void pack_rows_f16(const uint16_t *__restrict__ src, int64_t ld_src,
-                              uint16_t *__restrict__ dst, int64_t ld_dst, int64_t rows, int64_t cols)
+// Row copy into buffers whose rows start on 16-byte boundaries (TMA's stride rule), for up
+// to two operands in one launch: blockIdx.y < rows0 copies row blockIdx.y of operand 0, the
+// rest copy rows of operand 1.  Each thread moves 8 consecutive elements of one row: 8
+// two-byte loads (the source rows may start anywhere) and one 16-byte store.
+struct PackJob {
+    const uint16_t *src;
+    int64_t ld_src;
+    uint16_t *dst;
+    int64_t ld_dst;
+    int64_t rows, cols;
+};
+
+__global__ void pack_rows_f16(const PackJob j0, const PackJob j1)
 {
+    const bool first = blockIdx.y < j0.rows;
+    const PackJob &j = first ? j0 : j1;
+    const int64_t r = first ? blockIdx.y : blockIdx.y - j0.rows;
     const int64_t c8 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
-    if (c8 >= cols) return;
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-        const uint16_t *s = src + r * ld_src + c8;
-        uint16_t *d = dst + r * ld_dst + c8;
-        if (c8 + 8 <= cols) {
-            uint4 v;
-            v.x = static_cast<uint32_t>(s[0]) | (static_cast<uint32_t>(s[1]) << 16);
-            v.y = static_cast<uint32_t>(s[2]) | (static_cast<uint32_t>(s[3]) << 16);
-            v.z = static_cast<uint32_t>(s[4]) | (static_cast<uint32_t>(s[5]) << 16);
-            v.w = static_cast<uint32_t>(s[6]) | (static_cast<uint32_t>(s[7]) << 16);
-            *reinterpret_cast<uint4 *>(d) = v;
-        } else {
-            for (int64_t i = 0; i < cols - c8; ++i) d[i] = s[i];
-        }
+    if (c8 >= j.cols) return;
+    const uint16_t *s = j.src + r * j.ld_src + c8;
+    uint16_t *d = j.dst + r * j.ld_dst + c8;
+    if (c8 + 8 <= j.cols) {
+        uint4 v;
+        v.x = static_cast<uint32_t>(s[0]) | (static_cast<uint32_t>(s[1]) << 16);
+        v.y = static_cast<uint32_t>(s[2]) | (static_cast<uint32_t>(s[3]) << 16);
+        v.z = static_cast<uint32_t>(s[4]) | (static_cast<uint32_t>(s[5]) << 16);
+        v.w = static_cast<uint32_t>(s[6]) | (static_cast<uint32_t>(s[7]) << 16);
+        *reinterpret_cast<uint4 *>(d) = v;
+    } else {
+        for (int64_t i = 0; i < j.cols - c8; ++i) d[i] = s[i];
     }
 }
 
@@ -621,17 +630,41 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUte
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_pack(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows,
-                        int64_t cols, int num_sms, cudaStream_t stream)
+cudaError_t launch_pack2(const void *src0, int64_t ld_src0, void *dst0, int64_t ld_dst0, int64_t rows0, int64_t cols0,
+                         const void *src1, int64_t ld_src1, void *dst1, int64_t ld_dst1, int64_t rows1, int64_t cols1,
+                         cudaStream_t stream)
 {
-    (void)num_sms;
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const int64_t chunks = (cols + 7) / 8;
-    const unsigned gx = static_cast<unsigned>((chunks + 127) / 128);
-    const unsigned gy = static_cast<unsigned>(rows < 8192 ? rows : 8192);
-    pack_rows_f16<<<dim3(gx, gy, 1), 128, 0, stream>>>(static_cast<const uint16_t *>(src), ld_src,
-                                                         static_cast<uint16_t *>(dst), ld_dst, rows, cols);
-    return cudaGetLastError();
+    const PackJob j0{static_cast<const uint16_t *>(src0), ld_src0, static_cast<uint16_t *>(dst0), ld_dst0,
+                     src0 ? rows0 : 0, cols0};
+    const PackJob j1{static_cast<const uint16_t *>(src1), ld_src1, static_cast<uint16_t *>(dst1), ld_dst1,
+                     src1 ? rows1 : 0, cols1};
+    const int64_t rows = j0.rows + j1.rows;
+    if (rows <= 0) return cudaSuccess;
+    if (rows > 2147483647ll) return cudaErrorInvalidValue;
+    const int64_t cols = (j0.rows ? cols0 : 0) > (j1.rows ? cols1 : 0) ? cols0 : cols1;
+    const unsigned gx = static_cast<unsigned>(((cols + 7) / 8 + 127) / 128);
+    if (rows <= 65535) {
+        pack_rows_f16<<<dim3(gx, static_cast<unsigned>(rows), 1), 128, 0, stream>>>(j0, j1);
+        return cudaGetLastError();
+    }
+    // gridDim.y is limited to 65535: launch in slices of rows
+    for (int64_t r0 = 0; r0 < rows; r0 += 65535) {
+        const int64_t n = rows - r0 < 65535 ? rows - r0 : 65535;
+        PackJob a = j0, b = j1;
+        // express the slice as rows [r0, r0 + n) of the concatenation
+        const int64_t a_lo = r0 < j0.rows ? r0 : j0.rows, a_hi = (r0 + n) < j0.rows ? r0 + n : j0.rows;
+        a.src = j0.src ? j0.src + a_lo * j0.ld_src : nullptr;
+        a.dst = j0.dst ? j0.dst + a_lo * j0.ld_dst : nullptr;
+        a.rows = a_hi - a_lo;
+        const int64_t b_lo = r0 > j0.rows ? r0 - j0.rows : 0, b_hi = r0 + n > j0.rows ? r0 + n - j0.rows : 0;
+        b.src = j1.src ? j1.src + b_lo * j1.ld_src : nullptr;
+        b.dst = j1.dst ? j1.dst + b_lo * j1.ld_dst : nullptr;
+        b.rows = b_hi - b_lo;
+        pack_rows_f16<<<dim3(gx, static_cast<unsigned>(n), 1), 128, 0, stream>>>(a, b);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_fill_zero(float *C, int64_t ldc, int64_t rows, int64_t cols, int num_sms,

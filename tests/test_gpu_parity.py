@@ -154,6 +154,17 @@ def test_leading_dims_offsets_and_guard_zones(M, N, K, pad_a, pad_b, pad_c, off)
     assert within_tol(body[:, :N], R, K)
 
 
+@pytest.mark.parametrize("M,N,K", [(70001, 24, 33), (60000, 25, 10001)])
+def test_repack_more_rows_than_one_launch_covers(M, N, K):
+    """Operands with unaligned rows are repacked by a kernel whose grid covers at most 65535
+    rows per launch; taller operands (and A and B together) are repacked in slices."""
+    rng = np.random.default_rng(19)
+    A, B = inputs.normal_pair(rng, M, N, K)
+    plan = tct.gemm_f16_f32_plan(M, N, K)
+    assert plan["pack_a"] == 1
+    check_tol(A, B)
+
+
 def test_repeat_runs_bitwise_identical():
     rng = np.random.default_rng(21)
     A, B = inputs.normal_pair(rng, 1000, 1100, 700)
