@@ -54,6 +54,14 @@ def _load():
         fn.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64]
     lib.oracle_gemm_elems.restype = ctypes.c_int
     lib.oracle_gemm_elems.argtypes = [vp, vp, i64, i64, i64, i64, i64, vp, vp, i64, vp, vp]
+    lib.oracle_bf16_to_f64.restype = ctypes.c_double
+    lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_gemm_ex_rows_f32.restype = ctypes.c_int
+    lib.oracle_gemm_ex_rows_f32.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, i64, i64, i64, i64,
+                                            i64, i64, i64, i64]
+    lib.oracle_gemm_ex_elems.restype = ctypes.c_int
+    lib.oracle_gemm_ex_elems.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, i64, i64, i64, i64, i64,
+                                         vp, vp, i64, vp, vp]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_set_num_threads.restype = None
@@ -155,3 +163,59 @@ def num_threads():
 
 def set_num_threads(n):
     _load().oracle_set_num_threads(int(n))
+
+
+# ---- generalised operands: FP16 or BF16 storage, either operand stored transposed ---------
+
+F16, BF16 = 0, 1
+
+
+def bf16_to_f64(bits):
+    """Decode one BF16 bit pattern (int) with the oracle's own decoder."""
+    return _load().oracle_bf16_to_f64(int(bits) & 0xFFFF)
+
+
+def _bits16(x):
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float16:
+        return x.view(np.uint16)
+    if x.dtype == np.uint16:
+        return x
+    raise TypeError("oracle operands are 16-bit patterns (uint16) or float16")
+
+
+def gemm_ex_f32(A, B, dtype=F16, trans_a=False, trans_b=False, M=None, N=None, K=None, row0=0, nrows=None):
+    """C = op(A) . op(B) rounded once to FP32.  A, B are 16-bit patterns of `dtype` (F16 or
+    BF16) stored row-major: A is M x K (trans_a False) or K x M (True), B is K x N (trans_b
+    False) or N x K (True); wider arrays give leading dimensions.  Rows [row0, row0+nrows)."""
+    A, B = _bits16(A), _bits16(B)
+    Mi = A.shape[1] if trans_a else A.shape[0]
+    Ki = A.shape[0] if trans_a else A.shape[1]
+    Ni = B.shape[0] if trans_b else B.shape[1]
+    M = Mi if M is None else M
+    K = Ki if K is None else K
+    N = Ni if N is None else N
+    nrows = M - row0 if nrows is None else nrows
+    C = np.zeros((nrows, max(N, 1)), np.float32)
+    rc = _load().oracle_gemm_ex_rows_f32(int(dtype), int(bool(trans_a)), int(bool(trans_b)), _ptr(A), _ptr(B),
+                                         _ptr(C), M, N, K, A.shape[1], B.shape[1], C.shape[1], row0, nrows)
+    if rc:
+        raise ValueError(f"oracle_gemm_ex_rows_f32 rejected the arguments (rc={rc})")
+    return C[:, :N]
+
+
+def gemm_ex_elems(A, B, rows, cols, dtype=F16, trans_a=False, trans_b=False, M=None, N=None, K=None):
+    """Selected outputs of op(A) . op(B): (fp64 sums, fp32 results)."""
+    A, B = _bits16(A), _bits16(B)
+    M = (A.shape[1] if trans_a else A.shape[0]) if M is None else M
+    K = (A.shape[0] if trans_a else A.shape[1]) if K is None else K
+    N = (B.shape[0] if trans_b else B.shape[1]) if N is None else N
+    rows = np.ascontiguousarray(rows, np.int64)
+    cols = np.ascontiguousarray(cols, np.int64)
+    o64 = np.zeros(rows.size, np.float64)
+    o32 = np.zeros(rows.size, np.float32)
+    rc = _load().oracle_gemm_ex_elems(int(dtype), int(bool(trans_a)), int(bool(trans_b)), _ptr(A), _ptr(B), M, N, K,
+                                      A.shape[1], B.shape[1], _ptr(rows), _ptr(cols), rows.size, _ptr(o64), _ptr(o32))
+    if rc:
+        raise ValueError(f"oracle_gemm_ex_elems rejected the arguments (rc={rc})")
+    return o64, o32

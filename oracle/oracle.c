@@ -179,6 +179,103 @@ int oracle_gemm_elems(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N
     return 0;
 }
 
+/* ---------------------------------------------------------------------------------
+ * Generalised operands (still the plain definition, one FP64 running sum per output):
+ *
+ *     R[i][j] = (float) sum_k  opA(i, k) * opB(k, j)
+ *
+ *   dtype 0: FP16 (binary16, decoded as above); dtype 1: BF16, whose 16 bits are the upper
+ *   half of an IEEE binary32 value (1 sign, 8 exponent, 7 fraction bits), so its value is
+ *   that binary32 value, exact in double.  A BF16 x BF16 product has at most 8 + 8
+ *   significand bits, so it too is exact in FP64.
+ *   trans_a 0: opA(i, k) = A[i*lda + k] (A stored M x K); 1: opA(i, k) = A[k*lda + i]
+ *   (A stored K x M).  trans_b 0: opB(k, j) = B[k*ldb + j] (B stored K x N); 1:
+ *   opB(k, j) = B[j*ldb + k] (B stored N x K).
+ * --------------------------------------------------------------------------------- */
+double oracle_bf16_to_f64(uint16_t h)
+{
+    union {
+        uint32_t u;
+        float f;
+    } v;
+    v.u = (uint32_t)h << 16;
+    return (double)v.f;
+}
+
+static double g_bf16_table[65536];
+static int g_bf16_table_ready = 0;
+
+static const double *bf16_table(void)
+{
+    if (!g_bf16_table_ready) {
+        for (int i = 0; i < 65536; ++i)
+            g_bf16_table[i] = oracle_bf16_to_f64((uint16_t)i);
+        g_bf16_table_ready = 1;
+    }
+    return g_bf16_table;
+}
+
+int oracle_gemm_ex_rows_f32(int dtype, int trans_a, int trans_b, const uint16_t *A, const uint16_t *B, float *C,
+                            int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t row0,
+                            int64_t nrows)
+{
+    if (dtype != 0 && dtype != 1) return 1;
+    if (M < 0 || N < 0 || K < 0 || ldc < N) return 1;
+    if (lda < (trans_a ? M : K) || ldb < (trans_b ? K : N)) return 1;
+    if (row0 < 0 || nrows < 0 || row0 + nrows > M) return 1;
+    if (M > 0 && N > 0 && (!C || (K > 0 && (!A || !B)))) return 1;
+    const double *T = dtype ? bf16_table() : f16_table();
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+        if (!acc) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = row0; i < row0 + nrows; ++i) {
+            if (!acc) continue;
+            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = T[trans_a ? A[k * lda + i] : A[i * lda + k]];
+                if (trans_b) {
+                    for (int64_t j = 0; j < N; ++j) acc[j] += a * T[B[j * ldb + k]];
+                } else {
+                    const uint16_t *b = B + k * ldb;
+                    for (int64_t j = 0; j < N; ++j) acc[j] += a * T[b[j]];
+                }
+            }
+            float *c = C + (i - row0) * ldc;
+            for (int64_t j = 0; j < N; ++j) c[j] = (float)acc[j];
+        }
+        free(acc);
+    }
+    return bad ? 2 : 0;
+}
+
+int oracle_gemm_ex_elems(int dtype, int trans_a, int trans_b, const uint16_t *A, const uint16_t *B, int64_t M,
+                         int64_t N, int64_t K, int64_t lda, int64_t ldb, const int64_t *rows, const int64_t *cols,
+                         int64_t n, double *out64, float *out32)
+{
+    if (dtype != 0 && dtype != 1) return 1;
+    if (M < 0 || N < 0 || K < 0 || n < 0) return 1;
+    if (lda < (trans_a ? M : K) || ldb < (trans_b ? K : N)) return 1;
+    for (int64_t t = 0; t < n; ++t)
+        if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return 1;
+    const double *T = dtype ? bf16_table() : f16_table();
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        const int64_t i = rows[t], j = cols[t];
+        double s = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            s += T[trans_a ? A[k * lda + i] : A[i * lda + k]] * T[trans_b ? B[j * ldb + k] : B[k * ldb + j]];
+        if (out64) out64[t] = s;
+        if (out32) out32[t] = (float)s;
+    }
+    return 0;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

@@ -91,3 +91,48 @@ def workload(name):
         i = int(name.split(":")[1])
         return list(shape_set(4, LARGE_SHAPES[: i + 1]))
     raise KeyError(name)
+
+
+# ---- BF16 operands and transposed storage ------------------------------------------------
+
+def to_bf16_bits(x):
+    """float array -> BF16 bit patterns (uint16): rounded to FP32, then to BF16, each to
+    nearest with ties to even (torch's conversion)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def normal_bf16(rng, rows, cols):
+    """A rows x cols BF16 matrix (bit patterns) of N(0,1) draws, row-major from ``rng``."""
+    out = np.empty((rows, cols), np.uint16)
+    if rows == 0 or cols == 0:
+        return out
+    step = max(1, _CHUNK_ELEMS // cols)
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        out[r0:r1] = to_bf16_bits(rng.standard_normal((r1 - r0, cols)))
+    return out
+
+
+def pair_ex(rng, M, N, K, dtype="f16", integer=False, trans_a=False, trans_b=False):
+    """(A, B) for C = op(A) . op(B): the logical A (M x K) is drawn first, then the logical B
+    (K x N), exactly as in normal_pair / integer_pair; then each is stored transposed if asked
+    (A as K x M, B as N x K).  FP16 arrays are float16, BF16 arrays are uint16 bit patterns."""
+    if integer:
+        A = rng.integers(-4, 4, size=(M, K), endpoint=True)
+        B = rng.integers(-4, 4, size=(K, N), endpoint=True)
+        if dtype == "f16":
+            A, B = A.astype(np.float16), B.astype(np.float16)
+        else:
+            A, B = to_bf16_bits(A), to_bf16_bits(B)
+    elif dtype == "f16":
+        A, B = normal_pair(rng, M, N, K)
+    else:
+        A = normal_bf16(rng, M, K)
+        B = normal_bf16(rng, K, N)
+    if trans_a:
+        A = np.ascontiguousarray(A.T)
+    if trans_b:
+        B = np.ascontiguousarray(B.T)
+    return A, B
