@@ -101,6 +101,29 @@ TCT_API gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int6
                             int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void *stream,
                             const gemm_options *opt);
 
+/* Operand element type and storage of gemm_f32acc. */
+typedef enum gemm_dtype { GEMM_DTYPE_F16 = 0, GEMM_DTYPE_BF16 = 1 } gemm_dtype;
+typedef enum gemm_op { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op;
+
+/*
+ * gemm_f32acc -- C = op(A) . op(B) with FP16 or BF16 operands, FP32 accumulation, FP32 C.
+ * The same blocked tensor-core product as gemm_f16_f32, with the operand storage and type
+ * chosen by the caller:
+ *   ab_type : GEMM_DTYPE_F16 or GEMM_DTYPE_BF16 (both operands).
+ *   op_a    : GEMM_OP_N -- A stored M x K row-major, op(A)(i, k) = A[i*lda + k], lda >= K;
+ *             GEMM_OP_T -- A stored K x M row-major (column-major M x K), op(A)(i, k) =
+ *             A[k*lda + i], lda >= M.
+ *   op_b    : GEMM_OP_N -- B stored K x N row-major, op(B)(k, j) = B[k*ldb + j], ldb >= N;
+ *             GEMM_OP_T -- B stored N x K row-major, op(B)(k, j) = B[j*ldb + k], ldb >= K.
+ *   C       : FP32, M x N row-major, ldc >= N.
+ * Everything else (alignment handling, options, errors, stream semantics) is as for
+ * gemm_f16_f32_ex; the stages option must name a variant compiled for the layout (the
+ * planner's defaults always are).
+ */
+TCT_API gemm_status gemm_f32acc(int32_t ab_type, int32_t op_a, int32_t op_b, const void *A, const void *B,
+                                float *C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                int64_t ldc, void *stream, const gemm_options *opt);
+
 /*
  * Launch plan the library would use for a problem (host only, no GPU needed when
  * num_sms > 0 is given; num_sms <= 0 queries the current device).

@@ -18,11 +18,15 @@ GEMM_ERR_UNSUPPORTED_DEVICE = 2
 GEMM_ERR_CUDA = 3
 GEMM_ERR_DEVICE_TIMEOUT = 4
 
+GEMM_DTYPE_F16, GEMM_DTYPE_BF16 = 0, 1
+GEMM_OP_N, GEMM_OP_T = 0, 1
+
 # Every function the header declares (checked by the test-suite against the .so).
 EXPORTED = (
     "gemm_f16_f32",
     "gemm_f16_f32_ex",
     "gemm_f16_f32_noalloc",
+    "gemm_f32acc",
     "gemm_f16_f32_plan",
     "gemm_f16_f32_work_item",
     "gemm_tile_coord",
@@ -77,6 +81,9 @@ def load():
     lib.gemm_f16_f32.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
     lib.gemm_f16_f32_noalloc.restype = ctypes.c_int
     lib.gemm_f16_f32_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
+    lib.gemm_f32acc.restype = ctypes.c_int
+    lib.gemm_f32acc.argtypes = [i32, i32, i32, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp,
+                                ctypes.POINTER(GemmOptions)]
     lib.gemm_f16_f32_ex.restype = ctypes.c_int
     lib.gemm_f16_f32_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, ctypes.POINTER(GemmOptions)]
     lib.gemm_f16_f32_plan.restype = ctypes.c_int
@@ -138,6 +145,13 @@ def gemm_f16_f32_ex(A, B, C, M, N, K, lda, ldb, ldc, stream=0, **options):
     return load().gemm_f16_f32_ex(A, B, C, M, N, K, lda, ldb, ldc, stream or None, ctypes.byref(opt))
 
 
+def gemm_f32acc(ab_type, op_a, op_b, A, B, C, M, N, K, lda, ldb, ldc, stream=0, **options):
+    """Raw C-ABI call for FP16/BF16 operands stored as given (op = GEMM_OP_N or GEMM_OP_T)."""
+    opt = _options(**options)
+    return load().gemm_f32acc(ab_type, op_a, op_b, A, B, C, M, N, K, lda, ldb, ldc, stream or None,
+                              ctypes.byref(opt))
+
+
 def gemm_f16_f32_plan(M, N, K, lda=None, ldb=None, num_sms=0, **options):
     """The launch plan (tile shape, stages, grid, waves) as a dict."""
     opt = _options(**options)
@@ -186,15 +200,28 @@ def _current_stream_ptr(device):
     return torch.cuda.current_stream(device).cuda_stream
 
 
+def _operand(t, rows, cols, name):
+    """(op, ld) of a 2-D tensor holding a rows x cols operand: row-major (unit column stride)
+    is op N with ld = row stride; column-major (unit row stride) is op T, i.e. the transpose
+    stored row-major, with ld = column stride."""
+    r_stride, c_stride = t.stride()
+    if cols <= 1 or c_stride == 1:
+        return GEMM_OP_N, max(r_stride if rows > 1 else cols, cols, 1)
+    if rows <= 1 or r_stride == 1:
+        return GEMM_OP_T, max(c_stride if cols > 1 else rows, rows, 1)
+    raise ValueError(f"{name} must be row-major or column-major (one unit stride)")
+
+
 def matmul(A, B, C=None, stream=None, **options):
-    """C = A @ B for torch CUDA tensors: A (M x K) and B (K x N) float16 with unit column
-    stride, C (M x N) float32 (allocated if None).  Runs on ``stream`` (a torch.cuda.Stream)
-    or the current stream; raises GemmError on a non-zero status."""
+    """C = A @ B for torch CUDA tensors: A (M x K) and B (K x N) both float16 or both bfloat16,
+    each row-major or column-major (e.g. a transposed view), C (M x N) float32 row-major
+    (allocated if None).  Runs on ``stream`` (a torch.cuda.Stream) or the current stream;
+    raises GemmError on a non-zero status."""
     import torch
     if A.dim() != 2 or B.dim() != 2:
         raise ValueError("A and B must be 2-D")
-    if A.dtype != torch.float16 or B.dtype != torch.float16:
-        raise TypeError("A and B must be float16")
+    if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("A and B must both be float16 or both bfloat16")
     if not (A.is_cuda and B.is_cuda) or A.device != B.device:
         raise ValueError("A and B must be CUDA tensors on one device")
     M, K = A.shape
@@ -205,18 +232,22 @@ def matmul(A, B, C=None, stream=None, **options):
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     if C.dtype != torch.float32 or tuple(C.shape) != (M, N) or C.device != A.device:
         raise ValueError("C must be a float32 M x N tensor on A's device")
-    for name, t in (("A", A), ("B", B), ("C", C)):
-        if t.numel() and t.shape[1] > 1 and t.stride(1) != 1:
-            raise ValueError(f"{name} must be row-major (unit column stride)")
-    lda = A.stride(0) if M > 1 else max(K, 1)
-    ldb = B.stride(0) if K > 1 else max(N, 1)
+    if C.numel() and N > 1 and C.stride(1) != 1:
+        raise ValueError("C must be row-major (unit column stride)")
+    op_a, lda = _operand(A, M, K, "A")
+    op_b, ldb = _operand(B, K, N, "B")
     ldc = C.stride(0) if M > 1 else max(N, 1)
     s = stream.cuda_stream if stream is not None else _current_stream_ptr(A.device)
+    dt = GEMM_DTYPE_BF16 if A.dtype == torch.bfloat16 else GEMM_DTYPE_F16
     with torch.cuda.device(A.device):
-        if options:
-            st = gemm_f16_f32_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc, s, **options)
+        if dt == GEMM_DTYPE_F16 and op_a == GEMM_OP_N and op_b == GEMM_OP_N:
+            if options:
+                st = gemm_f16_f32_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc, s, **options)
+            else:
+                st = gemm_f16_f32(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc, s)
         else:
-            st = gemm_f16_f32(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc, s)
+            st = gemm_f32acc(dt, op_a, op_b, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc, s,
+                             **options)
     if st:
-        raise GemmError(st, "gemm_f16_f32")
+        raise GemmError(st, "gemm_f32acc" if (dt or op_a or op_b) else "gemm_f16_f32")
     return C

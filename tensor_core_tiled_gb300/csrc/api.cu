@@ -127,10 +127,10 @@ gemm_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn)
     return GEMM_OK;
 }
 
-// 2-D FP16 tensor map over a row-major matrix of `rows` x `cols` with leading dimension
-// `ld` (elements), boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill.
-gemm_status encode_fp16_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld,
-                           uint32_t box_rows)
+// 2-D FP16 or BF16 tensor map over a row-major matrix of `rows` x `cols` with leading
+// dimension `ld` (elements), boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill.
+gemm_status encode_16bit_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld,
+                            uint32_t box_rows, bool bf16)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     gemm_status st = get_encoder(&enc);
@@ -139,8 +139,9 @@ gemm_status encode_fp16_2d(CUtensorMap *m, const void *base, int64_t rows, int64
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -171,11 +172,16 @@ gemm_status check_options(const gemm_options *opt)
     return GEMM_OK;
 }
 
+// Layout bits: 1 = A stored K x M, 2 = B stored N x K, 4 = BF16 operands.
+bool a_t(int layout) { return (layout & 1) != 0; }
+bool b_t(int layout) { return (layout & 2) != 0; }
+bool is_bf16(int layout) { return (layout & 4) != 0; }
+
 gemm_status check_args(const void *A, const void *B, const float *C, int64_t M, int64_t N, int64_t K,
-                       int64_t lda, int64_t ldb, int64_t ldc)
+                       int64_t lda, int64_t ldb, int64_t ldc, int layout = 0)
 {
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_ARG;
-    if (lda < K || ldb < N || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (lda < (a_t(layout) ? M : K) || ldb < (b_t(layout) ? K : N) || ldc < N) return GEMM_ERR_INVALID_ARG;
     if (lda > kMaxDim * 4 || ldb > kMaxDim * 4 || ldc > kMaxDim * 4) return GEMM_ERR_INVALID_ARG;
     if (M > 0 && N > 0) {
         if (!C || reinterpret_cast<uintptr_t>(C) % 4 != 0) return GEMM_ERR_INVALID_ARG;
@@ -256,7 +262,8 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
 // of each variant, and HBM time for bandwidth-bound shapes.
 // pair_slots: co-resident CTA pairs (from the device, or sms / 2 when planning offline).
 gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int sms, int pair_slots,
-                      const gemm_options *opt, const void *A, const void *B, gemm_plan *pl, bool allow_split = true)
+                      const gemm_options *opt, const void *A, const void *B, gemm_plan *pl, bool allow_split = true,
+                      int layout = 0)
 {
     std::memset(pl, 0, sizeof(*pl));
     const int want_cg = opt ? opt->cta_group : 0;
@@ -268,7 +275,7 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
     Split best_sp{};
     for (const Candidate &c : kCandidates) {
         if ((want_cg && want_cg != c.cta_group) || (want_tn && want_tn != c.tile_n)) continue;
-        if (want_st && tct::variant_smem_bytes(c.cta_group, c.tile_n, want_st) < 0) continue;
+        if (!tct::variant_exists(layout, c.cta_group, c.tile_n, want_st ? want_st : c.stages)) continue;
         int64_t units = c.cta_group == 2 ? pair_slots : sms;
         if (cap > 0) units = std::min<int64_t>(units, std::max<int64_t>(1, cap / c.cta_group));
         if (units < 1) continue;
@@ -377,14 +384,11 @@ int device_pair_slots(DeviceInfo *dev)
 
 gemm_status to_status(cudaError_t e) { return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA; }
 
-}  // namespace
-
-extern "C" {
-
-gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
-                            int64_t lda, int64_t ldb, int64_t ldc, void *stream, const gemm_options *opt)
+// The launch sequence for every operand layout (see make_plan for the layout bits).
+gemm_status run_gemm(int layout, const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, void *stream, const gemm_options *opt)
 {
-    gemm_status st = check_args(A, B, C, M, N, K, lda, ldb, ldc);
+    gemm_status st = check_args(A, B, C, M, N, K, lda, ldb, ldc, layout);
     if (st != GEMM_OK) return st;
     st = check_options(opt);
     if (st != GEMM_OK) return st;
@@ -396,17 +400,21 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
     if (K == 0) return to_status(tct::launch_fill_zero(C, ldc, M, N, dev.sms, s));
 
     gemm_plan pl;
-    st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), opt, A, B, &pl);
+    st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), opt, A, B, &pl, true, layout);
     if (st != GEMM_OK) return st;
+
+    // Stored shapes: A is M x K, or K x M when transposed; B is K x N, or N x K.
+    const int64_t a_rows = a_t(layout) ? K : M, a_cols = a_t(layout) ? M : K;
+    const int64_t b_rows = b_t(layout) ? N : K, b_cols = b_t(layout) ? K : N;
 
     // Operands whose rows do not start on 16-byte boundaries are copied first (TMA needs
     // 16-byte aligned bases and row strides); the copy is stream-ordered.  The same
-    // stream-ordered block holds the stream-K partial tiles.
+    // stream-ordered block holds the split tiles' parts and flags.
     const void *a_use = A, *b_use = B;
     int64_t lda_use = lda, ldb_use = ldb;
-    const int64_t lda_p = round_up(K, 8), ldb_p = round_up(N, 8);
-    const int64_t a_bytes = pl.pack_a ? round_up(M * lda_p * 2, 256) : 0;
-    const int64_t b_bytes = pl.pack_b ? round_up(K * ldb_p * 2, 256) : 0;
+    const int64_t lda_p = round_up(a_cols, 8), ldb_p = round_up(b_cols, 8);
+    const int64_t a_bytes = pl.pack_a ? round_up(a_rows * lda_p * 2, 256) : 0;
+    const int64_t b_bytes = pl.pack_b ? round_up(b_rows * ldb_p * 2, 256) : 0;
     const int64_t w_bytes = split_parts_bytes(pl), f_bytes = split_flags_bytes(pl);
     void *ws = nullptr;
     if (a_bytes + b_bytes + w_bytes + f_bytes > 0) {
@@ -425,8 +433,8 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
             b_use = w + a_bytes;
             ldb_use = ldb_p;
         }
-        cudaError_t e = tct::launch_pack2(pl.pack_a ? A : nullptr, lda, w, lda_p, M, K, pl.pack_b ? B : nullptr, ldb,
-                                          w + a_bytes, ldb_p, K, N, s);
+        cudaError_t e = tct::launch_pack2(pl.pack_a ? A : nullptr, lda, w, lda_p, a_rows, a_cols,
+                                          pl.pack_b ? B : nullptr, ldb, w + a_bytes, ldb_p, b_rows, b_cols, s);
         if (e == cudaSuccess && f_bytes)  // the split tiles' flags start lowered
             e = cudaMemsetAsync(w + a_bytes + b_bytes + w_bytes, 0, static_cast<size_t>(f_bytes), s);
         if (e != cudaSuccess) {
@@ -435,9 +443,13 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
         }
     }
 
+    // TMA boxes: A as M x K -> 64(K) x 128(M); as K x M -> 64(M) x 64(K).  B as K x N ->
+    // 64(N) x 64(K); as N x K -> 64(K) x (tile_n / cta_group)(N).
     CUtensorMap ta, tb;
-    st = encode_fp16_2d(&ta, a_use, M, K, lda_use, kTileM);
-    if (st == GEMM_OK) st = encode_fp16_2d(&tb, b_use, K, N, ldb_use, kTileK);
+    st = encode_16bit_2d(&ta, a_use, a_rows, a_cols, lda_use, a_t(layout) ? 64 : kTileM, is_bf16(layout));
+    if (st == GEMM_OK)
+        st = encode_16bit_2d(&tb, b_use, b_rows, b_cols, ldb_use,
+                             b_t(layout) ? static_cast<uint32_t>(pl.tile_n / pl.cta_group) : kTileK, is_bf16(layout));
     if (st == GEMM_OK) {
         const int tmo = opt && opt->timeout_ms ? opt->timeout_ms : kDefaultTimeoutMs;
         tct::KernelParams p = make_params(pl, C, M, N, K, ldc, tmo);
@@ -451,12 +463,33 @@ gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, i
             st = encode_parts(&tp, p.workspace, static_cast<int64_t>(pl.stream_k_tiles) * pl.tile_m, pl.tile_n);
         }
         if (st == GEMM_OK)
-            st = to_status(tct::launch_gemm(ta, tb, tp, p, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
+            st = to_status(tct::launch_gemm(ta, tb, tp, p, layout, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
     }
     if (ws) {
         if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
     }
     return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int64_t ldc, void *stream, const gemm_options *opt)
+{
+    return run_gemm(0, A, B, C, M, N, K, lda, ldb, ldc, stream, opt);
+}
+
+gemm_status gemm_f32acc(int32_t ab_type, int32_t op_a, int32_t op_b, const void *A, const void *B, float *C,
+                        int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void *stream,
+                        const gemm_options *opt)
+{
+    if ((ab_type != GEMM_DTYPE_F16 && ab_type != GEMM_DTYPE_BF16) || (op_a != GEMM_OP_N && op_a != GEMM_OP_T) ||
+        (op_b != GEMM_OP_N && op_b != GEMM_OP_T))
+        return GEMM_ERR_INVALID_ARG;
+    const int layout = (op_a == GEMM_OP_T ? 1 : 0) | (op_b == GEMM_OP_T ? 2 : 0) | (ab_type == GEMM_DTYPE_BF16 ? 4 : 0);
+    return run_gemm(layout, A, B, C, M, N, K, lda, ldb, ldc, stream, opt);
 }
 
 gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
@@ -638,11 +671,11 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
     }
 
     CUtensorMap ta, tb;
-    st = encode_fp16_2d(&ta, a_use, M, K, lda_use, kTileM);
-    if (st == GEMM_OK) st = encode_fp16_2d(&tb, b_use, K, N, ldb_use, kTileK);
+    st = encode_16bit_2d(&ta, a_use, M, K, lda_use, kTileM, false);
+    if (st == GEMM_OK) st = encode_16bit_2d(&tb, b_use, K, N, ldb_use, kTileK, false);
     if (st != GEMM_OK) return st;
     const tct::KernelParams p = make_params(pl, C, M, N, K, ldc, kDefaultTimeoutMs);
     CUtensorMap tp;  // no split tiles on this path
     std::memset(&tp, 0, sizeof(tp));
-    return to_status(tct::launch_gemm(ta, tb, tp, p, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
+    return to_status(tct::launch_gemm(ta, tb, tp, p, 0, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
 }

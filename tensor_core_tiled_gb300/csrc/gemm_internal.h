@@ -99,6 +99,17 @@ inline bool work_item(const KernelParams &p, int32_t u, int32_t idx, WorkItem &i
     X(2, 128, 6)        \
     X(2, 128, 8)
 
+// Variants compiled for the other operand layouts and BF16 (the planner's candidates).
+#define TCT_VARIANTS_EX(X) \
+    X(2, 256, 6)           \
+    X(1, 256, 4)           \
+    X(1, 128, 6)           \
+    X(2, 128, 8)
+
+// Operand layout and type of a launch: bit 0 = A stored K x M, bit 1 = B stored N x K,
+// bit 2 = BF16 (else FP16).  0 is the FP16, untransposed form.
+int variant_exists(int layout, int cta_group, int tile_n, int stages);
+
 int variant_smem_bytes(int cta_group, int tile_n, int stages);
 
 // 1 if the variant's stage buffers can hold a split tile's other half in its epilogue.
@@ -109,7 +120,7 @@ int variant_max_clusters(int cta_group, int tile_n, int stages);
 
 // tp: 2-D FP32 map of the split-tile parts (box tile_n x 32), unused when split_tiles == 0.
 cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const KernelParams &p,
-                        int cta_group, int tile_n, int stages, int grid, cudaStream_t stream);
+                        int layout, int cta_group, int tile_n, int stages, int grid, cudaStream_t stream);
 
 // Copies up to two FP16 operands (a NULL src skips one) into buffers with 16-byte aligned rows,
 // in one launch.

@@ -43,8 +43,11 @@ namespace tct {
 
 __device__ unsigned int g_error_word;
 
-template <int CG_, int BN_, int STAGES_>
+template <int CG_, int BN_, int STAGES_, bool AT_ = false, bool BT_ = false, bool BF16_ = false>
 struct Cfg {
+    static constexpr bool AT = AT_;      // A stored K x M (transposed): MN-major A tiles
+    static constexpr bool BT = BT_;      // B stored N x K (transposed): K-major B tiles
+    static constexpr bool BF16 = BF16_;  // BF16 operands instead of FP16
     static constexpr int CG = CG_;            // CTAs per tile (1 or 2)
     static constexpr int BM = 128;            // tile rows held by one CTA
     static constexpr int BN = BN_;            // tile columns (the MMA's N)
@@ -54,7 +57,8 @@ struct Cfg {
     static constexpr int UMMA_K = 16;         // K of one kind::f16 MMA
     static constexpr int A_STAGE = BM * BK * 2;
     static constexpr int B_SUB = BK * 64 * 2;  // one 64-column TMA box of B
-    static constexpr int B_BOXES = BN_CTA / 64;
+    static constexpr int B_BOXES = BT_ ? 1 : BN_CTA / 64;  // TMA boxes of B per stage
+    static constexpr int A_BOXES = AT_ ? 2 : 1;            // TMA boxes of A per stage
     static constexpr int B_STAGE = BK * BN_CTA * 2;
     static constexpr int STAGE_TX = CG * (A_STAGE + B_STAGE);  // bytes counted on one full barrier
     static constexpr int EPI_WARPS = 4;
@@ -207,12 +211,12 @@ __device__ __forceinline__ bool wait_flag(const unsigned int *flag, uint64_t lim
     return true;
 }
 
-template <int CG, int BN, int STAGES>
+template <int CG, int BN, int STAGES, bool AT, bool BT, bool BF16>
 __global__ void __launch_bounds__(192, 1)
-    gemm_f16_f32_tcgen05(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmP, const KernelParams p)
+    gemm_tcgen05_f32acc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmP, const KernelParams p)
 {
-    using Cf = Cfg<CG, BN, STAGES>;
+    using Cf = Cfg<CG, BN, STAGES, AT, BT, BF16>;
     constexpr bool kPair = CG == 2;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms must start on 1024-byte boundaries of the shared space.
@@ -295,22 +299,38 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     const int32_t k0 = kb * Cf::BK;
+                    // Box coordinates (innermost first) of this stage's operand tiles:
+                    //   A as M x K: one 64(K) x 128(M) box; A as K x M: two 64(M) x 64(K) boxes;
+                    //   B as K x N: 64(N) x 64(K) boxes; B as N x K: one 64(K) x BN_CTA(N) box.
+                    uint32_t fb = full_bar(s);
                     if constexpr (kPair) {
                         // Both CTAs' bytes are counted on the even CTA's full barrier.
-                        const uint32_t fb = map_to_cta(full_bar(s), 0);
+                        fb = map_to_cta(full_bar(s), 0);
                         if (rank == 0) mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_TX);
-                        tma_load_2d_pair(smem_u32(sA + s * Cf::A_STAGE), &tmA, k0, m0, fb);
-#pragma unroll
-                        for (int j = 0; j < Cf::B_BOXES; ++j)
-                            tma_load_2d_pair(smem_u32(sB + s * Cf::B_STAGE + j * Cf::B_SUB), &tmB,
-                                             n0 + 64 * j, k0, fb);
                     } else {
                         mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_TX);
-                        tma_load_2d(smem_u32(sA + s * Cf::A_STAGE), &tmA, k0, m0, full_bar(s));
+                    }
+                    auto load = [&](uint32_t dst, const CUtensorMap *tm, int32_t c0, int32_t c1) {
+                        if constexpr (kPair)
+                            tma_load_2d_pair(dst, tm, c0, c1, fb);
+                        else
+                            tma_load_2d(dst, tm, c0, c1, fb);
+                    };
 #pragma unroll
-                        for (int j = 0; j < Cf::B_BOXES; ++j)
-                            tma_load_2d(smem_u32(sB + s * Cf::B_STAGE + j * Cf::B_SUB), &tmB, n0 + 64 * j,
-                                        k0, full_bar(s));
+                    for (int j = 0; j < Cf::A_BOXES; ++j) {
+                        const uint32_t dst = smem_u32(sA + s * Cf::A_STAGE + j * Cf::B_SUB);
+                        if constexpr (AT)
+                            load(dst, &tmA, m0 + 64 * j, k0);
+                        else
+                            load(dst, &tmA, k0, m0);
+                    }
+#pragma unroll
+                    for (int j = 0; j < Cf::B_BOXES; ++j) {
+                        const uint32_t dst = smem_u32(sB + s * Cf::B_STAGE + j * Cf::B_SUB);
+                        if constexpr (BT)
+                            load(dst, &tmB, k0, n0);
+                        else
+                            load(dst, &tmB, n0 + 64 * j, k0);
                     }
                     issued[s] = true;
                     issued_parity[s] = ph;
@@ -345,7 +365,7 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && rank == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(Cf::BM * CG, BN, /*b_mn_major=*/true);
+            constexpr uint32_t idesc = idesc_f32acc(Cf::BM * CG, BN, /*a_mn_major=*/AT, /*b_mn_major=*/!BT, BF16);
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
@@ -372,12 +392,14 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t b_base = smem_u32(sB + s * Cf::B_STAGE);
 #pragma unroll
                     for (int kk = 0; kk < Cf::BK / Cf::UMMA_K; ++kk) {
-                        // A: K-major, 128-byte rows, 8-row groups 1024 B apart; a K step of
-                        // 16 elements is 32 bytes inside the swizzle row.
-                        const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                        // B: N-major, 64-column boxes B_SUB bytes apart (leading offset),
-                        // 8-row K groups 1024 B apart (stride offset); 16 K rows = 2048 B.
-                        const uint64_t bdesc = smem_desc_sw128(b_base + kk * 2048, Cf::B_SUB, 1024);
+                        // K-major tiles: 128-byte rows of K, 8-row groups 1024 B apart (stride
+                        // offset); a K step of 16 elements is 32 bytes inside the swizzle row.
+                        // MN-major tiles: 64-element MN boxes B_SUB bytes apart (leading
+                        // offset), 8-row K groups 1024 B apart; 16 K rows = 2048 B.
+                        const uint64_t adesc = AT ? smem_desc_sw128(a_base + kk * 2048, Cf::B_SUB, 1024)
+                                                  : smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                        const uint64_t bdesc = BT ? smem_desc_sw128(b_base + kk * 32, 16, 1024)
+                                                  : smem_desc_sw128(b_base + kk * 2048, Cf::B_SUB, 1024);
                         const uint32_t acc = (kb != w.kb0 || kk != 0) ? 1u : 0u;
                         if constexpr (kPair)
                             tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, acc);
@@ -556,11 +578,11 @@ static cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunc
     return cfg;
 }
 
-template <int CG, int BN, int STAGES>
+template <int CG, int BN, int STAGES, bool AT, bool BT, bool BF16>
 static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp,
                                   const KernelParams &p, int grid, cudaStream_t stream)
 {
-    auto kern = gemm_f16_f32_tcgen05<CG, BN, STAGES>;
+    auto kern = gemm_tcgen05_f32acc<CG, BN, STAGES, AT, BT, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<CG, BN, STAGES>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -576,7 +598,7 @@ static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, 
 template <int CG, int BN, int STAGES>
 static int max_clusters_variant()
 {
-    auto kern = gemm_f16_f32_tcgen05<CG, BN, STAGES>;
+    auto kern = gemm_tcgen05_f32acc<CG, BN, STAGES, false, false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<CG, BN, STAGES>::SMEM_BYTES) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -619,15 +641,54 @@ int variant_split_ok(int cta_group, int tile_n, int stages)
     return 0;
 }
 
-cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const KernelParams &p,
-                        int cta_group, int tile_n, int stages, int grid, cudaStream_t stream)
+int variant_exists(int layout, int cta_group, int tile_n, int stages)
+{
+    if (layout == 0) {
+#define TCT_CASE(CG_, BN_, ST_) \
+        if (cta_group == CG_ && tile_n == BN_ && stages == ST_) return 1;
+        TCT_VARIANTS(TCT_CASE)
+#undef TCT_CASE
+        return 0;
+    }
+    if (layout < 0 || layout > 7) return 0;
+#define TCT_CASE(CG_, BN_, ST_) \
+    if (cta_group == CG_ && tile_n == BN_ && stages == ST_) return 1;
+    TCT_VARIANTS_EX(TCT_CASE)
+#undef TCT_CASE
+    return 0;
+}
+
+template <bool AT, bool BT, bool BF16>
+static cudaError_t launch_layout(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp,
+                                 const KernelParams &p, int cta_group, int tile_n, int stages, int grid,
+                                 cudaStream_t stream)
 {
 #define TCT_CASE(CG_, BN_, ST_)                             \
     if (cta_group == CG_ && tile_n == BN_ && stages == ST_) \
-        return launch_variant<CG_, BN_, ST_>(ta, tb, tp, p, grid, stream);
-    TCT_VARIANTS(TCT_CASE)
+        return launch_variant<CG_, BN_, ST_, AT, BT, BF16>(ta, tb, tp, p, grid, stream);
+    if constexpr (!AT && !BT && !BF16) {
+        TCT_VARIANTS(TCT_CASE)
+    } else {
+        TCT_VARIANTS_EX(TCT_CASE)
+    }
 #undef TCT_CASE
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const KernelParams &p,
+                        int layout, int cta_group, int tile_n, int stages, int grid, cudaStream_t stream)
+{
+    switch (layout) {
+    case 0: return launch_layout<false, false, false>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
+    case 1: return launch_layout<true, false, false>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
+    case 2: return launch_layout<false, true, false>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
+    case 3: return launch_layout<true, true, false>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
+    case 4: return launch_layout<false, false, true>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
+    case 5: return launch_layout<true, false, true>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
+    case 6: return launch_layout<false, true, true>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
+    case 7: return launch_layout<true, true, true>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_pack2(const void *src0, int64_t ld_src0, void *dst0, int64_t ld_dst0, int64_t rows0, int64_t cols0,

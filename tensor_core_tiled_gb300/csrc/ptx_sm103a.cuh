@@ -301,13 +301,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// Instruction descriptor for kind::f16 with FP16 A and B and an FP32 accumulator:
-// D format (bits 4..5) = F32, A/B formats (7..9, 10..12) = F16, A K-major (bit 15 = 0),
-// B major-ness in bit 16 (1 = MN-major), N >> 3 in bits 17..22, M >> 4 in bits 24..28.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t m, uint32_t n, bool b_mn_major)
+// Instruction descriptor for kind::f16 with an FP32 accumulator: D format (bits 4..5) =
+// F32, A/B formats (7..9, 10..12) = F16 (0) or BF16 (1), A major-ness in bit 15 and B
+// major-ness in bit 16 (0 = K-major, 1 = MN-major), N >> 3 in bits 17..22, M >> 4 in bits
+// 24..28.
+__host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t m, uint32_t n, bool a_mn_major, bool b_mn_major,
+                                                    bool bf16)
 {
-    return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((n >> 3) << 17) | ((m >> 4) << 24);
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 }  // namespace tct

@@ -64,6 +64,12 @@ def test_invalid_arguments_rejected_before_any_device_work(tct_lib):
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, cta_group=3) == tct.GEMM_ERR_INVALID_ARG
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, stream_k=3) == tct.GEMM_ERR_INVALID_ARG
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, fault_inject=2) == tct.GEMM_ERR_INVALID_ARG
+    # generalised entry: bad type or op, and leading dimensions checked against the storage
+    assert tct.gemm_f32acc(2, 0, 0, p, p, p, 4, 4, 4, 4, 4, 4, 0) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_f32acc(0, 2, 0, p, p, p, 4, 4, 4, 4, 4, 4, 0) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_f32acc(1, 1, 0, p, p, p, 8, 4, 2, 4, 4, 4, 0) == tct.GEMM_ERR_INVALID_ARG   # lda < M
+    assert tct.gemm_f32acc(1, 0, 1, p, p, p, 4, 8, 6, 6, 4, 8, 0) == tct.GEMM_ERR_INVALID_ARG   # ldb < K
+    assert tct.gemm_f32acc(1, 1, 1, 0, 0, 0, 0, 4, 4, 1, 4, 4, 0) == tct.GEMM_OK                # empty
 
 
 @pytest.mark.parametrize("num_m,num_n", [(9, 9), (7, 14), (32, 16), (13, 5), (1, 40), (40, 1)])
