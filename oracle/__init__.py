@@ -62,6 +62,18 @@ def _load():
     lib.oracle_gemm_ex_elems.restype = ctypes.c_int
     lib.oracle_gemm_ex_elems.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, i64, i64, i64, i64, i64,
                                          vp, vp, i64, vp, vp]
+    lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+    lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_f16_n.restype = None
+    lib.oracle_f32_to_f16_n.argtypes = [vp, vp, i64]
+    lib.oracle_f32_to_bf16_n.restype = None
+    lib.oracle_f32_to_bf16_n.argtypes = [vp, vp, i64]
+    lib.oracle_gemm_epilogue.restype = ctypes.c_int
+    lib.oracle_gemm_epilogue.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, i64, i64, i64, i64, i64,
+                                         ctypes.c_double, ctypes.c_double, vp, ctypes.c_int, i64, vp, ctypes.c_int,
+                                         vp, ctypes.c_int, i64]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_set_num_threads.restype = None
@@ -219,3 +231,56 @@ def gemm_ex_elems(A, B, rows, cols, dtype=F16, trans_a=False, trans_b=False, M=N
     if rc:
         raise ValueError(f"oracle_gemm_ex_elems rejected the arguments (rc={rc})")
     return o64, o32
+
+
+# ---- epilogue: D = round_out(alpha * S + beta * Cin + bias[j]) ------------------------------
+
+F32 = 2
+
+
+def f32_to_f16_bits(x):
+    """binary16 bit pattern of a float32 value, the oracle's own rounding."""
+    return _load().oracle_f32_to_f16(float(np.float32(x)))
+
+
+def f32_to_bf16_bits(x):
+    return _load().oracle_f32_to_bf16(float(np.float32(x)))
+
+
+def _typed(x, t):
+    """Contiguous array of the given oracle type code (F16/BF16 as uint16 bits, F32)."""
+    x = np.ascontiguousarray(x)
+    if t == F32:
+        if x.dtype != np.float32:
+            raise TypeError("expected float32")
+        return x
+    return _bits16(x)
+
+
+def gemm_epilogue(A, B, dtype=F16, trans_a=False, trans_b=False, alpha=1.0, beta=0.0, Cin=None, cin_type=F32,
+                  bias=None, bias_type=F32, out_type=F32):
+    """D = round_out(alpha * op(A).op(B) + beta * Cin + bias[j]) -- see oracle.c.  Returns a
+    float32 array (out F32) or uint16 bit patterns (out F16/BF16)."""
+    A, B = _bits16(A), _bits16(B)
+    M = A.shape[1] if trans_a else A.shape[0]
+    K = A.shape[0] if trans_a else A.shape[1]
+    N = B.shape[0] if trans_b else B.shape[1]
+    D = np.zeros((M, max(N, 1)), np.float32 if out_type == F32 else np.uint16)
+    cin = _typed(Cin, cin_type) if (beta != 0.0 and Cin is not None) else None
+    bs = _typed(bias, bias_type) if bias is not None else None
+    rc = _load().oracle_gemm_epilogue(int(dtype), int(bool(trans_a)), int(bool(trans_b)), _ptr(A), _ptr(B), M, N, K,
+                                      A.shape[1], B.shape[1], float(alpha), float(beta), _ptr(cin), int(cin_type),
+                                      cin.shape[1] if cin is not None else N, _ptr(bs), int(bias_type), _ptr(D),
+                                      int(out_type), D.shape[1])
+    if rc:
+        raise ValueError(f"oracle_gemm_epilogue rejected the arguments (rc={rc})")
+    return D[:, :N]
+
+
+def f32_to_16bit_array(x, out_type):
+    """Vectorised oracle rounding of float32 values to F16 or BF16 bit patterns."""
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.empty(x.shape, np.uint16)
+    fn = _load().oracle_f32_to_f16_n if out_type == F16 else _load().oracle_f32_to_bf16_n
+    fn(_ptr(x), _ptr(out), x.size)
+    return out

@@ -276,6 +276,144 @@ int oracle_gemm_ex_elems(int dtype, int trans_a, int trans_b, const uint16_t *A,
     return 0;
 }
 
+/* ---------------------------------------------------------------------------------
+ * Epilogue (the plain reading of a scaled, biased product written in a chosen type):
+ *
+ *     D[i][j] = round_out( alpha * S[i][j] + beta * Cin[i][j] + bias[j] )
+ *
+ *   S is the FP64 sum of oracle_gemm_ex_rows_f32 before its final rounding; the scaled sum,
+ *   the FP64 values of Cin and bias (decoded from their types) are combined in FP64 and
+ *   rounded once to FP32; a narrower output type is then produced from that FP32 value by
+ *   round-to-nearest-even (FP16 through a C conversion of the FP32 value, which is exact
+ *   to double and then rounded by the binary16 rule below; BF16 by rounding the FP32 bit
+ *   pattern to its upper 16 bits).  beta == 0 does not read Cin; bias may be NULL.
+ *   Types: 0 FP16, 1 BF16, 2 FP32.
+ * --------------------------------------------------------------------------------- */
+static double decode_any(const void *p, int type, int64_t idx)
+{
+    if (type == 2) return (double)((const float *)p)[idx];
+    const uint16_t h = ((const uint16_t *)p)[idx];
+    return type == 1 ? oracle_bf16_to_f64(h) : oracle_f16_to_f64(h);
+}
+
+/* binary16 of a float by round to nearest, ties to even (IEEE 754: 11-bit significands,
+ * exponents -14..15, subnormals in steps of 2^-24, overflow to infinity).  The float is
+ * m * 2^p exactly; its binary16 quantum at that magnitude is 2^qe with
+ * qe = max(floor(log2|f|) - 10, -24); q = m * 2^(p - qe) rounded to an integer. */
+uint16_t oracle_f32_to_f16(float f)
+{
+    union {
+        float f;
+        uint32_t u;
+    } v;
+    v.f = f;
+    const uint16_t sign = (uint16_t)((v.u >> 16) & 0x8000u);
+    const uint32_t ex = (v.u >> 23) & 0xffu, man = v.u & 0x7fffffu;
+    if (ex == 0xffu) return (uint16_t)(sign | 0x7c00u | (man ? 0x200u : 0u));
+    if (ex == 0 && man == 0) return sign;
+    const uint64_t m = ex ? (man | 0x800000u) : man;
+    const int p = ex ? (int)ex - 150 : -149;
+    const int bl = 64 - __builtin_clzll(m);
+    const int e = p + bl - 1;
+    int qe = e - 10 < -24 ? -24 : e - 10;
+    uint64_t q;
+    if (qe > p) {
+        const int rs = qe - p;
+        if (rs > 63) {
+            q = 0;
+        } else {
+            q = m >> rs;
+            const uint64_t rem = m & ((1ull << rs) - 1), half = 1ull << (rs - 1);
+            if (rem > half || (rem == half && (q & 1))) ++q;
+        }
+    } else {
+        q = m << (p - qe);
+    }
+    if (q == 2048) { /* rounded up into the next binade */
+        q = 1024;
+        ++qe;
+    }
+    if (q < 1024) return (uint16_t)(sign | q); /* subnormal, qe == -24 */
+    const int field = qe + 25;
+    if (field >= 31) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | ((uint32_t)field << 10) | (uint32_t)(q - 1024));
+}
+
+/* bfloat16 of a float: its upper 16 bits after round to nearest, ties to even on the lower
+ * 16 bits (NaN stays NaN). */
+uint16_t oracle_f32_to_bf16(float f)
+{
+    union {
+        float f;
+        uint32_t u;
+    } v;
+    v.f = f;
+    if (((v.u >> 23) & 0xffu) == 0xffu) return (uint16_t)((v.u >> 16) | ((v.u & 0xffffu) ? 0x40u : 0u));
+    const uint32_t lower = v.u & 0xffffu, upper = v.u >> 16;
+    uint32_t r = upper;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) ++r;
+    return (uint16_t)r;
+}
+
+void oracle_f32_to_f16_n(const float *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_f16(x[i]);
+}
+
+void oracle_f32_to_bf16_n(const float *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(x[i]);
+}
+
+int oracle_gemm_epilogue(int ab_type, int trans_a, int trans_b, const uint16_t *A, const uint16_t *B, int64_t M,
+                         int64_t N, int64_t K, int64_t lda, int64_t ldb, double alpha, double beta,
+                         const void *Cin, int cin_type, int64_t ldcin, const void *bias, int bias_type, void *D,
+                         int d_type, int64_t ldd)
+{
+    if (d_type < 0 || d_type > 2 || cin_type < 0 || cin_type > 2 || bias_type < 0 || bias_type > 2) return 1;
+    if (M < 0 || N < 0 || ldd < N || (beta != 0.0 && (!Cin || ldcin < N))) return 1;
+    if (M == 0 || N == 0) return 0;
+    float *S = (float *)malloc((size_t)M * (size_t)N * sizeof(float));
+    double *S64 = (double *)malloc((size_t)M * (size_t)N * sizeof(double));
+    if (!S || !S64) {
+        free(S);
+        free(S64);
+        return 2;
+    }
+    /* the FP64 sums, row by row, through the generalised definition's element routine */
+    int64_t *rows = (int64_t *)malloc((size_t)N * sizeof(int64_t));
+    int64_t *cols = (int64_t *)malloc((size_t)N * sizeof(int64_t));
+    int rc = (!rows || !cols) ? 2 : 0;
+    for (int64_t i = 0; i < M && !rc; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            rows[j] = i;
+            cols[j] = j;
+        }
+        rc = oracle_gemm_ex_elems(ab_type, trans_a, trans_b, A, B, M, N, K, lda, ldb, rows, cols, N, S64 + i * N,
+                                  S + i * N);
+    }
+    free(rows);
+    free(cols);
+    if (!rc) {
+        for (int64_t i = 0; i < M; ++i)
+            for (int64_t j = 0; j < N; ++j) {
+                double x = alpha * S64[i * N + j];
+                if (beta != 0.0) x += beta * decode_any(Cin, cin_type, i * ldcin + j);
+                if (bias) x += decode_any(bias, bias_type, j);
+                const float f = (float)x;
+                if (d_type == 2)
+                    ((float *)D)[i * ldd + j] = f;
+                else if (d_type == 1)
+                    ((uint16_t *)D)[i * ldd + j] = oracle_f32_to_bf16(f);
+                else
+                    ((uint16_t *)D)[i * ldd + j] = oracle_f32_to_f16(f);
+            }
+    }
+    free(S);
+    free(S64);
+    return rc;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP
