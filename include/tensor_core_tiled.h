@@ -102,7 +102,7 @@ TCT_API gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int6
                             const gemm_options *opt);
 
 /* Operand element type and storage of gemm_f32acc. */
-typedef enum gemm_dtype { GEMM_DTYPE_F16 = 0, GEMM_DTYPE_BF16 = 1 } gemm_dtype;
+typedef enum gemm_dtype { GEMM_DTYPE_F16 = 0, GEMM_DTYPE_BF16 = 1, GEMM_DTYPE_F32 = 2 } gemm_dtype;
 typedef enum gemm_op { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op;
 
 /*
@@ -123,6 +123,34 @@ typedef enum gemm_op { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op;
 TCT_API gemm_status gemm_f32acc(int32_t ab_type, int32_t op_a, int32_t op_b, const void *A, const void *B,
                                 float *C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                 int64_t ldc, void *stream, const gemm_options *opt);
+
+/*
+ * Epilogue of gemm_ex: C = alpha * op(A).op(B) + beta * C + bias[j] for every row, computed
+ * in FP32 and stored in C's type (narrower types by round to nearest even).
+ *   alpha, beta : finite scale factors; beta == 0 means C is not read (any content, NaN
+ *                 included, is overwritten).
+ *   bias        : NULL, or N values of bias_type added to each row (aligned to its type).
+ *   bias_type   : GEMM_DTYPE_F32, GEMM_DTYPE_F16 or GEMM_DTYPE_BF16.
+ *   reserved    : must be zero.
+ */
+typedef struct gemm_epilogue {
+    float alpha;
+    float beta;
+    const void *bias;
+    int32_t bias_type;
+    int32_t reserved;
+} gemm_epilogue;
+
+/*
+ * gemm_ex -- C = alpha * op(A).op(B) + beta * C + bias, FP16/BF16 operands stored as for
+ * gemm_f32acc, FP32 accumulation, C of c_type (GEMM_DTYPE_F32, F16 or BF16), row-major with
+ * ldc >= N and aligned to its type.  epi may be NULL (alpha 1, beta 0, no bias).  With
+ * K == 0 the product is the empty sum, so C = beta * C + bias.  Stream semantics, options
+ * and errors as for gemm_f16_f32_ex.
+ */
+TCT_API gemm_status gemm_ex(int32_t ab_type, int32_t op_a, int32_t op_b, const void *A, const void *B, void *C,
+                            int32_t c_type, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                            int64_t ldc, const gemm_epilogue *epi, void *stream, const gemm_options *opt);
 
 /*
  * Launch plan the library would use for a problem (host only, no GPU needed when

@@ -18,7 +18,7 @@ GEMM_ERR_UNSUPPORTED_DEVICE = 2
 GEMM_ERR_CUDA = 3
 GEMM_ERR_DEVICE_TIMEOUT = 4
 
-GEMM_DTYPE_F16, GEMM_DTYPE_BF16 = 0, 1
+GEMM_DTYPE_F16, GEMM_DTYPE_BF16, GEMM_DTYPE_F32 = 0, 1, 2
 GEMM_OP_N, GEMM_OP_T = 0, 1
 
 # Every function the header declares (checked by the test-suite against the .so).
@@ -27,6 +27,7 @@ EXPORTED = (
     "gemm_f16_f32_ex",
     "gemm_f16_f32_noalloc",
     "gemm_f32acc",
+    "gemm_ex",
     "gemm_f16_f32_plan",
     "gemm_f16_f32_work_item",
     "gemm_tile_coord",
@@ -58,6 +59,11 @@ class GemmPlan(ctypes.Structure):
                 ("effective_waves", ctypes.c_double)]
 
 
+class GemmEpilogue(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("bias_type", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 class GemmWork(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int32), ("kb0", ctypes.c_int32), ("kb1", ctypes.c_int32), ("mode", ctypes.c_int32),
                 ("part", ctypes.c_int32)]
@@ -84,6 +90,9 @@ def load():
     lib.gemm_f32acc.restype = ctypes.c_int
     lib.gemm_f32acc.argtypes = [i32, i32, i32, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp,
                                 ctypes.POINTER(GemmOptions)]
+    lib.gemm_ex.restype = ctypes.c_int
+    lib.gemm_ex.argtypes = [i32, i32, i32, vp, vp, vp, i32, i64, i64, i64, i64, i64, i64,
+                            ctypes.POINTER(GemmEpilogue), vp, ctypes.POINTER(GemmOptions)]
     lib.gemm_f16_f32_ex.restype = ctypes.c_int
     lib.gemm_f16_f32_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, ctypes.POINTER(GemmOptions)]
     lib.gemm_f16_f32_plan.restype = ctypes.c_int
@@ -150,6 +159,16 @@ def gemm_f32acc(ab_type, op_a, op_b, A, B, C, M, N, K, lda, ldb, ldc, stream=0, 
     opt = _options(**options)
     return load().gemm_f32acc(ab_type, op_a, op_b, A, B, C, M, N, K, lda, ldb, ldc, stream or None,
                               ctypes.byref(opt))
+
+
+def gemm_ex(ab_type, op_a, op_b, A, B, C, c_type, M, N, K, lda, ldb, ldc, alpha=1.0, beta=0.0, bias=0,
+            bias_type=GEMM_DTYPE_F32, stream=0, **options):
+    """Raw C-ABI call with the epilogue C = alpha * op(A) op(B) + beta * C + bias (pointers as ints)."""
+    epi = GemmEpilogue()
+    epi.alpha, epi.beta, epi.bias, epi.bias_type, epi.reserved = alpha, beta, bias or None, bias_type, 0
+    opt = _options(**options)
+    return load().gemm_ex(ab_type, op_a, op_b, A, B, C, c_type, M, N, K, lda, ldb, ldc, ctypes.byref(epi),
+                          stream or None, ctypes.byref(opt))
 
 
 def gemm_f16_f32_plan(M, N, K, lda=None, ldb=None, num_sms=0, **options):
@@ -250,4 +269,36 @@ def matmul(A, B, C=None, stream=None, **options):
                              **options)
     if st:
         raise GemmError(st, "gemm_f32acc" if (dt or op_a or op_b) else "gemm_f16_f32")
+    return C
+
+
+def gemm(A, B, C=None, alpha=1.0, beta=0.0, bias=None, out_dtype=None, stream=None, **options):
+    """C = alpha * A @ B + beta * C + bias for torch CUDA tensors (A, B float16 or bfloat16,
+    row- or column-major; bias None or a length-N float32/float16/bfloat16 vector; C row-major
+    float32/float16/bfloat16, allocated as out_dtype (default float32) when None)."""
+    import torch
+    types = {torch.float16: GEMM_DTYPE_F16, torch.bfloat16: GEMM_DTYPE_BF16, torch.float32: GEMM_DTYPE_F32}
+    if A.dim() != 2 or B.dim() != 2 or A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("A and B must be 2-D, both float16 or both bfloat16")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if C is None:
+        C = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
+    if C.dtype not in types or tuple(C.shape) != (M, N) or (C.numel() and N > 1 and C.stride(1) != 1):
+        raise ValueError("C must be a row-major M x N float32/float16/bfloat16 tensor")
+    if bias is not None and (bias.dim() != 1 or bias.numel() != N or bias.dtype not in types or
+                             (N > 1 and bias.stride(0) != 1)):
+        raise ValueError("bias must be a contiguous length-N float32/float16/bfloat16 vector")
+    op_a, lda = _operand(A, M, K, "A")
+    op_b, ldb = _operand(B, K, N, "B")
+    ldc = C.stride(0) if M > 1 else max(N, 1)
+    s = stream.cuda_stream if stream is not None else _current_stream_ptr(A.device)
+    with torch.cuda.device(A.device):
+        st = gemm_ex(types[A.dtype], op_a, op_b, A.data_ptr(), B.data_ptr(), C.data_ptr(), types[C.dtype], M, N, K,
+                     lda, ldb, ldc, alpha, beta, bias.data_ptr() if bias is not None else 0,
+                     types[bias.dtype] if bias is not None else GEMM_DTYPE_F32, s, **options)
+    if st:
+        raise GemmError(st, "gemm_ex")
     return C

@@ -177,14 +177,16 @@ bool a_t(int layout) { return (layout & 1) != 0; }
 bool b_t(int layout) { return (layout & 2) != 0; }
 bool is_bf16(int layout) { return (layout & 4) != 0; }
 
-gemm_status check_args(const void *A, const void *B, const float *C, int64_t M, int64_t N, int64_t K,
-                       int64_t lda, int64_t ldb, int64_t ldc, int layout = 0)
+int type_bytes(int t) { return t == GEMM_DTYPE_F32 ? 4 : 2; }
+
+gemm_status check_args(const void *A, const void *B, const void *C, int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc, int layout = 0, int c_type = GEMM_DTYPE_F32)
 {
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_ARG;
     if (lda < (a_t(layout) ? M : K) || ldb < (b_t(layout) ? K : N) || ldc < N) return GEMM_ERR_INVALID_ARG;
     if (lda > kMaxDim * 4 || ldb > kMaxDim * 4 || ldc > kMaxDim * 4) return GEMM_ERR_INVALID_ARG;
     if (M > 0 && N > 0) {
-        if (!C || reinterpret_cast<uintptr_t>(C) % 4 != 0) return GEMM_ERR_INVALID_ARG;
+        if (!C || reinterpret_cast<uintptr_t>(C) % type_bytes(c_type) != 0) return GEMM_ERR_INVALID_ARG;
     }
     if (M > 0 && N > 0 && K > 0) {
         if (!A || reinterpret_cast<uintptr_t>(A) % 2 != 0) return GEMM_ERR_INVALID_ARG;
@@ -313,11 +315,24 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
 }
 
 // Kernel parameters for a plan (the caller sets `workspace` when stream-K is used).
+// Epilogue fields of the kernel parameters (identity when epi is NULL).
+void set_epilogue(tct::KernelParams &p, void *C, int c_type, int64_t ldc, const gemm_epilogue *epi)
+{
+    p.C = C;
+    p.c_type = c_type;
+    p.vec_store = (reinterpret_cast<uintptr_t>(C) % (4 * type_bytes(c_type)) == 0 && ldc % 4 == 0) ? 1 : 0;
+    p.alpha = epi ? epi->alpha : 1.0f;
+    p.beta = epi ? epi->beta : 0.0f;
+    p.bias = epi ? epi->bias : nullptr;
+    p.bias_type = epi ? epi->bias_type : GEMM_DTYPE_F32;
+    p.epi = (p.alpha != 1.0f || p.beta != 0.0f || p.bias != nullptr) ? 1 : 0;
+}
+
 tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t N, int64_t K, int64_t ldc,
                               int timeout_ms)
 {
     tct::KernelParams p;
-    p.C = C;
+    set_epilogue(p, C, GEMM_DTYPE_F32, ldc, nullptr);
     p.ldc = ldc;
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
@@ -327,7 +342,6 @@ tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t 
     p.num_kb = static_cast<int32_t>(tct::ceil_div(K, kTileK));
     p.num_tiles = static_cast<int32_t>(pl.tiles);
     p.group_m = pl.group_m;
-    p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 1 : 0;
     p.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
     p.units = pl.units;
     p.dp_tiles = static_cast<int32_t>(pl.tiles - pl.stream_k_tiles);
@@ -385,10 +399,26 @@ int device_pair_slots(DeviceInfo *dev)
 gemm_status to_status(cudaError_t e) { return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA; }
 
 // The launch sequence for every operand layout (see make_plan for the layout bits).
-gemm_status run_gemm(int layout, const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
-                     int64_t lda, int64_t ldb, int64_t ldc, void *stream, const gemm_options *opt)
+gemm_status check_epilogue(int c_type, const gemm_epilogue *epi)
 {
-    gemm_status st = check_args(A, B, C, M, N, K, lda, ldb, ldc, layout);
+    if (c_type != GEMM_DTYPE_F16 && c_type != GEMM_DTYPE_BF16 && c_type != GEMM_DTYPE_F32) return GEMM_ERR_INVALID_ARG;
+    if (!epi) return GEMM_OK;
+    if (epi->reserved != 0) return GEMM_ERR_INVALID_ARG;
+    if (epi->bias_type != GEMM_DTYPE_F16 && epi->bias_type != GEMM_DTYPE_BF16 && epi->bias_type != GEMM_DTYPE_F32)
+        return GEMM_ERR_INVALID_ARG;
+    if (epi->bias && reinterpret_cast<uintptr_t>(epi->bias) % type_bytes(epi->bias_type) != 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (!std::isfinite(epi->alpha) || !std::isfinite(epi->beta)) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_type, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, const gemm_epilogue *epi, void *stream,
+                     const gemm_options *opt)
+{
+    gemm_status st = check_args(A, B, C, M, N, K, lda, ldb, ldc, layout, c_type);
+    if (st != GEMM_OK) return st;
+    st = check_epilogue(c_type, epi);
     if (st != GEMM_OK) return st;
     st = check_options(opt);
     if (st != GEMM_OK) return st;
@@ -397,7 +427,14 @@ gemm_status run_gemm(int layout, const void *A, const void *B, float *C, int64_t
     st = device_info(&dev);
     if (st != GEMM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return to_status(tct::launch_fill_zero(C, ldc, M, N, dev.sms, s));
+    if (K == 0) {
+        tct::KernelParams p{};
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.ldc = ldc;
+        set_epilogue(p, C, c_type, ldc, epi);
+        return to_status(tct::launch_fill_epilogue(p, dev.sms, s));
+    }
 
     gemm_plan pl;
     st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), opt, A, B, &pl, true, layout);
@@ -452,7 +489,8 @@ gemm_status run_gemm(int layout, const void *A, const void *B, float *C, int64_t
                              b_t(layout) ? static_cast<uint32_t>(pl.tile_n / pl.cta_group) : kTileK, is_bf16(layout));
     if (st == GEMM_OK) {
         const int tmo = opt && opt->timeout_ms ? opt->timeout_ms : kDefaultTimeoutMs;
-        tct::KernelParams p = make_params(pl, C, M, N, K, ldc, tmo);
+        tct::KernelParams p = make_params(pl, nullptr, M, N, K, ldc, tmo);
+        set_epilogue(p, C, c_type, ldc, epi);
         p.fault_inject = opt ? opt->fault_inject : 0;
         CUtensorMap tp;
         std::memset(&tp, 0, sizeof(tp));
@@ -478,7 +516,7 @@ extern "C" {
 gemm_status gemm_f16_f32_ex(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
                             int64_t lda, int64_t ldb, int64_t ldc, void *stream, const gemm_options *opt)
 {
-    return run_gemm(0, A, B, C, M, N, K, lda, ldb, ldc, stream, opt);
+    return run_gemm(0, A, B, C, GEMM_DTYPE_F32, M, N, K, lda, ldb, ldc, nullptr, stream, opt);
 }
 
 gemm_status gemm_f32acc(int32_t ab_type, int32_t op_a, int32_t op_b, const void *A, const void *B, float *C,
@@ -489,7 +527,18 @@ gemm_status gemm_f32acc(int32_t ab_type, int32_t op_a, int32_t op_b, const void 
         (op_b != GEMM_OP_N && op_b != GEMM_OP_T))
         return GEMM_ERR_INVALID_ARG;
     const int layout = (op_a == GEMM_OP_T ? 1 : 0) | (op_b == GEMM_OP_T ? 2 : 0) | (ab_type == GEMM_DTYPE_BF16 ? 4 : 0);
-    return run_gemm(layout, A, B, C, M, N, K, lda, ldb, ldc, stream, opt);
+    return run_gemm(layout, A, B, C, GEMM_DTYPE_F32, M, N, K, lda, ldb, ldc, nullptr, stream, opt);
+}
+
+gemm_status gemm_ex(int32_t ab_type, int32_t op_a, int32_t op_b, const void *A, const void *B, void *C,
+                    int32_t c_type, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                    const gemm_epilogue *epi, void *stream, const gemm_options *opt)
+{
+    if ((ab_type != GEMM_DTYPE_F16 && ab_type != GEMM_DTYPE_BF16) || (op_a != GEMM_OP_N && op_a != GEMM_OP_T) ||
+        (op_b != GEMM_OP_N && op_b != GEMM_OP_T))
+        return GEMM_ERR_INVALID_ARG;
+    const int layout = (op_a == GEMM_OP_T ? 1 : 0) | (op_b == GEMM_OP_T ? 2 : 0) | (ab_type == GEMM_DTYPE_BF16 ? 4 : 0);
+    return run_gemm(layout, A, B, C, c_type, M, N, K, lda, ldb, ldc, epi, stream, opt);
 }
 
 gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
@@ -642,7 +691,14 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
     st = device_info(&dev);
     if (st != GEMM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return to_status(tct::launch_fill_zero(C, ldc, M, N, dev.sms, s));
+    if (K == 0) {
+        tct::KernelParams p{};
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.ldc = ldc;
+        set_epilogue(p, C, GEMM_DTYPE_F32, ldc, nullptr);
+        return to_status(tct::launch_fill_epilogue(p, dev.sms, s));
+    }
 
     gemm_plan pl;
     st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), nullptr, A, B, &pl,

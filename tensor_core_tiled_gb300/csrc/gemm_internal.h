@@ -13,12 +13,19 @@ namespace tct {
 constexpr unsigned GEMM_ERR_DEVICE_TIMEOUT_CODE = 4u;
 
 struct KernelParams {
-    float *C;
+    void *C;  // element type c_type
     int64_t ldc;
     int32_t M, N, K;
     int32_t num_m, num_n, num_kb, num_tiles;
     int32_t group_m;
-    int32_t vec_store;  // 1 when C is 16-byte aligned and ldc % 4 == 0
+    int32_t vec_store;  // 1 when C is aligned to 4 elements and ldc % 4 == 0
+    // Epilogue: C = alpha * acc + beta * C + bias[col], in c_type (0 FP16, 1 BF16, 2 FP32).
+    // epi == 0 means alpha 1, beta 0, no bias (C is not read).
+    int32_t c_type;
+    int32_t epi;
+    float alpha, beta;
+    const void *bias;
+    int32_t bias_type;
     uint64_t timeout_ns;
     // Work split.  `units` CTAs (cta_group 1) or CTA pairs (cta_group 2) first take whole
     // tiles 0 .. dp_tiles-1 (tile u + i * units goes to unit u).  The last split_tiles tiles
@@ -128,8 +135,8 @@ cudaError_t launch_pack2(const void *src0, int64_t ld_src0, void *dst0, int64_t 
                          const void *src1, int64_t ld_src1, void *dst1, int64_t ld_dst1, int64_t rows1, int64_t cols1,
                          cudaStream_t stream);
 
-cudaError_t launch_fill_zero(float *C, int64_t ldc, int64_t rows, int64_t cols, int num_sms,
-                             cudaStream_t stream);
+// K == 0: C = beta * C + bias[col] (the empty sum), or zeros when epi == 0.
+cudaError_t launch_fill_epilogue(const KernelParams &p, int num_sms, cudaStream_t stream);
 
 cudaError_t read_and_clear_error(unsigned *out);
 

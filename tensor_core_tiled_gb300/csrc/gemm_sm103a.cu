@@ -31,6 +31,8 @@
 //   * Every pipeline wait is bounded in wall time; on expiry the CTA records an error
 //     code in a device word, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -127,13 +129,73 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 // this warp's 32 rows of the split tile's other half, staged in shared memory as 32 rows
 // of BN floats, is added before the store.
 struct TileDst {
-    float *base;
+    void *base;
     int64_t ld;
     int64_t rows, cols;
     bool vec;
     bool streaming;
     const float *part;
+    // epilogue (C stores only): out_type 0 FP16, 1 BF16, 2 FP32; when epi, the stored value
+    // is alpha * acc + beta * (current C) + bias[col]
+    int out_type;
+    bool epi;
+    float alpha, beta;
+    const void *bias;
+    int bias_type;
 };
+
+__device__ __forceinline__ float load_typed(const void *p, int type, int64_t i)
+{
+    if (type == 2) return __ldg(static_cast<const float *>(p) + i);
+    const unsigned short h = __ldg(static_cast<const unsigned short *>(p) + i);
+    return type == 1 ? __bfloat162float(__ushort_as_bfloat16(h)) : __half2float(__ushort_as_half(h));
+}
+
+__device__ __forceinline__ unsigned short to_16bit(float v, int type)
+{
+    return type == 1 ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
+}
+
+// Epilogue and store of 4 consecutive outputs (row grow, columns gcol..gcol+3), any type.
+__device__ __forceinline__ void store_general(const TileDst &d, int64_t grow, int64_t gcol, float4 v)
+{
+    float x[4] = {v.x, v.y, v.z, v.w};
+    const bool full = d.vec && gcol + 3 < d.cols;
+    if (d.epi) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (!full && gcol + e >= d.cols) continue;
+            float y = d.alpha * x[e];
+            if (d.beta != 0.0f) y = fmaf(d.beta, load_typed(d.base, d.out_type, grow * d.ld + gcol + e), y);
+            if (d.bias) y += load_typed(d.bias, d.bias_type, gcol + e);
+            x[e] = y;
+        }
+    }
+    if (d.out_type == 2) {
+        float *dst = static_cast<float *>(d.base) + grow * d.ld + gcol;
+        if (full) {
+            __stcs(reinterpret_cast<float4 *>(dst), make_float4(x[0], x[1], x[2], x[3]));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (gcol + e < d.cols) __stcs(dst + e, x[e]);
+        }
+    } else {
+        unsigned short *dst = static_cast<unsigned short *>(d.base) + grow * d.ld + gcol;
+        if (full) {
+            uint2 w;
+            w.x = static_cast<uint32_t>(to_16bit(x[0], d.out_type)) |
+                  (static_cast<uint32_t>(to_16bit(x[1], d.out_type)) << 16);
+            w.y = static_cast<uint32_t>(to_16bit(x[2], d.out_type)) |
+                  (static_cast<uint32_t>(to_16bit(x[3], d.out_type)) << 16);
+            __stcs(reinterpret_cast<uint2 *>(dst), w);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (gcol + e < d.cols) dst[e] = to_16bit(x[e], d.out_type);
+        }
+    }
+}
 
 // One accumulator buffer (this warp's 32 TMEM lanes x BN columns) to global memory.
 // `release` is called by lane 0 once every column has been read from TMEM.
@@ -175,8 +237,10 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst 
                 v.w += a.w;
             }
             const int64_t grow = row_base + rr;
-            if (grow < d.rows) {
-                float *dst = d.base + grow * d.ld + gcol;
+            if (grow < d.rows && (d.epi || d.out_type != 2)) {
+                store_general(d, grow, gcol, v);
+            } else if (grow < d.rows) {
+                float *dst = static_cast<float *>(d.base) + grow * d.ld + gcol;
                 if (d.vec && gcol + 3 < d.cols) {
                     if (d.streaming)
                         __stcs(reinterpret_cast<float4 *>(dst), v);
@@ -448,12 +512,14 @@ __global__ void __launch_bounds__(192, 1)
             const TileCoord c = tile_coord(w.tile, p.num_m, p.num_n, p.group_m);
             const int64_t lane_rows = static_cast<int64_t>(rank) * Cf::BM + q * 32;  // tile-local
             constexpr int64_t kTileElems = static_cast<int64_t>(Cf::BM * CG) * BN;
-            TileDst d{p.C, p.ldc, p.M, p.N, p.vec_store != 0, true, nullptr};
+            TileDst d{p.C,     p.ldc,   p.M,    p.N,    p.vec_store != 0, true,       nullptr,
+                      p.c_type, p.epi != 0, p.alpha, p.beta, p.bias,            p.bias_type};
             int64_t row_base = static_cast<int64_t>(c.m) * (Cf::BM * CG) + lane_rows;
             int64_t col_base = static_cast<int64_t>(c.n) * BN;
             if (w.mode == WORK_PARTIAL) {
                 // second half of a split tile for its owner: the whole tile, tile-local rows
-                d = TileDst{p.workspace + w.part * kTileElems, BN, Cf::BM * CG, BN, true, false, nullptr};
+                d = TileDst{p.workspace + w.part * kTileElems, BN, Cf::BM * CG, BN, true, false, nullptr,
+                            2, false, 1.0f, 0.0f, nullptr, 2};
                 row_base = lane_rows;
                 col_base = 0;
             } else if (w.mode == WORK_FIXUP) {
@@ -548,14 +614,17 @@ __global__ void pack_rows_f16(const PackJob j0, const PackJob j1)
     }
 }
 
-// K == 0: the empty sum.
-__global__ void fill_zero_f32(float *__restrict__ C, int64_t ldc, int64_t rows, int64_t cols)
+// K == 0: the empty sum, through the epilogue (C = beta * C + bias[col], or zeros).
+__global__ void fill_epilogue(const KernelParams p)
 {
-    const int64_t total = rows * cols;
+    TileDst d{p.C, p.ldc, p.M, p.N, false, true, nullptr, p.c_type, p.epi != 0, p.alpha, p.beta, p.bias, p.bias_type};
+    const int64_t cols4 = (static_cast<int64_t>(p.N) + 3) / 4;
+    const int64_t total = static_cast<int64_t>(p.M) * cols4;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / cols;
-        C[r * ldc + (i - r * cols)] = 0.0f;
+        const int64_t r = i / cols4;
+        const int64_t c = (i - r * cols4) * 4;
+        store_general(d, r, c, make_float4(0.f, 0.f, 0.f, 0.f));
     }
 }
 
@@ -728,15 +797,14 @@ cudaError_t launch_pack2(const void *src0, int64_t ld_src0, void *dst0, int64_t 
     return cudaSuccess;
 }
 
-cudaError_t launch_fill_zero(float *C, int64_t ldc, int64_t rows, int64_t cols, int num_sms,
-                             cudaStream_t stream)
+cudaError_t launch_fill_epilogue(const KernelParams &p, int num_sms, cudaStream_t stream)
 {
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const int64_t total = rows * cols;
+    const int64_t total = static_cast<int64_t>(p.M) * ((static_cast<int64_t>(p.N) + 3) / 4);
+    if (total <= 0) return cudaSuccess;
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
-    fill_zero_f32<<<static_cast<int>(blocks), 256, 0, stream>>>(C, ldc, rows, cols);
+    fill_epilogue<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

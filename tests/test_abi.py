@@ -70,6 +70,12 @@ def test_invalid_arguments_rejected_before_any_device_work(tct_lib):
     assert tct.gemm_f32acc(1, 1, 0, p, p, p, 8, 4, 2, 4, 4, 4, 0) == tct.GEMM_ERR_INVALID_ARG   # lda < M
     assert tct.gemm_f32acc(1, 0, 1, p, p, p, 4, 8, 6, 6, 4, 8, 0) == tct.GEMM_ERR_INVALID_ARG   # ldb < K
     assert tct.gemm_f32acc(1, 1, 1, 0, 0, 0, 0, 4, 4, 1, 4, 4, 0) == tct.GEMM_OK                # empty
+    # epilogue entry: bad C type, misaligned typed C or bias, non-finite scale
+    assert tct.gemm_ex(0, 0, 0, p, p, p, 3, 4, 4, 4, 4, 4, 4) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_ex(0, 0, 0, p, p, p + 2, 2, 4, 4, 4, 4, 4, 4) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_ex(0, 0, 0, p, p, p + 1, 0, 4, 4, 4, 4, 4, 4) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_ex(0, 0, 0, p, p, p, 2, 4, 4, 4, 4, 4, 4, bias=p + 2, bias_type=2) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_ex(0, 0, 0, p, p, p, 2, 4, 4, 4, 4, 4, 4, alpha=float("inf")) == tct.GEMM_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("num_m,num_n", [(9, 9), (7, 14), (32, 16), (13, 5), (1, 40), (40, 1)])
