@@ -74,6 +74,8 @@ def _load():
     lib.oracle_gemm_epilogue.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, i64, i64, i64, i64, i64,
                                          ctypes.c_double, ctypes.c_double, vp, ctypes.c_int, i64, vp, ctypes.c_int,
                                          vp, ctypes.c_int, i64]
+    lib.oracle_softmax_rows_f32.restype = ctypes.c_int
+    lib.oracle_softmax_rows_f32.argtypes = [vp, vp, i64, i64, i64, i64]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_set_num_threads.restype = None
@@ -284,3 +286,16 @@ def f32_to_16bit_array(x, out_type):
     fn = _load().oracle_f32_to_f16_n if out_type == F16 else _load().oracle_f32_to_bf16_n
     fn(_ptr(x), _ptr(out), x.size)
     return out
+
+
+# ---- row softmax ------------------------------------------------------------------------
+
+def softmax_rows_f32(X):
+    """Row softmax of a 2-D float32 array: FP64 arithmetic, one final round to FP32."""
+    X = np.ascontiguousarray(X, np.float32)
+    M, N = X.shape
+    Y = np.zeros((M, max(N, 1)), np.float32)
+    rc = _load().oracle_softmax_rows_f32(_ptr(X), _ptr(Y), M, N, N, Y.shape[1])
+    if rc:
+        raise ValueError(f"oracle_softmax_rows_f32 rejected the arguments (rc={rc})")
+    return Y[:, :N]

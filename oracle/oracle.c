@@ -414,6 +414,41 @@ int oracle_gemm_epilogue(int ab_type, int trans_a, int trans_b, const uint16_t *
     return rc;
 }
 
+/* ---------------------------------------------------------------------------------
+ * Row softmax ("06_triton_style.py", demo 3: the fused softmax workload): for each row x
+ * of an M x N FP32 matrix,
+ *
+ *     y[j] = exp(x[j] - max_k x[k]) / sum_k exp(x[k] - max_k x[k])
+ *
+ * in FP64 (the max subtracted first, as the page's kernels do, so exp never overflows),
+ * rounded once to FP32.  exp(-inf) = 0; a row whose maximum is +inf or NaN, or that is
+ * all -inf, has no finite softmax and yields NaN in every element.
+ * --------------------------------------------------------------------------------- */
+int oracle_softmax_rows_f32(const float *X, float *Y, int64_t M, int64_t N, int64_t ldx, int64_t ldy)
+{
+    if (M < 0 || N < 0 || ldx < N || ldy < N) return 1;
+    if (M > 0 && N > 0 && (!X || !Y)) return 1;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < M; ++i) {
+        const float *x = X + i * ldx;
+        float *y = Y + i * ldy;
+        double m = -INFINITY;
+        int bad = 0;
+        for (int64_t j = 0; j < N; ++j) {
+            if (isnan(x[j])) bad = 1;
+            if ((double)x[j] > m) m = (double)x[j];
+        }
+        if (bad || isinf(m)) {
+            for (int64_t j = 0; j < N; ++j) y[j] = NAN;
+            continue;
+        }
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j) s += exp((double)x[j] - m);
+        for (int64_t j = 0; j < N; ++j) y[j] = (float)(exp((double)x[j] - m) / s);
+    }
+    return 0;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP
