@@ -240,6 +240,19 @@ TCT_API gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float *C,
                                          int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void *stream);
 
 /*
+ * softmax_rows_f32 -- Y[i][j] = exp(X[i][j] - max_k X[i][k]) / sum_k exp(X[i][k] - max_k X[i][k])
+ * for every row of an M x N FP32 matrix: the fused row softmax of "06_triton_style.py"
+ * demo 3 (one read of X and one write of Y; rows longer than 51200 elements are read twice).
+ *   X, Y : FP32 device pointers, row-major, leading dimensions ldx, ldy >= N, 4-byte
+ *          aligned; Y may be X itself (ldy == ldx), other overlaps are undefined.
+ * exp(-inf) = 0; a row holding a NaN, whose maximum is +inf, or whose entries are all -inf
+ * is written as NaN.  M == 0 or N == 0 is a no-op.  Stream-ordered, no host sync.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED_DEVICE or GEMM_ERR_CUDA.
+ */
+TCT_API gemm_status softmax_rows_f32(const float *X, float *Y, int64_t M, int64_t N, int64_t ldx, int64_t ldy,
+                                     void *stream);
+
+/*
  * Reads and clears the device error word of the current device: GEMM_OK, or
  * GEMM_ERR_DEVICE_TIMEOUT if a kernel launched since the last read gave up on a pipeline
  * wait (its output is then incomplete).  Synchronises the current device first.

@@ -28,6 +28,7 @@ EXPORTED = (
     "gemm_f16_f32_noalloc",
     "gemm_f32acc",
     "gemm_ex",
+    "softmax_rows_f32",
     "gemm_f16_f32_plan",
     "gemm_f16_f32_work_item",
     "gemm_tile_coord",
@@ -93,6 +94,8 @@ def load():
     lib.gemm_ex.restype = ctypes.c_int
     lib.gemm_ex.argtypes = [i32, i32, i32, vp, vp, vp, i32, i64, i64, i64, i64, i64, i64,
                             ctypes.POINTER(GemmEpilogue), vp, ctypes.POINTER(GemmOptions)]
+    lib.softmax_rows_f32.restype = ctypes.c_int
+    lib.softmax_rows_f32.argtypes = [vp, vp, i64, i64, i64, i64, vp]
     lib.gemm_f16_f32_ex.restype = ctypes.c_int
     lib.gemm_f16_f32_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, ctypes.POINTER(GemmOptions)]
     lib.gemm_f16_f32_plan.restype = ctypes.c_int
@@ -302,3 +305,29 @@ def gemm(A, B, C=None, alpha=1.0, beta=0.0, bias=None, out_dtype=None, stream=No
     if st:
         raise GemmError(st, "gemm_ex")
     return C
+
+
+def softmax_rows_f32(X, Y, M, N, ldx, ldy, stream=0):
+    """Raw C-ABI call of the row softmax (pointers as ints); returns the status code."""
+    return load().softmax_rows_f32(X, Y, M, N, ldx, ldy, stream or None)
+
+
+def softmax(X, out=None, stream=None):
+    """Row softmax of a 2-D float32 CUDA tensor (row-major; out may be X for in place)."""
+    import torch
+    if X.dim() != 2 or X.dtype != torch.float32 or not X.is_cuda:
+        raise TypeError("X must be a 2-D float32 CUDA tensor")
+    M, N = X.shape
+    if N > 1 and X.stride(1) != 1:
+        raise ValueError("X must be row-major")
+    if out is None:
+        out = torch.empty_like(X)
+    if out.shape != X.shape or out.dtype != torch.float32 or (N > 1 and out.stride(1) != 1):
+        raise ValueError("out must be a row-major float32 tensor of X's shape")
+    s = stream.cuda_stream if stream is not None else _current_stream_ptr(X.device)
+    with torch.cuda.device(X.device):
+        st = softmax_rows_f32(X.data_ptr(), out.data_ptr(), M, N, X.stride(0) if M > 1 else max(N, 1),
+                              out.stride(0) if M > 1 else max(N, 1), s)
+    if st:
+        raise GemmError(st, "softmax_rows_f32")
+    return out

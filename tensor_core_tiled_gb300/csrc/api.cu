@@ -541,6 +541,18 @@ gemm_status gemm_ex(int32_t ab_type, int32_t op_a, int32_t op_b, const void *A, 
     return run_gemm(layout, A, B, C, c_type, M, N, K, lda, ldb, ldc, epi, stream, opt);
 }
 
+gemm_status softmax_rows_f32(const float *X, float *Y, int64_t M, int64_t N, int64_t ldx, int64_t ldy, void *stream)
+{
+    if (M < 0 || N < 0 || M > kMaxDim || N > kMaxDim || ldx < N || ldy < N) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!X || !Y || reinterpret_cast<uintptr_t>(X) % 4 || reinterpret_cast<uintptr_t>(Y) % 4) return GEMM_ERR_INVALID_ARG;
+    if (X == Y && ldx != ldy) return GEMM_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    const gemm_status st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    return to_status(tct::launch_softmax_rows(X, Y, M, N, ldx, ldy, dev.sms, static_cast<cudaStream_t>(stream)));
+}
+
 gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
                          int64_t lda, int64_t ldb, int64_t ldc, void *stream)
 {

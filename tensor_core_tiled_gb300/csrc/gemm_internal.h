@@ -140,4 +140,8 @@ cudaError_t launch_fill_epilogue(const KernelParams &p, int num_sms, cudaStream_
 
 cudaError_t read_and_clear_error(unsigned *out);
 
+// Row softmax of an M x N FP32 matrix (softmax_sm103a.cu).
+cudaError_t launch_softmax_rows(const float *X, float *Y, int64_t M, int64_t N, int64_t ldx, int64_t ldy, int num_sms,
+                                cudaStream_t stream);
+
 }  // namespace tct

@@ -136,3 +136,23 @@ def pair_ex(rng, M, N, K, dtype="f16", integer=False, trans_a=False, trans_b=Fal
     if trans_b:
         B = np.ascontiguousarray(B.T)
     return A, B
+
+
+# ---- row softmax inputs -------------------------------------------------------------------
+
+# The page's softmax workload ("06_triton_style.py" demo 3): a 4096 x 1024 FP32 matrix of
+# N(0,1) draws; the larger case is the same recipe at 32768 x 4096 (512 MiB, above L2).
+SOFTMAX_PAGE = (4096, 1024)
+SOFTMAX_LARGE = (32768, 4096)
+
+
+def normal_f32(rng, rows, cols):
+    """A rows x cols FP32 matrix of N(0,1) draws (float64 rounded to nearest), row-major."""
+    out = np.empty((rows, cols), np.float32)
+    if rows == 0 or cols == 0:
+        return out
+    step = max(1, _CHUNK_ELEMS // cols)
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        out[r0:r1] = rng.standard_normal((r1 - r0, cols)).astype(np.float32)
+    return out

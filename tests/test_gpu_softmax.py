@@ -1,0 +1,153 @@
+"""Parity of the fused row softmax (softmax_rows_f32) with the oracle.
+
+The workload is the one of "06_triton_style.py" demo 3: N(0,1) rows, softmax along each
+row.  Shapes cover the three kernels the library picks by row length -- a warp per row
+(N <= 2048), a CTA per row staged in shared memory (N <= 51200), and the two-pass online
+kernel beyond -- each at its boundaries, plus ragged lengths, padded and unaligned rows,
+in-place use, special values and empty shapes.
+
+Error bound (per element, relative to the exact softmax r_j, with u = 2^-24):
+  x_j - max rounds once (u |d_j| after exp), expf is within 2 ulp (4u), every term of the
+  row sum carries the same, a summation chain of n terms adds n u, the online kernel's
+  rescales add at most 5u each plus u |d|max in total, the division u, the oracle's final
+  rounding u:  |y_j - r_j| <= u (16 + |d_j| + 2 |d|max + 7 n) r_j,
+  where n = ceil(N / 32) when a warp holds the row, ceil(N / 256) otherwise, plus 8 levels
+  of tree reduction.  A dropped or doubled term of weight w moves every output by w, far
+  above this bound at the tested lengths.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import tensor_core_tiled_gb300 as tct
+from tensor_core_tiled_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+U = 2.0 ** -24
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu(tct_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+
+
+def _chain(N):
+    return math.ceil(N / 32) if N <= 2048 else math.ceil(N / 256)
+
+
+def _check(x, y):
+    """y (the kernel's output) against the oracle on x, element by element."""
+    ref = oracle.softmax_rows_f32(x)
+    assert y.shape == ref.shape
+    nan_ref = np.isnan(ref)
+    assert np.array_equal(np.isnan(y), nan_ref), "NaN rows differ"
+    valid = ~nan_ref.any(axis=1)
+    with np.errstate(invalid="ignore"):
+        d = x.astype(np.float64) - x.max(axis=1, keepdims=True).astype(np.float64)
+    ad = np.where(np.isfinite(d), np.abs(d), 0)
+    n = _chain(x.shape[1]) + 8
+    tol = U * (16 + ad + 2 * ad.max(axis=1, keepdims=True) + 7 * n) * ref + 1e-37
+    err = np.abs(y.astype(np.float64) - ref.astype(np.float64))
+    bad = ~(err <= tol) & valid[:, None]
+    assert not bad.any(), (f"{bad.sum()} elements out of tolerance; worst "
+                           f"{np.unravel_index(np.argmax(np.where(valid[:, None], err / tol, 0)), err.shape)}")
+
+
+def _run(x, inplace=False):
+    X = torch.from_numpy(x).cuda()
+    out = tct.softmax(X, out=X if inplace else None)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+# (M, N, seed): warp kernel (N = 1 .. 2048, each VEC width and ragged tails), shared-memory
+# kernel (2049 .. 51200), online kernel (51201 and longer).
+SHAPES = [(1, 1, 10), (7, 1, 11), (33, 5, 12), (300, 37, 13), (129, 128, 14), (64, 129, 15), (257, 256, 16),
+          (100, 511, 17), (65, 1000, 18), (40, 1024, 19), (31, 2047, 20), (17, 2048, 21), (9, 2049, 22),
+          (20, 3000, 23), (5, 12345, 24), (3, 51199, 25), (2, 51200, 26), (2, 51201, 27), (3, 200003, 28)]
+
+
+@pytest.mark.parametrize("M,N,seed", SHAPES)
+def test_matches_oracle(M, N, seed):
+    x = inputs.normal_f32(np.random.default_rng(seed), M, N)
+    _check(x, _run(x))
+
+
+def test_page_workload():
+    """The page's 4096 x 1024 case; row sums are 1 to within the summation bound."""
+    x = inputs.normal_f32(np.random.default_rng(2), *inputs.SOFTMAX_PAGE)
+    y = _run(x)
+    _check(x, y)
+    assert np.all(np.abs(y.astype(np.float64).sum(axis=1) - 1) < 1e-5)
+
+
+@pytest.mark.parametrize("N", [100, 5000, 70000])
+def test_wide_range_rows(N):
+    """Scaled rows (values up to +-80): exp underflows to zero for most entries."""
+    x = (inputs.normal_f32(np.random.default_rng(N), 16, N) * np.float32(20)).astype(np.float32)
+    _check(x, _run(x))
+
+
+@pytest.mark.parametrize("N", [1000, 4000, 60000])
+def test_padded_and_unaligned(N):
+    """Rows with ld > N, and a base 4 bytes off 16-byte alignment (the scalar load path)."""
+    M = 37
+    rng = np.random.default_rng(N + 1)
+    x = inputs.normal_f32(rng, M, N)
+    for ld, off in [(N + 3, 0), (N + 8, 4), (N + 1, 1)]:
+        buf = torch.full((M * ld + 8,), float("nan"), device="cuda")
+        src = buf[off:off + M * ld].view(M, ld)
+        src[:, :N] = torch.from_numpy(x).cuda()
+        ybuf = torch.full((M * ld + 8,), -7.0, device="cuda")
+        dst = ybuf[off:off + M * ld].view(M, ld)
+        st = tct.softmax_rows_f32(src.data_ptr(), dst.data_ptr(), M, N, ld, ld,
+                                  torch.cuda.current_stream().cuda_stream)
+        assert st == 0
+        torch.cuda.synchronize()
+        _check(x, dst[:, :N].cpu().numpy())
+        assert torch.all(dst[:, N:] == -7.0), "padding columns were written"
+        assert torch.all(ybuf[:off] == -7.0) and torch.all(ybuf[off + M * ld:] == -7.0)
+
+
+@pytest.mark.parametrize("N", [300, 3000, 60000])
+def test_in_place(N):
+    x = inputs.normal_f32(np.random.default_rng(N + 2), 21, N)
+    _check(x, _run(x, inplace=True))
+
+
+@pytest.mark.parametrize("N", [4, 3000, 60000])
+def test_special_values(N):
+    """-inf entries give exactly 0; rows with NaN, +inf or only -inf give NaN everywhere."""
+    x = inputs.normal_f32(np.random.default_rng(N + 3), 6, N)
+    x[1, 0] = -np.inf
+    x[1, N - 1] = -np.inf
+    x[2, N // 2] = np.nan
+    x[3, N - 1] = np.inf
+    x[4, :] = -np.inf
+    x[5, :] = 1e30
+    y = _run(x)
+    _check(x, y)
+    assert y[1, 0] == 0 and y[1, N - 1] == 0
+    assert np.isnan(y[2:5]).all()
+    assert np.all(y[5] == np.float32(1) / np.float32(N))
+
+
+def test_empty_and_invalid():
+    X = torch.zeros(4, 8, device="cuda")
+    p = X.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+    assert tct.softmax_rows_f32(p, p, 0, 8, 8, 8, s) == 0
+    assert tct.softmax_rows_f32(p, p, 4, 0, 8, 8, s) == 0
+    assert tct.softmax_rows_f32(p, p, 4, 8, 7, 8, s) == 1   # ldx < N
+    assert tct.softmax_rows_f32(p, p, 4, 8, 8, 12, s) == 1  # in place with ldx != ldy
+    assert tct.softmax_rows_f32(p + 2, p + 64, 2, 8, 8, 8, s) == 1  # misaligned
+    assert tct.softmax_rows_f32(0, p, 2, 8, 8, 8, s) == 1
+    torch.cuda.synchronize()
+    assert torch.all(X == 0)
