@@ -550,7 +550,11 @@ gemm_status softmax_rows_f32(const float *X, float *Y, int64_t M, int64_t N, int
     DeviceInfo dev;
     const gemm_status st = device_info(&dev);
     if (st != GEMM_OK) return st;
-    return to_status(tct::launch_softmax_rows(X, Y, M, N, ldx, ldy, dev.sms, static_cast<cudaStream_t>(stream)));
+    unsigned *err = nullptr;
+    if (tct::error_word_address(&err) != cudaSuccess) return GEMM_ERR_CUDA;
+    return to_status(tct::launch_softmax_rows(X, Y, M, N, ldx, ldy, dev.sms, err,
+                                              static_cast<uint64_t>(kDefaultTimeoutMs) * 1000000ull,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,

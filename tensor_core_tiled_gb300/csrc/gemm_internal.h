@@ -140,8 +140,12 @@ cudaError_t launch_fill_epilogue(const KernelParams &p, int num_sms, cudaStream_
 
 cudaError_t read_and_clear_error(unsigned *out);
 
-// Row softmax of an M x N FP32 matrix (softmax_sm103a.cu).
+// Device address of the library's error word (code | wait site << 8) on the current device.
+cudaError_t error_word_address(unsigned **out);
+
+// Row softmax of an M x N FP32 matrix (softmax_sm103a.cu).  `err` is the error word that
+// a timed-out wait records into; `timeout_ns` bounds every wait.
 cudaError_t launch_softmax_rows(const float *X, float *Y, int64_t M, int64_t N, int64_t ldx, int64_t ldy, int num_sms,
-                                cudaStream_t stream);
+                                unsigned *err, uint64_t timeout_ns, cudaStream_t stream);
 
 }  // namespace tct

@@ -808,6 +808,14 @@ cudaError_t launch_fill_epilogue(const KernelParams &p, int num_sms, cudaStream_
     return cudaGetLastError();
 }
 
+cudaError_t error_word_address(unsigned **out)
+{
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_error_word);
+    *out = static_cast<unsigned *>(ptr);
+    return e;
+}
+
 cudaError_t read_and_clear_error(unsigned *out)
 {
     cudaError_t e = cudaDeviceSynchronize();

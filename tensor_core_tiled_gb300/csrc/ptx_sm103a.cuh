@@ -165,6 +165,23 @@ __device__ __forceinline__ void tmem_wait_ld()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Bulk (non-tensor) copy of `bytes` contiguous bytes from global memory into this CTA's
+// shared memory, counted on the mbarrier `bar`.  Both addresses must be 16-byte aligned
+// and `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Barrier over the first `threads` threads of the CTA (named barrier `id`, 1..15).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ---------------------------------------------------------------- clusters / CTA pairs
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -177,6 +194,38 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
 __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Index of this CTA's cluster along x, and the number of clusters along x.
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Writes the pair (a, b) to the shared::cluster address `dst` (another CTA's shared memory,
+// or this CTA's) and counts its 8 bytes on the mbarrier at shared::cluster address `bar`,
+// which must be in the same CTA as `dst`.
+__device__ __forceinline__ void st_async_f32x2(uint32_t dst, float a, float b, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(dst),
+                 "f"(a), "f"(b), "r"(bar)
+                 : "memory");
 }
 
 // Shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.

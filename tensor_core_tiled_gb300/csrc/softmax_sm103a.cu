@@ -1,25 +1,38 @@
 // softmax_sm103a.cu -- fused row softmax, the second workload of the lecture pages
 // ("06_triton_style.py", demo 3: one program reads a row once, keeps it on chip, and writes
 // exp(x - max) / sum once -- MN reads and MN writes instead of the 5MN + 2M / 3MN + 2M of
-// five separate kernels).  Bandwidth-bound: every variant reads each input once and writes
-// each output once, except rows too long for shared memory, which are read twice.
+// five separate kernels).  Bandwidth-bound: each input element is read once and each output
+// written once, except rows too long for on-chip staging, which are read twice.
 //
-//   * N <= 2048: one warp per row, the row held in registers (up to 16 float4 per lane).
-//   * N <= 51200: one 256-thread CTA per row, the row staged in shared memory.
-//   * longer rows: one CTA per row, an online pass for (max, sum) -- the running sum is
-//     rescaled whenever the running maximum grows -- then a second pass that writes.
-// Rows are walked by a persistent grid.  exp(-inf) = 0; a row holding a NaN, whose maximum
-// is +inf, or that is all -inf has no finite softmax and is written as NaN.
+// Rows whose base and leading dimensions are 16-byte aligned take the staged kernels: a
+// producer warp streams rows from HBM into a ring of shared-memory slots with bulk
+// asynchronous copies (cp.async.bulk, completion counted on an mbarrier per slot), so that
+// tens of kilobytes per SM are in flight with no registers held for them, while eight
+// compute warps reduce the staged rows and write the result with 16-byte streaming stores.
+//   * N <= 1024: a slot holds several rows; one compute warp per row.
+//   * N <= 12288: a slot holds one row (or a 16 KB piece of it); the eight warps share it.
+//   * longer rows: a cluster of up to 16 CTAs splits each row; every CTA reduces its slice
+//     to (max, sum), sends the pair to every CTA of the cluster through distributed shared
+//     memory (st.async, counted on the receiver's mbarrier), and rescales its slice by
+//     exp(max_slice - max_row) / sum_row.
+// Other layouts (and rows beyond 16 slices of 96 KB) take the plain kernels below: a warp per
+// row held in registers, a CTA per row staged in shared memory, or two passes over the row.
+// exp(-inf) = 0; a row holding a NaN, whose maximum is +inf, or that is all -inf has no
+// finite softmax and is written as NaN.
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "gemm_internal.h"
+#include "ptx_sm103a.cuh"
 
 namespace tct {
 
 namespace {
+
+__host__ __device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -217,16 +230,538 @@ __global__ void __launch_bounds__(kThreads) softmax_online_rows(const float *X, 
     }
 }
 
+
+// ---------------------------------------------------------------- staged kernels
+
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kStagedThreads = kComputeThreads + 32;  // + one producer warp
+constexpr int kMaxRing = 32;                          // ring slots (one mbarrier pair each)
+constexpr uint32_t kRingBytes = 32 * 1024;            // staging ring per CTA (at least two slots)
+constexpr uint32_t kMaxSmemBytes = 200 * 1024;        // dynamic shared memory opt-in of the staged kernels
+constexpr uint32_t kLongRingBytes = 96 * 1024;        // ring of the long-slice cluster kernel
+constexpr int kCtasPerSm = 2;
+constexpr uint32_t kHeaderBytes = 1024;               // barriers and reduction scratch
+constexpr uint32_t kChunkBytes = 16 * 1024;           // slot size of the CTA kernel for long slices
+constexpr int kMaxCluster = 16;
+
+enum SoftmaxWaitSite : unsigned {
+    SITE_SM_EMPTY = 16,  // producer waiting for a free slot
+    SITE_SM_FULL = 17,   // compute warps waiting for a slot's copy
+    SITE_SM_XCHG = 18,   // waiting for the cluster's (max, sum) pairs
+    SITE_SM_DRAIN = 19,  // producer waiting for its last copies before exit
+};
+
+struct StagedParams {
+    const float *X;
+    float *Y;
+    int64_t M, N, ldx, ldy;
+    int64_t slice;          // CTA kernel: columns per cluster rank (multiple of 4)
+    int64_t tiles;          // warp kernel: tiles of rows_per_tile rows; CTA kernel: rows
+    int32_t rows_per_tile;  // warp kernel
+    int32_t ring;           // ring slots in use (<= kMaxRing)
+    uint32_t slot_bytes;    // warp kernel: bytes per staged row; CTA kernel: bytes per slot
+    int32_t contiguous;     // warp kernel: rows adjacent (ldx == N, N % 4 == 0), one copy per tile
+    unsigned *err;
+    uint64_t timeout_ns;
+};
+
+struct StagedShared {
+    uint64_t full[kMaxRing];
+    uint64_t empty[kMaxRing];
+    uint64_t xchg[2];
+    float2 pairs[2][kMaxCluster];  // (slice max, slice sum) of every rank, two rows in turn
+    float redm[kComputeWarps];
+    float reds[kComputeWarps];
+    int redn[kComputeWarps];
+    int abort_flag;
+};
+static_assert(sizeof(StagedShared) <= kHeaderBytes, "staged kernel header");
+
+__device__ __forceinline__ void staged_timeout(StagedShared &sh, const StagedParams &p, unsigned site)
+{
+    atomicCAS(p.err, 0u, GEMM_ERR_DEVICE_TIMEOUT_CODE | (site << 8));
+    *reinterpret_cast<volatile int *>(&sh.abort_flag) = 1;
+    __threadfence_block();
+}
+
+// Bounded wait on an mbarrier phase; gives up at the time limit or as soon as another warp
+// of this CTA has given up.  On false the caller carries on without waiting again (the
+// results are then undefined and the error word says why), so that every warp still
+// reaches every barrier of the CTA and the kernel ends.
+template <bool kClusterScope>
+__device__ __forceinline__ bool staged_wait(uint32_t bar, uint32_t parity, StagedShared &sh, const StagedParams &p,
+                                            unsigned site)
+{
+    auto ready = [&]() { return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (ready()) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spins = 1;; ++spins) {
+        if (ready()) return true;
+        if ((spins & 15u) == 0u) {
+            if (*reinterpret_cast<volatile int *>(&sh.abort_flag)) return false;
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+                staged_timeout(sh, p, site);
+                return false;
+            }
+        }
+    }
+}
+
+// Producer epilogue: waits (bounded, even after an abort) until the copies into the last
+// min(issued, ring) slots have landed, so that no copy targets the CTA after it exits.
+__device__ __forceinline__ void staged_drain(StagedShared &sh, const StagedParams &p, uint32_t issued)
+{
+    const uint32_t first = issued > static_cast<uint32_t>(p.ring) ? issued - p.ring : 0u;
+    for (uint32_t j = first; j < issued; ++j) {
+        const uint32_t s = j % p.ring;
+        if (!mbar_wait(smem_u32(&sh.full[s]), (j / p.ring) & 1u, p.timeout_ns)) {
+            staged_timeout(sh, p, SITE_SM_DRAIN);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ void staged_init(StagedShared &sh, const StagedParams &p)
+{
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.ring; ++i) {
+            mbar_init(smem_u32(&sh.full[i]), 1);
+            mbar_init(smem_u32(&sh.empty[i]), kComputeWarps);
+        }
+        mbar_init(smem_u32(&sh.xchg[0]), 1);
+        mbar_init(smem_u32(&sh.xchg[1]), 1);
+        sh.abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ float max4(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
+__device__ __forceinline__ int nan4(float4 v) { return isnan(v.x) | isnan(v.y) | isnan(v.z) | isnan(v.w); }
+
+// Reductions over a team of TT threads (TT = 8, 16, 32 lanes of one warp, or 2-8 whole
+// warps).  Within a warp, xor-shuffles over aligned groups of min(TT, 32) lanes; across the
+// warps of a team, each warp publishes its partial in slot `warp` of `red` and, after the
+// team's named barrier (1 + team), every lane combines the partials in warp order.
+template <int TT>
+__device__ __forceinline__ float group_max(float v)
+{
+#pragma unroll
+    for (int o = (TT < 32 ? TT : 32) / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+template <int TT>
+__device__ __forceinline__ float group_sum(float v)
+{
+#pragma unroll
+    for (int o = (TT < 32 ? TT : 32) / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int TT>
+__device__ __forceinline__ int group_any(int v)
+{
+#pragma unroll
+    for (int o = (TT < 32 ? TT : 32) / 2; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int TT>
+__device__ __forceinline__ void team_reduce_max_any(float &m, int &nan, StagedShared &sh, int team, int warp, int lane)
+{
+    m = group_max<TT>(m);
+    nan = group_any<TT>(nan);
+    if constexpr (TT > 32) {
+        constexpr int T = TT / 32;
+        if (lane == 0) sh.redm[warp] = m, sh.redn[warp] = nan;
+        named_bar_sync(1 + team, TT);
+        m = sh.redm[team * T];
+        nan = sh.redn[team * T];
+#pragma unroll
+        for (int w = 1; w < T; ++w) m = fmaxf(m, sh.redm[team * T + w]), nan |= sh.redn[team * T + w];
+    }
+}
+
+template <int TT>
+__device__ __forceinline__ float team_reduce_sum(float v, StagedShared &sh, int team, int warp, int lane)
+{
+    v = group_sum<TT>(v);
+    if constexpr (TT > 32) {
+        constexpr int T = TT / 32;
+        if (lane == 0) sh.reds[warp] = v;
+        named_bar_sync(1 + team, TT);
+        v = sh.reds[team * T];
+#pragma unroll
+        for (int w = 1; w < T; ++w) v += sh.reds[team * T + w];
+    }
+    return v;
+}
+
+// Rows (or, in a cluster, row slices) of at most TT * VEC * 4 columns.  The 256 compute
+// threads form 256 / TT teams of TT threads; a ring slot holds a tile of rows_per_tile staged
+// rows (a multiple of the team count), and team k takes rows k, k + teams, ... of each tile.
+// A team reads its row from shared memory into registers once (VEC float4 per thread),
+// releases the slot after its last row of the tile, and computes and stores the softmax from
+// registers.  Every warp runs the same number of row iterations, so that shuffles always
+// have all 32 lanes; a team past the end of the tile runs on -inf fill and stores nothing.
+template <int TT, int VEC, bool kCluster>
+__global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_team(const StagedParams p)
+{
+    constexpr int kTeams = kComputeThreads / TT;
+    constexpr int kTeamsPerWarp = TT < 32 ? 32 / TT : 1;
+    static_assert(TT == 8 || TT == 16 || TT == 32 || TT == 64 || TT == 128 || TT == 256, "team size");
+    static_assert(!kCluster || TT == kComputeThreads, "a cluster row slice is reduced by the whole CTA");
+    extern __shared__ __align__(1024) unsigned char smem[];
+    StagedShared &sh = *reinterpret_cast<StagedShared *>(smem);
+    unsigned char *ring = smem + kHeaderBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    staged_init(sh, p);
+    if constexpr (kCluster) cluster_sync_all();  // every CTA's barriers exist before any st.async
+    const uint32_t rank = kCluster ? cluster_ctarank() : 0u;
+    const uint32_t csize = kCluster ? cluster_nctarank() : 1u;
+    const int64_t cid = kCluster ? static_cast<int64_t>(cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
+    const int64_t ncl = kCluster ? static_cast<int64_t>(cluster_count_x()) : static_cast<int64_t>(gridDim.x);
+    const int64_t c0 = static_cast<int64_t>(rank) * p.slice;
+    const int64_t len = p.N - c0 > 0 ? lmin(p.slice, p.N - c0) : int64_t(0);
+    const int64_t nb = len & ~int64_t(3);
+    const int n4 = static_cast<int>(nb >> 2);
+    const int64_t R = p.rows_per_tile;
+    const uint32_t tile_bytes = static_cast<uint32_t>(R) * p.slot_bytes;
+
+    if (warp == kComputeWarps) {  // producer warp
+        uint32_t q = 0;
+        for (int64_t t = cid; t < p.tiles; t += ncl, ++q) {
+            const uint32_t s = q % p.ring, ph = (q / p.ring) & 1u;
+            const int64_t r0 = t * R;
+            const int rows = static_cast<int>(lmin(R, p.M - r0));
+            bool ok = true;
+            if (lane == 0) ok = staged_wait<false>(smem_u32(&sh.empty[s]), ph ^ 1u, sh, p, SITE_SM_EMPTY);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            const uint32_t full = smem_u32(&sh.full[s]);
+            const uint32_t dst = smem_u32(ring) + s * tile_bytes;
+            if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(rows * nb * 4));
+            __syncwarp();
+            if (nb > 0) {
+                if (p.contiguous) {
+                    if (lane == 0) bulk_load(dst, p.X + r0 * p.ldx, static_cast<uint32_t>(rows * nb * 4), full);
+                } else {
+                    for (int r = lane; r < rows; r += 32)
+                        bulk_load(dst + r * p.slot_bytes, p.X + (r0 + r) * p.ldx + c0, static_cast<uint32_t>(nb * 4),
+                                  full);
+                }
+            }
+        }
+        if (lane == 0) staged_drain(sh, p, q);
+    } else {
+        const int team = threadIdx.x / TT;
+        const int tt = threadIdx.x % TT;                    // thread index within the team
+        const int warp_team0 = warp * kTeamsPerWarp;        // first team of this warp (TT <= 32)
+        const int lead = TT <= 32 ? warp_team0 : team;      // team whose rows pace this warp's loop
+        const bool has_tail = tt < len - nb;                // columns nb .. len-1 (at most 3): global loads
+        uint32_t q = 0, row_ctr = 0;
+        for (int64_t t = cid; t < p.tiles; t += ncl, ++q) {
+            const uint32_t s = q % p.ring, ph = (q / p.ring) & 1u;
+            const int64_t r0 = t * R;
+            const int rows = static_cast<int>(lmin(R, p.M - r0));
+            staged_wait<false>(smem_u32(&sh.full[s]), ph, sh, p, SITE_SM_FULL);
+            const unsigned char *tile = ring + static_cast<size_t>(s) * tile_bytes;
+            if (lead >= rows) {  // nothing for this warp in a short last tile
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
+            }
+            for (int base = 0; lead + base < rows; base += kTeams, ++row_ctr) {
+                const int r = team + base;
+                const bool live = r < rows;
+                const float *xg = p.X + (r0 + r) * p.ldx + c0;
+                float *yg = p.Y + (r0 + r) * p.ldy + c0;
+                const float4 *x4 = reinterpret_cast<const float4 *>(tile + static_cast<size_t>(r) * p.slot_bytes);
+                float4 v[VEC];
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) {
+                    const int i = tt + k * TT;
+                    v[k] = live && i < n4 ? x4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                }
+                if (lead + base + kTeams >= rows) {  // the warp's last rows of this tile are in registers
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
+                }
+                const float tv = live && has_tail ? xg[nb + tt] : -INFINITY;
+                float m = tv;
+                int nan = isnan(tv);
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) nan |= nan4(v[k]), m = fmaxf(m, max4(v[k]));
+                team_reduce_max_any<TT>(m, nan, sh, team, warp, lane);
+                const bool none = (m == -INFINITY);  // all -inf (or empty): every term is 0
+                float sum = 0.0f;
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) {
+                    float4 &e = v[k];
+                    e.x = none ? 0.0f : expf(e.x - m), e.y = none ? 0.0f : expf(e.y - m);
+                    e.z = none ? 0.0f : expf(e.z - m), e.w = none ? 0.0f : expf(e.w - m);
+                    sum += (e.x + e.y) + (e.z + e.w);
+                }
+                const float te = has_tail && !none ? expf(tv - m) : 0.0f;
+                sum = team_reduce_sum<TT>(sum + te, sh, team, warp, lane);
+
+                float f;
+                if constexpr (kCluster) {
+                    const uint32_t j = row_ctr & 1u;
+                    const uint32_t xbar = smem_u32(&sh.xchg[j]);
+                    if (tt == 0) {
+                        mbar_arrive_expect_tx(xbar, csize * 8u);
+                        const uint32_t slot = smem_u32(&sh.pairs[j][rank]);
+                        const float sv = nan ? NAN : sum;
+                        for (uint32_t c = 0; c < csize; ++c)
+                            st_async_f32x2(map_to_cta(slot, c), m, sv, map_to_cta(xbar, c));
+                    }
+                    staged_wait<true>(xbar, (row_ctr >> 1) & 1u, sh, p, SITE_SM_XCHG);
+                    float M = -INFINITY;
+                    for (uint32_t c = 0; c < csize; ++c) M = fmaxf(M, sh.pairs[j][c].x);
+                    float S = 0.0f;
+                    int bad = 0;
+                    for (uint32_t c = 0; c < csize; ++c) {
+                        const float2 pr = sh.pairs[j][c];
+                        bad |= isnan(pr.y);
+                        S += pr.x == -INFINITY ? 0.0f : pr.y * expf(pr.x - M);
+                    }
+                    f = (!bad && isfinite(M)) ? (none ? 0.0f : expf(m - M) / S) : NAN;
+                } else {
+                    f = (!nan && isfinite(m)) ? __frcp_rn(sum) : NAN;
+                }
+                if (live) {
+                    float4 *y4 = reinterpret_cast<float4 *>(yg);
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) {
+                        const int i = tt + k * TT;
+                        if (i < n4) __stcs(y4 + i, make_float4(v[k].x * f, v[k].y * f, v[k].z * f, v[k].w * f));
+                    }
+                    if (has_tail) __stcs(yg + nb + tt, te * f);
+                }
+            }
+        }
+    }
+    if constexpr (kCluster) cluster_sync_all();  // no CTA leaves while a peer may still write to it
+}
+
+// Longer rows: a CTA (kCluster false) or a cluster of CTAs (kCluster true) per row.  Rank r
+// of the cluster owns columns [r * slice, min(N, (r + 1) * slice)); its slice is staged as
+// ceil(bytes / slot_bytes) consecutive ring slots, all resident before the slice is reduced.
+template <bool kCluster>
+__global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_tma_cta(const StagedParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem[];
+    StagedShared &sh = *reinterpret_cast<StagedShared *>(smem);
+    unsigned char *ring = smem + kHeaderBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    staged_init(sh, p);
+    if constexpr (kCluster) cluster_sync_all();  // every CTA's barriers exist before any st.async
+    const uint32_t rank = kCluster ? cluster_ctarank() : 0u;
+    const uint32_t csize = kCluster ? cluster_nctarank() : 1u;
+    const int64_t cid = kCluster ? static_cast<int64_t>(cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
+    const int64_t ncl = kCluster ? static_cast<int64_t>(cluster_count_x()) : static_cast<int64_t>(gridDim.x);
+    const int64_t c0 = static_cast<int64_t>(rank) * p.slice;
+    const int64_t len = (p.N - c0 > 0 ? lmin(p.slice, p.N - c0) : int64_t(0));
+    const int64_t nb = len & ~int64_t(3);
+    const int64_t n4 = nb >> 2;
+    const uint32_t slot_f4 = p.slot_bytes / 16;
+    const uint32_t nch = static_cast<uint32_t>((n4 + slot_f4 - 1) / slot_f4);
+
+    if (warp == kComputeWarps) {  // producer (one lane)
+        if (lane == 0) {
+            uint32_t q = 0;
+            bool ok = true;
+            for (int64_t t = cid; ok && t < p.tiles; t += ncl) {
+                const float *src = p.X + t * p.ldx + c0;
+                for (uint32_t c = 0; c < nch; ++c, ++q) {
+                    const uint32_t s = q % p.ring, ph = (q / p.ring) & 1u;
+                    if (!staged_wait<false>(smem_u32(&sh.empty[s]), ph ^ 1u, sh, p, SITE_SM_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t f4 = static_cast<uint32_t>(lmin(slot_f4, n4 - int64_t(c) * slot_f4));
+                    const uint32_t full = smem_u32(&sh.full[s]);
+                    mbar_arrive_expect_tx(full, f4 * 16);
+                    bulk_load(smem_u32(ring) + s * p.slot_bytes, src + static_cast<int64_t>(c) * slot_f4 * 4, f4 * 16,
+                              full);
+                }
+            }
+            staged_drain(sh, p, q);
+        }
+    } else {
+        const int tid = threadIdx.x;
+        uint32_t q = 0, row_ctr = 0;
+        for (int64_t t = cid; t < p.tiles; t += ncl, ++row_ctr, q += nch) {
+            const float *xg = p.X + t * p.ldx + c0;
+            float *yg = p.Y + t * p.ldy + c0;
+            const bool has_tail = tid < len - nb;
+            const float tv = has_tail ? xg[nb + tid] : -INFINITY;
+            float m = tv;
+            int nan = isnan(tv);
+            for (uint32_t c = 0; c < nch; ++c) {
+                const uint32_t j = q + c, s = j % p.ring;
+                staged_wait<false>(smem_u32(&sh.full[s]), (j / p.ring) & 1u, sh, p, SITE_SM_FULL);
+                const float4 *x4 = reinterpret_cast<const float4 *>(ring + static_cast<size_t>(s) * p.slot_bytes);
+                const uint32_t f4 = static_cast<uint32_t>(lmin(slot_f4, n4 - int64_t(c) * slot_f4));
+#pragma unroll 4
+                for (uint32_t i = tid; i < f4; i += kComputeThreads) {
+                    const float4 v = x4[i];
+                    nan |= nan4(v);
+                    m = fmaxf(m, max4(v));
+                }
+            }
+            m = warp_max(m);
+            nan = warp_any(nan);
+            if (lane == 0) sh.redm[warp] = m, sh.redn[warp] = nan;
+            named_bar_sync(1, kComputeThreads);
+            m = sh.redm[0];
+            nan = sh.redn[0];
+#pragma unroll
+            for (int w = 1; w < kComputeWarps; ++w) m = fmaxf(m, sh.redm[w]), nan |= sh.redn[w];
+
+            // exp(x - m) back into the slots, and the slice sum; an all -inf slice sums to 0
+            const bool none = (m == -INFINITY);
+            float sum = 0.0f;
+            for (uint32_t c = 0; c < nch; ++c) {
+                const uint32_t s = (q + c) % p.ring;
+                float4 *x4 = reinterpret_cast<float4 *>(ring + static_cast<size_t>(s) * p.slot_bytes);
+                const uint32_t f4 = static_cast<uint32_t>(lmin(slot_f4, n4 - int64_t(c) * slot_f4));
+#pragma unroll 4
+                for (uint32_t i = tid; i < f4; i += kComputeThreads) {
+                    float4 v = x4[i];
+                    if (none) {
+                        v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        v.x = expf(v.x - m), v.y = expf(v.y - m), v.z = expf(v.z - m), v.w = expf(v.w - m);
+                    }
+                    x4[i] = v;
+                    sum += (v.x + v.y) + (v.z + v.w);
+                }
+            }
+            const float te = has_tail && !none ? expf(tv - m) : 0.0f;
+            sum = warp_sum(sum + te);
+            fence_proxy_async_smem();
+            if (lane == 0) sh.reds[warp] = sum;
+            named_bar_sync(1, kComputeThreads);
+            sum = sh.reds[0];
+#pragma unroll
+            for (int w = 1; w < kComputeWarps; ++w) sum += sh.reds[w];
+
+            float f;
+            if constexpr (kCluster) {
+                const uint32_t j = row_ctr & 1u;
+                const uint32_t xbar = smem_u32(&sh.xchg[j]);
+                if (tid == 0) {
+                    mbar_arrive_expect_tx(xbar, csize * 8u);
+                    const uint32_t slot = smem_u32(&sh.pairs[j][rank]);
+                    const float sv = nan ? NAN : sum;
+                    for (uint32_t r = 0; r < csize; ++r) st_async_f32x2(map_to_cta(slot, r), m, sv, map_to_cta(xbar, r));
+                }
+                staged_wait<true>(xbar, (row_ctr >> 1) & 1u, sh, p, SITE_SM_XCHG);
+                float M = -INFINITY;
+                for (uint32_t r = 0; r < csize; ++r) M = fmaxf(M, sh.pairs[j][r].x);
+                float S = 0.0f;
+                int bad = 0;
+                for (uint32_t r = 0; r < csize; ++r) {
+                    const float2 pr = sh.pairs[j][r];
+                    bad |= isnan(pr.y);
+                    S += pr.x == -INFINITY ? 0.0f : pr.y * expf(pr.x - M);
+                }
+                f = (!bad && isfinite(M)) ? (none ? 0.0f : expf(m - M) / S) : NAN;
+            } else {
+                f = (!nan && isfinite(m)) ? 1.0f / sum : NAN;
+            }
+
+            float4 *y4 = reinterpret_cast<float4 *>(yg);
+            for (uint32_t c = 0; c < nch; ++c) {
+                const uint32_t s = (q + c) % p.ring;
+                const float4 *x4 = reinterpret_cast<const float4 *>(ring + static_cast<size_t>(s) * p.slot_bytes);
+                const uint32_t f4 = static_cast<uint32_t>(lmin(slot_f4, n4 - int64_t(c) * slot_f4));
+                float4 *yc = y4 + static_cast<int64_t>(c) * slot_f4;
+#pragma unroll 4
+                for (uint32_t i = tid; i < f4; i += kComputeThreads) {
+                    float4 v = x4[i];
+                    v.x *= f, v.y *= f, v.z *= f, v.w *= f;
+                    __stcs(yc + i, v);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
+            }
+            if (has_tail) __stcs(yg + nb + tid, te * f);
+        }
+    }
+    if constexpr (kCluster) cluster_sync_all();  // no CTA leaves while a peer may still write to it
+}
+
 }  // namespace
 
-cudaError_t launch_softmax_rows(const float *X, float *Y, int64_t M, int64_t N, int64_t ldx, int64_t ldy, int num_sms,
-                                cudaStream_t stream)
+namespace {
+
+// Per-device launch state: the staged kernels' shared-memory opt-in, and how many clusters
+// of each size fit on the device at once.
+struct SoftmaxDevState {
+    bool smem_set = false;
+    int clusters[2][kMaxCluster + 1] = {};  // [team, long][size]: 0 = not queried, -1 = does not fit
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_sm_mu;
+SoftmaxDevState g_sm_dev[kMaxDevices];
+
+using StagedKernel = void (*)(StagedParams);
+
+// Team kernels by row length: (threads per team, float4 per thread) covering up to
+// TT * VEC * 4 columns.  Teams grow with the row so that a tile (one row per team) stays
+// near 16 KB: a shallow ring of small tiles streams faster than a deep one.
+struct TeamVariant {
+    int64_t max_cols;
+    int team_threads;
+    StagedKernel kernel;
+};
+const TeamVariant kTeamVariants[] = {
+    {32, 8, softmax_team<8, 1, false>},       {64, 8, softmax_team<8, 2, false>},
+    {128, 8, softmax_team<8, 4, false>},      {256, 16, softmax_team<16, 4, false>},
+    {512, 32, softmax_team<32, 4, false>},    {1024, 64, softmax_team<64, 4, false>},
+    {2048, 128, softmax_team<128, 4, false>}, {4096, 256, softmax_team<256, 4, false>},
+    {8192, 256, softmax_team<256, 8, false>},
+};
+constexpr int64_t kTeamMaxCols = 8192;  // also the slice length of the cluster team kernel
+StagedKernel const kClusterTeam = softmax_team<256, 8, true>;
+StagedKernel const kClusterLong = softmax_tma_cta<true>;
+
+cudaError_t set_staged_smem()
 {
-    if (M <= 0 || N <= 0) return cudaSuccess;
-    const int vec = (reinterpret_cast<uintptr_t>(X) % 16 == 0 && reinterpret_cast<uintptr_t>(Y) % 16 == 0 &&
-                     ldx % 4 == 0 && ldy % 4 == 0)
-                        ? 1
-                        : 0;
+    const int bytes = static_cast<int>(kMaxSmemBytes);
+    cudaError_t e = cudaSuccess;
+    for (const TeamVariant &v : kTeamVariants)
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(v.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    for (StagedKernel k : {kClusterTeam, kClusterLong}) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    }
+    return e;
+}
+
+// Clusters of `csize` CTAs (smem bytes each) that are co-resident on the current device.
+cudaError_t max_clusters(StagedKernel kernel, int csize, size_t smem, int *out)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(csize) * 64u);
+    cfg.blockDim = dim3(kStagedThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(out, kernel, &cfg);
+}
+
+cudaError_t launch_plain(const float *X, float *Y, int64_t M, int64_t N, int64_t ldx, int64_t ldy, int num_sms, int vec,
+                         cudaStream_t stream)
+{
     if (N <= static_cast<int64_t>(kWarpMaxVec) * 128) {
         const int64_t rows_per_block = kWarps;
         int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
@@ -264,6 +799,118 @@ cudaError_t launch_softmax_rows(const float *X, float *Y, int64_t M, int64_t N, 
     if (blocks > cap) blocks = cap;
     softmax_online_rows<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(X, Y, M, N, ldx, ldy);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_softmax_rows(const float *X, float *Y, int64_t M, int64_t N, int64_t ldx, int64_t ldy, int num_sms,
+                                unsigned *err, uint64_t timeout_ns, cudaStream_t stream)
+{
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    const int vec = (reinterpret_cast<uintptr_t>(X) % 16 == 0 && reinterpret_cast<uintptr_t>(Y) % 16 == 0 &&
+                     ldx % 4 == 0 && ldy % 4 == 0)
+                        ? 1
+                        : 0;
+    // Rows split over at most kMaxCluster CTAs, each slice within one ring.
+    const int64_t max_staged = static_cast<int64_t>(kMaxCluster) * (kLongRingBytes / 4);
+    if (!vec || N > max_staged) return launch_plain(X, Y, M, N, ldx, ldy, num_sms, vec, stream);
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_sm_mu);
+    SoftmaxDevState &ds = g_sm_dev[dev];
+    if (!ds.smem_set) {
+        e = set_staged_smem();
+        if (e != cudaSuccess) return e;
+        ds.smem_set = true;
+    }
+
+    StagedParams p = {};
+    p.X = X, p.Y = Y, p.M = M, p.N = N, p.ldx = ldx, p.ldy = ldy;
+    p.err = err, p.timeout_ns = timeout_ns;
+    // Ring slots hold tiles of R staged rows (slices), R a multiple of the teams per CTA,
+    // about 16 KB per tile (at most 128 rows, at least one row per team).
+    auto tile_rows = [](uint32_t slot_bytes, int teams) {
+        int64_t R = 16384 / slot_bytes;
+        R = R > 128 ? 128 : R;
+        R = R / teams * teams;
+        return R < teams ? int64_t(teams) : R;
+    };
+    // Slots in the ring: as many tiles as kRingBytes holds, but never fewer than two.
+    auto ring_slots = [](uint32_t tile_bytes) {
+        const int64_t n = kRingBytes / tile_bytes;
+        return static_cast<int32_t>(n < 2 ? 2 : (n > kMaxRing ? kMaxRing : n));
+    };
+    if (N <= kTeamMaxCols) {
+        const TeamVariant *v = kTeamVariants;
+        while (v->max_cols < N) ++v;
+        p.slice = N;
+        p.slot_bytes = static_cast<uint32_t>(((N + 3) & ~int64_t(3)) * 4);
+        p.rows_per_tile = static_cast<int32_t>(tile_rows(p.slot_bytes, kComputeThreads / v->team_threads));
+        const uint32_t tile_bytes = static_cast<uint32_t>(p.rows_per_tile) * p.slot_bytes;
+        p.ring = ring_slots(tile_bytes);
+        p.contiguous = (ldx == N && N % 4 == 0) ? 1 : 0;
+        p.tiles = (M + p.rows_per_tile - 1) / p.rows_per_tile;
+        const size_t smem = kHeaderBytes + static_cast<size_t>(p.ring) * tile_bytes;
+        if (smem > kMaxSmemBytes) return cudaErrorInvalidConfiguration;
+        const int64_t grid = lmin(p.tiles, static_cast<int64_t>(num_sms) * kCtasPerSm);
+        v->kernel<<<static_cast<unsigned>(grid), kStagedThreads, smem, stream>>>(p);
+        return cudaGetLastError();
+    }
+
+    // A cluster per row: slices of at most kTeamMaxCols columns (registers), or for longer
+    // rows up to one ring of 16 KB slots (shared memory).
+    const bool team = N <= static_cast<int64_t>(kMaxCluster) * kTeamMaxCols;
+    int csize = static_cast<int>((N + kTeamMaxCols - 1) / kTeamMaxCols);
+    if (csize > kMaxCluster) csize = kMaxCluster;
+    p.slice = (((N + csize - 1) / csize) + 3) & ~int64_t(3);
+    StagedKernel kernel;
+    size_t smem;
+    if (team) {
+        kernel = kClusterTeam;
+        p.slot_bytes = static_cast<uint32_t>(p.slice * 4);
+        p.rows_per_tile = static_cast<int32_t>(tile_rows(p.slot_bytes, 1));
+        const uint32_t tile_bytes = static_cast<uint32_t>(p.rows_per_tile) * p.slot_bytes;
+        p.ring = ring_slots(tile_bytes);
+        p.tiles = (M + p.rows_per_tile - 1) / p.rows_per_tile;
+        smem = kHeaderBytes + static_cast<size_t>(p.ring) * tile_bytes;
+    } else {
+        kernel = kClusterLong;
+        p.slot_bytes = kChunkBytes;
+        p.ring = static_cast<int32_t>(kLongRingBytes / kChunkBytes);  // holds a whole slice (<= 96 KB)
+        p.tiles = M;
+        smem = kHeaderBytes + static_cast<size_t>(p.ring) * p.slot_bytes;
+    }
+    if (smem > kMaxSmemBytes) return cudaErrorInvalidConfiguration;
+    int &fit = ds.clusters[team ? 0 : 1][csize];
+    if (fit == 0) {
+        int n = 0;
+        // queried at the largest shared-memory size this mode uses, so the count holds for all
+        const size_t fit_smem = team ? kHeaderBytes + 2 * (kTeamMaxCols * 4) : kHeaderBytes + kLongRingBytes;
+        e = max_clusters(kernel, csize, fit_smem, &n);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        fit = n > 0 ? n : -1;
+    }
+    if (fit < 0) return launch_plain(X, Y, M, N, ldx, ldy, num_sms, vec, stream);
+    const int64_t clusters = lmin(p.tiles, fit);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * csize));
+    cfg.blockDim = dim3(kStagedThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace tct

@@ -67,11 +67,16 @@ def _run(x, inplace=False):
     return out.cpu().numpy()
 
 
-# (M, N, seed): warp kernel (N = 1 .. 2048, each VEC width and ragged tails), shared-memory
-# kernel (2049 .. 51200), online kernel (51201 and longer).
+# (M, N, seed) for 16-byte-aligned rows.  Up to 8192 columns a team of 1, 2, 4 or 8 warps
+# holds a row in registers (several rows staged per ring slot); up to 16 * 8192 columns a
+# cluster of ceil(N / 8192) CTAs splits each row the same way; up to 16 * 24576 columns a
+# cluster of 16 CTAs stages each slice in 16 KB shared-memory slots; beyond that the
+# two-pass kernel.  The tall shapes wrap every CTA's slot ring several times.
 SHAPES = [(1, 1, 10), (7, 1, 11), (33, 5, 12), (300, 37, 13), (129, 128, 14), (64, 129, 15), (257, 256, 16),
-          (100, 511, 17), (65, 1000, 18), (40, 1024, 19), (31, 2047, 20), (17, 2048, 21), (9, 2049, 22),
-          (20, 3000, 23), (5, 12345, 24), (3, 51199, 25), (2, 51200, 26), (2, 51201, 27), (3, 200003, 28)]
+          (100, 511, 17), (65, 1000, 18), (40, 1024, 19), (80000, 100, 40), (31, 1025, 20), (17, 2048, 21),
+          (9, 2049, 22), (20, 3000, 23), (5, 4096, 24), (5, 4097, 25), (3, 8192, 26), (8000, 2000, 41),
+          (3, 8193, 27), (2, 51200, 28), (2, 51201, 29), (1000, 30000, 42), (2, 131072, 43), (2, 131073, 44),
+          (2, 200003, 30), (2, 393216, 31), (2, 393217, 32)]
 
 
 @pytest.mark.parametrize("M,N,seed", SHAPES)
@@ -95,13 +100,14 @@ def test_wide_range_rows(N):
     _check(x, _run(x))
 
 
-@pytest.mark.parametrize("N", [1000, 4000, 60000])
+@pytest.mark.parametrize("N", [1000, 4000, 30000, 60000])
 def test_padded_and_unaligned(N):
-    """Rows with ld > N, and a base 4 bytes off 16-byte alignment (the scalar load path)."""
+    """Rows with ld > N: 16-byte-aligned padded rows (staged kernels), and rows whose ld or base
+    is not a multiple of 16 bytes (plain kernels)."""
     M = 37
     rng = np.random.default_rng(N + 1)
     x = inputs.normal_f32(rng, M, N)
-    for ld, off in [(N + 3, 0), (N + 8, 4), (N + 1, 1)]:
+    for ld, off in [(N + 3, 0), (N + 8, 4), (N + 1, 1), (N + 4, 0)]:
         buf = torch.full((M * ld + 8,), float("nan"), device="cuda")
         src = buf[off:off + M * ld].view(M, ld)
         src[:, :N] = torch.from_numpy(x).cuda()
