@@ -545,42 +545,55 @@ __global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_team(const
     if constexpr (kCluster) cluster_sync_all();  // no CTA leaves while a peer may still write to it
 }
 
-// Longer rows: a CTA (kCluster false) or a cluster of CTAs (kCluster true) per row.  Rank r
-// of the cluster owns columns [r * slice, min(N, (r + 1) * slice)); its slice is staged as
-// ceil(bytes / slot_bytes) consecutive ring slots, all resident before the slice is reduced.
-template <bool kCluster>
-__global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_tma_cta(const StagedParams p)
+// Rows longer than 16 * 8192 columns: a cluster of 16 CTAs per row, rank r owning columns
+// [r * slice, min(N, (r + 1) * slice)), streamed through a ring of 16 KB slots.  When the
+// slice fits in the ring (resident mode) it is read once: the (max, sum) pass writes
+// exp(x - max) back into the slots and the output pass scales them.  Otherwise (streaming
+// mode) the slice is read twice: an online pass keeps a running (max, sum) per thread,
+// rescaling the sum whenever its maximum grows, and the output pass recomputes
+// exp(x - row max) from the second read.
+__global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_long_slices(const StagedParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem[];
     StagedShared &sh = *reinterpret_cast<StagedShared *>(smem);
     unsigned char *ring = smem + kHeaderBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     staged_init(sh, p);
-    if constexpr (kCluster) cluster_sync_all();  // every CTA's barriers exist before any st.async
-    const uint32_t rank = kCluster ? cluster_ctarank() : 0u;
-    const uint32_t csize = kCluster ? cluster_nctarank() : 1u;
-    const int64_t cid = kCluster ? static_cast<int64_t>(cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
-    const int64_t ncl = kCluster ? static_cast<int64_t>(cluster_count_x()) : static_cast<int64_t>(gridDim.x);
+    cluster_sync_all();  // every CTA's barriers exist before any st.async
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t csize = cluster_nctarank();
+    const int64_t cid = cluster_id_x();
+    const int64_t ncl = cluster_count_x();
     const int64_t c0 = static_cast<int64_t>(rank) * p.slice;
-    const int64_t len = (p.N - c0 > 0 ? lmin(p.slice, p.N - c0) : int64_t(0));
+    const int64_t len = p.N - c0 > 0 ? lmin(p.slice, p.N - c0) : int64_t(0);
     const int64_t nb = len & ~int64_t(3);
     const int64_t n4 = nb >> 2;
     const uint32_t slot_f4 = p.slot_bytes / 16;
     const uint32_t nch = static_cast<uint32_t>((n4 + slot_f4 - 1) / slot_f4);
+    const bool resident = nch <= static_cast<uint32_t>(p.ring);
+    const uint32_t loads_per_row = resident ? nch : 2 * nch;
+    auto chunk_f4 = [&](uint32_t c) { return static_cast<uint32_t>(lmin(slot_f4, n4 - int64_t(c) * slot_f4)); };
+    auto slot_ptr = [&](uint32_t j) { return ring + static_cast<size_t>(j % p.ring) * p.slot_bytes; };
+    auto wait_full = [&](uint32_t j) { staged_wait<false>(smem_u32(&sh.full[j % p.ring]), (j / p.ring) & 1u, sh, p, SITE_SM_FULL); };
+    auto release = [&](uint32_t j) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.empty[j % p.ring]));
+    };
 
-    if (warp == kComputeWarps) {  // producer (one lane)
+    if (warp == kComputeWarps) {  // producer (one lane): the slice once, or twice when streaming
         if (lane == 0) {
             uint32_t q = 0;
             bool ok = true;
             for (int64_t t = cid; ok && t < p.tiles; t += ncl) {
                 const float *src = p.X + t * p.ldx + c0;
-                for (uint32_t c = 0; c < nch; ++c, ++q) {
+                for (uint32_t k = 0; k < loads_per_row; ++k, ++q) {
+                    const uint32_t c = k < nch ? k : k - nch;
                     const uint32_t s = q % p.ring, ph = (q / p.ring) & 1u;
                     if (!staged_wait<false>(smem_u32(&sh.empty[s]), ph ^ 1u, sh, p, SITE_SM_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t f4 = static_cast<uint32_t>(lmin(slot_f4, n4 - int64_t(c) * slot_f4));
+                    const uint32_t f4 = chunk_f4(c);
                     const uint32_t full = smem_u32(&sh.full[s]);
                     mbar_arrive_expect_tx(full, f4 * 16);
                     bulk_load(smem_u32(ring) + s * p.slot_bytes, src + static_cast<int64_t>(c) * slot_f4 * 4, f4 * 16,
@@ -592,106 +605,130 @@ __global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_tma_cta(co
     } else {
         const int tid = threadIdx.x;
         uint32_t q = 0, row_ctr = 0;
-        for (int64_t t = cid; t < p.tiles; t += ncl, ++row_ctr, q += nch) {
+        for (int64_t t = cid; t < p.tiles; t += ncl, ++row_ctr, q += loads_per_row) {
             const float *xg = p.X + t * p.ldx + c0;
             float *yg = p.Y + t * p.ldy + c0;
             const bool has_tail = tid < len - nb;
             const float tv = has_tail ? xg[nb + tid] : -INFINITY;
-            float m = tv;
+            float m = tv, sum = 0.0f;
             int nan = isnan(tv);
-            for (uint32_t c = 0; c < nch; ++c) {
-                const uint32_t j = q + c, s = j % p.ring;
-                staged_wait<false>(smem_u32(&sh.full[s]), (j / p.ring) & 1u, sh, p, SITE_SM_FULL);
-                const float4 *x4 = reinterpret_cast<const float4 *>(ring + static_cast<size_t>(s) * p.slot_bytes);
-                const uint32_t f4 = static_cast<uint32_t>(lmin(slot_f4, n4 - int64_t(c) * slot_f4));
+            if (resident) {
+                for (uint32_t c = 0; c < nch; ++c) {
+                    wait_full(q + c);
+                    const float4 *x4 = reinterpret_cast<const float4 *>(slot_ptr(q + c));
+                    const uint32_t f4 = chunk_f4(c);
 #pragma unroll 4
-                for (uint32_t i = tid; i < f4; i += kComputeThreads) {
-                    const float4 v = x4[i];
-                    nan |= nan4(v);
-                    m = fmaxf(m, max4(v));
-                }
-            }
-            m = warp_max(m);
-            nan = warp_any(nan);
-            if (lane == 0) sh.redm[warp] = m, sh.redn[warp] = nan;
-            named_bar_sync(1, kComputeThreads);
-            m = sh.redm[0];
-            nan = sh.redn[0];
-#pragma unroll
-            for (int w = 1; w < kComputeWarps; ++w) m = fmaxf(m, sh.redm[w]), nan |= sh.redn[w];
-
-            // exp(x - m) back into the slots, and the slice sum; an all -inf slice sums to 0
-            const bool none = (m == -INFINITY);
-            float sum = 0.0f;
-            for (uint32_t c = 0; c < nch; ++c) {
-                const uint32_t s = (q + c) % p.ring;
-                float4 *x4 = reinterpret_cast<float4 *>(ring + static_cast<size_t>(s) * p.slot_bytes);
-                const uint32_t f4 = static_cast<uint32_t>(lmin(slot_f4, n4 - int64_t(c) * slot_f4));
-#pragma unroll 4
-                for (uint32_t i = tid; i < f4; i += kComputeThreads) {
-                    float4 v = x4[i];
-                    if (none) {
-                        v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    } else {
-                        v.x = expf(v.x - m), v.y = expf(v.y - m), v.z = expf(v.z - m), v.w = expf(v.w - m);
+                    for (uint32_t i = tid; i < f4; i += kComputeThreads) {
+                        const float4 v = x4[i];
+                        nan |= nan4(v);
+                        m = fmaxf(m, max4(v));
                     }
-                    x4[i] = v;
-                    sum += (v.x + v.y) + (v.z + v.w);
                 }
-            }
-            const float te = has_tail && !none ? expf(tv - m) : 0.0f;
-            sum = warp_sum(sum + te);
-            fence_proxy_async_smem();
-            if (lane == 0) sh.reds[warp] = sum;
-            named_bar_sync(1, kComputeThreads);
-            sum = sh.reds[0];
-#pragma unroll
-            for (int w = 1; w < kComputeWarps; ++w) sum += sh.reds[w];
-
-            float f;
-            if constexpr (kCluster) {
-                const uint32_t j = row_ctr & 1u;
-                const uint32_t xbar = smem_u32(&sh.xchg[j]);
-                if (tid == 0) {
-                    mbar_arrive_expect_tx(xbar, csize * 8u);
-                    const uint32_t slot = smem_u32(&sh.pairs[j][rank]);
-                    const float sv = nan ? NAN : sum;
-                    for (uint32_t r = 0; r < csize; ++r) st_async_f32x2(map_to_cta(slot, r), m, sv, map_to_cta(xbar, r));
+                team_reduce_max_any<kComputeThreads>(m, nan, sh, 0, warp, lane);
+                const bool none = (m == -INFINITY);  // all -inf (or empty): every term is 0
+                for (uint32_t c = 0; c < nch; ++c) {
+                    float4 *x4 = reinterpret_cast<float4 *>(slot_ptr(q + c));
+                    const uint32_t f4 = chunk_f4(c);
+#pragma unroll 4
+                    for (uint32_t i = tid; i < f4; i += kComputeThreads) {
+                        float4 v = x4[i];
+                        if (none) {
+                            v = make_float4(0.f, 0.f, 0.f, 0.f);
+                        } else {
+                            v.x = expf(v.x - m), v.y = expf(v.y - m), v.z = expf(v.z - m), v.w = expf(v.w - m);
+                        }
+                        x4[i] = v;
+                        sum += (v.x + v.y) + (v.z + v.w);
+                    }
                 }
-                staged_wait<true>(xbar, (row_ctr >> 1) & 1u, sh, p, SITE_SM_XCHG);
-                float M = -INFINITY;
-                for (uint32_t r = 0; r < csize; ++r) M = fmaxf(M, sh.pairs[j][r].x);
-                float S = 0.0f;
-                int bad = 0;
-                for (uint32_t r = 0; r < csize; ++r) {
-                    const float2 pr = sh.pairs[j][r];
-                    bad |= isnan(pr.y);
-                    S += pr.x == -INFINITY ? 0.0f : pr.y * expf(pr.x - M);
-                }
-                f = (!bad && isfinite(M)) ? (none ? 0.0f : expf(m - M) / S) : NAN;
+                fence_proxy_async_smem();  // the slots are refilled by bulk copies after release
+                if (has_tail && !none) sum += expf(tv - m);
+                sum = team_reduce_sum<kComputeThreads>(sum, sh, 0, warp, lane);
             } else {
-                f = (!nan && isfinite(m)) ? 1.0f / sum : NAN;
+                // online pass: running (m, sum) per thread, sum relative to m
+                if (m == -INFINITY) m = -INFINITY, sum = 0.0f;
+                else sum = 1.0f;  // the tail element itself
+                for (uint32_t c = 0; c < nch; ++c) {
+                    wait_full(q + c);
+                    const float4 *x4 = reinterpret_cast<const float4 *>(slot_ptr(q + c));
+                    const uint32_t f4 = chunk_f4(c);
+#pragma unroll 2
+                    for (uint32_t i = tid; i < f4; i += kComputeThreads) {
+                        const float4 v = x4[i];
+                        nan |= nan4(v);
+                        const float mv = max4(v);
+                        if (mv > m) {
+                            sum = m == -INFINITY ? 0.0f : sum * expf(m - mv);
+                            m = mv;
+                        }
+                        if (m != -INFINITY) sum += (expf(v.x - m) + expf(v.y - m)) + (expf(v.z - m) + expf(v.w - m));
+                    }
+                    release(q + c);
+                }
+                float mt = m;
+                team_reduce_max_any<kComputeThreads>(m, nan, sh, 0, warp, lane);
+                sum = mt == -INFINITY ? 0.0f : sum * expf(mt - m);  // rescale to the slice maximum
+                sum = team_reduce_sum<kComputeThreads>(sum, sh, 0, warp, lane);
             }
+            const bool none = (m == -INFINITY);
+
+            // (max, sum) of every slice of the row, from every rank of the cluster
+            const uint32_t j = row_ctr & 1u;
+            const uint32_t xbar = smem_u32(&sh.xchg[j]);
+            if (tid == 0) {
+                mbar_arrive_expect_tx(xbar, csize * 8u);
+                const uint32_t slot = smem_u32(&sh.pairs[j][rank]);
+                const float sv = nan ? NAN : sum;
+                for (uint32_t r = 0; r < csize; ++r) st_async_f32x2(map_to_cta(slot, r), m, sv, map_to_cta(xbar, r));
+            }
+            staged_wait<true>(xbar, (row_ctr >> 1) & 1u, sh, p, SITE_SM_XCHG);
+            float M = -INFINITY;
+            for (uint32_t r = 0; r < csize; ++r) M = fmaxf(M, sh.pairs[j][r].x);
+            float S = 0.0f;
+            int bad = 0;
+            for (uint32_t r = 0; r < csize; ++r) {
+                const float2 pr = sh.pairs[j][r];
+                bad |= isnan(pr.y);
+                S += pr.x == -INFINITY ? 0.0f : pr.y * expf(pr.x - M);
+            }
+            const bool ok = !bad && isfinite(M);
 
             float4 *y4 = reinterpret_cast<float4 *>(yg);
-            for (uint32_t c = 0; c < nch; ++c) {
-                const uint32_t s = (q + c) % p.ring;
-                const float4 *x4 = reinterpret_cast<const float4 *>(ring + static_cast<size_t>(s) * p.slot_bytes);
-                const uint32_t f4 = static_cast<uint32_t>(lmin(slot_f4, n4 - int64_t(c) * slot_f4));
-                float4 *yc = y4 + static_cast<int64_t>(c) * slot_f4;
+            if (resident) {
+                const float f = ok ? (none ? 0.0f : expf(m - M) / S) : NAN;
+                for (uint32_t c = 0; c < nch; ++c) {
+                    const float4 *x4 = reinterpret_cast<const float4 *>(slot_ptr(q + c));
+                    const uint32_t f4 = chunk_f4(c);
+                    float4 *yc = y4 + static_cast<int64_t>(c) * slot_f4;
 #pragma unroll 4
-                for (uint32_t i = tid; i < f4; i += kComputeThreads) {
-                    float4 v = x4[i];
-                    v.x *= f, v.y *= f, v.z *= f, v.w *= f;
-                    __stcs(yc + i, v);
+                    for (uint32_t i = tid; i < f4; i += kComputeThreads) {
+                        float4 v = x4[i];
+                        v.x *= f, v.y *= f, v.z *= f, v.w *= f;
+                        __stcs(yc + i, v);
+                    }
+                    release(q + c);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
+                if (has_tail) __stcs(yg + nb + tid, (none ? 0.0f : expf(tv - m)) * f);
+            } else {
+                const float g = ok ? __frcp_rn(S) : NAN;
+                for (uint32_t c = 0; c < nch; ++c) {
+                    wait_full(q + nch + c);
+                    const float4 *x4 = reinterpret_cast<const float4 *>(slot_ptr(q + nch + c));
+                    const uint32_t f4 = chunk_f4(c);
+                    float4 *yc = y4 + static_cast<int64_t>(c) * slot_f4;
+#pragma unroll 2
+                    for (uint32_t i = tid; i < f4; i += kComputeThreads) {
+                        const float4 v = x4[i];
+                        __stcs(yc + i, make_float4(expf(v.x - M) * g, expf(v.y - M) * g, expf(v.z - M) * g,
+                                                   expf(v.w - M) * g));
+                    }
+                    release(q + nch + c);
+                }
+                if (has_tail) __stcs(yg + nb + tid, expf(tv - M) * g);
             }
-            if (has_tail) __stcs(yg + nb + tid, te * f);
         }
     }
-    if constexpr (kCluster) cluster_sync_all();  // no CTA leaves while a peer may still write to it
+    cluster_sync_all();  // no CTA leaves while a peer may still write to it
 }
 
 }  // namespace
@@ -727,7 +764,7 @@ const TeamVariant kTeamVariants[] = {
 };
 constexpr int64_t kTeamMaxCols = 8192;  // also the slice length of the cluster team kernel
 StagedKernel const kClusterTeam = softmax_team<256, 8, true>;
-StagedKernel const kClusterLong = softmax_tma_cta<true>;
+StagedKernel const kClusterLong = softmax_long_slices;
 
 cudaError_t set_staged_smem()
 {
@@ -811,9 +848,7 @@ cudaError_t launch_softmax_rows(const float *X, float *Y, int64_t M, int64_t N, 
                      ldx % 4 == 0 && ldy % 4 == 0)
                         ? 1
                         : 0;
-    // Rows split over at most kMaxCluster CTAs, each slice within one ring.
-    const int64_t max_staged = static_cast<int64_t>(kMaxCluster) * (kLongRingBytes / 4);
-    if (!vec || N > max_staged) return launch_plain(X, Y, M, N, ldx, ldy, num_sms, vec, stream);
+    if (!vec) return launch_plain(X, Y, M, N, ldx, ldy, num_sms, vec, stream);
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -879,7 +914,7 @@ cudaError_t launch_softmax_rows(const float *X, float *Y, int64_t M, int64_t N, 
     } else {
         kernel = kClusterLong;
         p.slot_bytes = kChunkBytes;
-        p.ring = static_cast<int32_t>(kLongRingBytes / kChunkBytes);  // holds a whole slice (<= 96 KB)
+        p.ring = static_cast<int32_t>(kLongRingBytes / kChunkBytes);  // a slice up to 96 KB is read once
         p.tiles = M;
         smem = kHeaderBytes + static_cast<size_t>(p.ring) * p.slot_bytes;
     }

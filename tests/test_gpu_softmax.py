@@ -1,19 +1,23 @@
 """Parity of the fused row softmax (softmax_rows_f32) with the oracle.
 
 The workload is the one of "06_triton_style.py" demo 3: N(0,1) rows, softmax along each
-row.  Shapes cover the three kernels the library picks by row length -- a warp per row
-(N <= 2048), a CTA per row staged in shared memory (N <= 51200), and the two-pass online
-kernel beyond -- each at its boundaries, plus ragged lengths, padded and unaligned rows,
+row.  Rows whose base and leading dimension are multiples of 16 bytes take the staged
+kernels (a team of threads per row up to 8192 columns, a cluster of CTAs per row beyond,
+reading long slices twice past 16 x 24576 columns); other rows take the plain kernels
+(a warp per row up to 2048 columns, a CTA per row in shared memory up to 51200, two passes
+beyond).  Shapes sit on each boundary, with ragged lengths, padded and unaligned rows,
 in-place use, special values and empty shapes.
 
 Error bound (per element, relative to the exact softmax r_j, with u = 2^-24):
   x_j - max rounds once (u |d_j| after exp), expf is within 2 ulp (4u), every term of the
-  row sum carries the same, a summation chain of n terms adds n u, the online kernel's
-  rescales add at most 5u each plus u |d|max in total, the division u, the oracle's final
-  rounding u:  |y_j - r_j| <= u (16 + |d_j| + 2 |d|max + 7 n) r_j,
-  where n = ceil(N / 32) when a warp holds the row, ceil(N / 256) otherwise, plus 8 levels
-  of tree reduction.  A dropped or doubled term of weight w moves every output by w, far
-  above this bound at the tested lengths.
+  row sum carries the same, a summation chain of n terms adds n u, online rescales add at
+  most 5u each plus u |d|max in total, the reciprocal or division u, the final product u,
+  the oracle's rounding u:  |y_j - r_j| <= u (16 + |d_j| + 2 |d|max + 7 n) r_j,
+  where n bounds the longest chain of additions: 64 + ceil(N / 4096) on the staged path
+  (at most 32 terms per thread in a team, N / 4096 per thread in a 16-CTA cluster, plus
+  the reduction trees), 64 + ceil(N / 256) on the plain path.  Rows of 0 and -inf entries
+  have an exact softmax (1/k on the k zeros) and are compared bit for bit, so that a
+  dropped or repeated piece of a long row cannot hide inside the bound.
 """
 import math
 
@@ -38,12 +42,15 @@ def _gpu(tct_lib):
     yield
 
 
-def _chain(N):
-    return math.ceil(N / 32) if N <= 2048 else math.ceil(N / 256)
+def _chain(N, staged):
+    return 64 + (math.ceil(N / 4096) if staged else math.ceil(N / 256))
 
 
-def _check(x, y):
-    """y (the kernel's output) against the oracle on x, element by element."""
+def _check(x, y, staged=None):
+    """y (the kernel's output) against the oracle on x, element by element.  `staged`
+    says whether the rows took the staged kernels (default: contiguous rows, N % 4 == 0)."""
+    if staged is None:
+        staged = x.shape[1] % 4 == 0
     ref = oracle.softmax_rows_f32(x)
     assert y.shape == ref.shape
     nan_ref = np.isnan(ref)
@@ -52,7 +59,7 @@ def _check(x, y):
     with np.errstate(invalid="ignore"):
         d = x.astype(np.float64) - x.max(axis=1, keepdims=True).astype(np.float64)
     ad = np.where(np.isfinite(d), np.abs(d), 0)
-    n = _chain(x.shape[1]) + 8
+    n = _chain(x.shape[1], staged)
     tol = U * (16 + ad + 2 * ad.max(axis=1, keepdims=True) + 7 * n) * ref + 1e-37
     err = np.abs(y.astype(np.float64) - ref.astype(np.float64))
     bad = ~(err <= tol) & valid[:, None]
@@ -70,13 +77,13 @@ def _run(x, inplace=False):
 # (M, N, seed) for 16-byte-aligned rows.  Up to 8192 columns a team of 1, 2, 4 or 8 warps
 # holds a row in registers (several rows staged per ring slot); up to 16 * 8192 columns a
 # cluster of ceil(N / 8192) CTAs splits each row the same way; up to 16 * 24576 columns a
-# cluster of 16 CTAs stages each slice in 16 KB shared-memory slots; beyond that the
-# two-pass kernel.  The tall shapes wrap every CTA's slot ring several times.
+# cluster of 16 CTAs stages each slice in 16 KB shared-memory slots, and reads it twice
+# when it exceeds the ring.  The tall shapes wrap every CTA's slot ring several times.
 SHAPES = [(1, 1, 10), (7, 1, 11), (33, 5, 12), (300, 37, 13), (129, 128, 14), (64, 129, 15), (257, 256, 16),
           (100, 511, 17), (65, 1000, 18), (40, 1024, 19), (80000, 100, 40), (31, 1025, 20), (17, 2048, 21),
           (9, 2049, 22), (20, 3000, 23), (5, 4096, 24), (5, 4097, 25), (3, 8192, 26), (8000, 2000, 41),
           (3, 8193, 27), (2, 51200, 28), (2, 51201, 29), (1000, 30000, 42), (2, 131072, 43), (2, 131073, 44),
-          (2, 200003, 30), (2, 393216, 31), (2, 393217, 32)]
+          (2, 200003, 30), (2, 393216, 31), (2, 393217, 32), (3, 1 << 20, 33), (2, 1000003, 34)]
 
 
 @pytest.mark.parametrize("M,N,seed", SHAPES)
@@ -117,7 +124,7 @@ def test_padded_and_unaligned(N):
                                   torch.cuda.current_stream().cuda_stream)
         assert st == 0
         torch.cuda.synchronize()
-        _check(x, dst[:, :N].cpu().numpy())
+        _check(x, dst[:, :N].cpu().numpy(), staged=(ld % 4 == 0 and off % 4 == 0))
         assert torch.all(dst[:, N:] == -7.0), "padding columns were written"
         assert torch.all(ybuf[:off] == -7.0) and torch.all(ybuf[off + M * ld:] == -7.0)
 
@@ -128,7 +135,7 @@ def test_in_place(N):
     _check(x, _run(x, inplace=True))
 
 
-@pytest.mark.parametrize("N", [4, 3000, 60000])
+@pytest.mark.parametrize("N", [4, 3000, 60000, 300000, 1 << 20])
 def test_special_values(N):
     """-inf entries give exactly 0; rows with NaN, +inf or only -inf give NaN everywhere."""
     x = inputs.normal_f32(np.random.default_rng(N + 3), 6, N)
@@ -157,3 +164,25 @@ def test_empty_and_invalid():
     assert tct.softmax_rows_f32(0, p, 2, 8, 8, 8, s) == 1
     torch.cuda.synchronize()
     assert torch.all(X == 0)
+
+
+@pytest.mark.parametrize("N", [3, 8, 100, 128, 1000, 1024, 2047, 4096, 8192, 8196, 30000, 131072, 131076,
+                               393216, 500000, 1 << 20])
+def test_exact_zero_inf_rows(N):
+    """Rows of 0 and -inf: exp gives exactly 1 and 0, so the softmax is exactly 1/k on the k
+    zeros, in every kernel; compared bit for bit (k = 0 gives a NaN row)."""
+    rng = np.random.default_rng(N + 5)
+    M = 6
+    x = np.where(rng.random((M, N)) < 0.5, np.float32(0), np.float32(-np.inf)).astype(np.float32)
+    x[1, :] = 0  # k = N
+    x[2, :] = -np.inf
+    x[2, N - 1] = 0  # k = 1, in the tail
+    x[3, :] = -np.inf  # k = 0
+    y = _run(x)
+    k = (x == 0).sum(axis=1)
+    for i in range(M):
+        if k[i] == 0:
+            assert np.isnan(y[i]).all()
+        else:
+            want = np.where(x[i] == 0, np.float32(1) / np.float32(k[i]), np.float32(0))
+            assert np.array_equal(y[i], want), f"row {i}: {np.flatnonzero(y[i] != want)[:5]}"
