@@ -1,6 +1,7 @@
 """Benchmark: FP16 -> FP32 GEMM throughput on GB300 through the library's C ABI.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
+                  [--workload {gemm,softmax}] [--configs]
 
 A step is one C = A.B call on the 8192 x 8192 x 8192 workload (A, B drawn N(0,1) from
 seed 4, rounded to FP16).  The inputs (256 MiB) are larger than L2, so no flush is needed
@@ -10,6 +11,11 @@ maximum over ranks and the value the aggregate throughput.
 
 --impl reference times the CPU oracle (the plain FP64-accumulating definition) on the
 host cores over a bounded sample of the same workload.
+
+--workload softmax measures the second, bandwidth-bound workload instead: the fused row
+softmax of a 65536 x 1024 FP32 matrix (N(0,1), seed 2; 256 MiB in, 256 MiB out, larger
+than L2), one softmax_rows_f32 call per step, in GB/s of algorithmic traffic (read MN +
+write MN), with the page's own 4096 x 1024 case (L2 flushed before each launch) beside it.
 """
 import argparse
 import hashlib
@@ -33,6 +39,12 @@ FALLBACK_PEAK_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
 SUSTAINED_SECONDS = 0.25
 KERNEL_SOURCES = ("gemm_sm103a.cu", "ptx_sm103a.cuh", "tile_sched.h", "gemm_internal.h", "api.cu")
+SOFTMAX_SOURCES = ("softmax_sm103a.cu", "ptx_sm103a.cuh", "gemm_internal.h")
+SOFTMAX_WORKLOAD = (65536, 1024)
+SOFTMAX_SEED = 2
+SOFTMAX_METRIC = "fused row softmax GB/s (read MN + write MN FP32); % of measured HBM copy bandwidth"
+SOFTMAX_UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
 
 
 def parse():
@@ -43,6 +55,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target length of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["gemm", "softmax"], default="gemm")
     ap.add_argument("--configs", action="store_true",
                     help="instead of the benchmark line, time every workload shape (one JSON line each)")
     return ap.parse_args()
@@ -79,24 +92,32 @@ def peaks():
         return FALLBACK_PEAK_TFLOPS, None, "fallback"
 
 
-def kernel_hash():
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash(sources=KERNEL_SOURCES):
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "tensor_core_tiled_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch():
-    """DRAM bytes (read + write) per launch of the main kernel from the committed ncu
+def traffic_per_launch(name="gemm_8192_dram_traffic.json", sources=KERNEL_SOURCES):
+    """DRAM bytes (read + write) per launch of the measured kernel from the committed ncu
     summary, or None if absent or taken on a different kernel source."""
-    path = os.path.join(ROOT, "profiles", "gemm_8192_dram_traffic.json")
+    path = os.path.join(ROOT, "profiles", name)
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("kernel_hash") != kernel_hash():
+    if d.get("kernel_hash") != kernel_hash(sources):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -505,8 +526,223 @@ def run_configs(args):
     return 0
 
 
+# ---------------------------------------------------------------- softmax workload
+
+def softmax_input(M, N, seed):
+    import numpy as np
+    from tensor_core_tiled_gb300 import inputs
+    return inputs.normal_f32(np.random.default_rng(seed), M, N)
+
+
+def _softmax_oracle_sample(X, rows):
+    """Time the oracle's softmax on rows [0, rows); returns (seconds, algorithmic bytes)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.softmax_rows_f32(X[:rows])
+    return time.perf_counter() - t0, 2.0 * 4 * rows * X.shape[1]
+
+
+def _softmax_rows_for(X, seconds):
+    import oracle
+    oracle.build()
+    probe = min(X.shape[0], 256)
+    s, _ = _softmax_oracle_sample(X, probe)
+    return int(max(1, min(X.shape[0], probe * seconds / max(s, 1e-9))))
+
+
+def _softmax_baseline_record(X, rows, secs, byts):
+    import oracle
+    M, N = X.shape
+    return {"value": byts / secs / 1e9, "unit": SOFTMAX_UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {M}x{N} seed-{SOFTMAX_SEED} matrix ({rows * N} outputs in "
+                      f"{secs:.2f} s), FP64 arithmetic, all host threads"}
+
+
+def softmax_config(M, N):
+    return {"workload": f"softmax_rows_f32 {M}x{N}, X N(0,1) FP32 from seed {SOFTMAX_SEED}, row softmax",
+            "M": M, "N": N, "l2": "input and output (256 MiB each) larger than L2; no flush"}
+
+
+def run_softmax_reference(args):
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return 0
+    M, N = SOFTMAX_WORKLOAD
+    X = softmax_input(M, N, SOFTMAX_SEED)
+    per_step = max(0.02, 6.0 * args.cpu_seconds / max(1, args.steps + args.warmup))
+    rows = _softmax_rows_for(X, per_step)
+    for _ in range(args.warmup):
+        _softmax_oracle_sample(X, rows)
+    secs = byts = 0.0
+    for _ in range(args.steps):
+        s, b = _softmax_oracle_sample(X, rows)
+        secs += s
+        byts += b
+    value = byts / secs / 1e9
+    rec = _softmax_baseline_record(X, rows, secs / args.steps, byts / args.steps)
+    rec["value"] = value
+    line = {"impl": "reference", "metric": SOFTMAX_METRIC, "value": value, "unit": SOFTMAX_UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": softmax_config(M, N), "cpu_baseline": rec,
+            "e2e": {"value": value, "unit": SOFTMAX_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_softmax(args):
+    import torch
+
+    import tensor_core_tiled_gb300 as tct
+    from tensor_core_tiled_gb300 import build as lib_build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        lib_build.build()
+    if dist:
+        dist.barrier()
+    tct.load()
+
+    M, N = SOFTMAX_WORKLOAD
+    X = softmax_input(M, N, SOFTMAX_SEED)
+    hX = torch.from_numpy(X).pin_memory()
+    dX = hX.to(dev)
+    dY = torch.empty_like(dX)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    byts = 2.0 * 4 * M * N
+
+    def launch(src=dX, dst=dY, m=M, n=N):
+        st = tct.softmax_rows_f32(src.data_ptr(), dst.data_ptr(), m, n, n, n, sp)
+        if st:
+            raise tct.GemmError(st, "softmax_rows_f32")
+
+    for _ in range(max(3, args.warmup)):
+        launch()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for e0, e1 in evs:
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    if dist:
+        dist.barrier()
+    total_ms = g0.elapsed_time(g1)
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+    if dist:
+        total_ms = dist_max(total_ms, dist, dev)
+    ms_per_step = total_ms / args.steps
+    value = world * byts / (ms_per_step * 1e-3) / 1e9
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+
+    # end to end with host buffers: H2D of X from pinned memory, the softmax, D2H of Y
+    hY = torch.empty_like(hX).pin_memory()
+    e2e_steps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        dX.copy_(hX, non_blocking=True)
+        launch()
+        hY.copy_(dY, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = x0.elapsed_time(x1) / e2e_steps
+    if dist:
+        e2e_ms = dist_max(e2e_ms, dist, dev)
+    e2e_value = world * byts / (e2e_ms * 1e-3) / 1e9
+
+    # the page's own case, 4096 x 1024 (16 MiB each way, inside L2): L2 flushed per launch
+    m2, n2 = 4096, 1024
+    sX = torch.from_numpy(softmax_input(m2, n2, SOFTMAX_SEED)).to(dev)
+    sY = torch.empty_like(sX)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(5):
+        launch(sX, sY, m2, n2)
+    n_sec = max(5, min(args.steps, 100))
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_sec)]
+    for a, b in pairs:
+        flush.fill_(1.0)
+        a.record(stream)
+        launch(sX, sY, m2, n2)
+        b.record(stream)
+    torch.cuda.synchronize()
+    sec_ms = statistics.mean([a.elapsed_time(b) for a, b in pairs])
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+
+    peak, peak_src = hbm_peak()
+    mean_launch = statistics.mean(launch_ms)
+    achieved = byts / (mean_launch * 1e-3) / 1e9
+    line = None
+    if rank == 0:
+        line = {
+            "metric": SOFTMAX_METRIC, "value": value, "unit": SOFTMAX_UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(softmax_config(M, N), parallelism=f"replicas x{world}"),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak,
+                         "traffic": traffic_per_launch("softmax_65536x1024_dram_traffic.json", SOFTMAX_SOURCES),
+                         "peak_source": f"{peak_src} HBM copy bandwidth (read + write bytes)",
+                         "algorithmic_bytes_per_launch": byts,
+                         "kernel_ms_mean": mean_launch, "kernel_ms_min": min(launch_ms)},
+            "e2e": {"value": e2e_value, "unit": SOFTMAX_UNIT, "h2d_bytes_per_step": int(dX.numel() * 4),
+                    "d2h_bytes_per_step": int(dY.numel() * 4), "steps": e2e_steps, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "secondary": {"workload": f"softmax_rows_f32 {m2}x{n2} (the page's case), seed {SOFTMAX_SEED}, "
+                                      f"L2 flushed before each launch",
+                          "value": 2.0 * 4 * m2 * n2 / (sec_ms * 1e-3) / 1e9, "unit": SOFTMAX_UNIT,
+                          "us_mean": sec_ms * 1e3, "launches": n_sec},
+            "kernel_hash": kernel_hash(SOFTMAX_SOURCES),
+        }
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            rows = _softmax_rows_for(X, args.cpu_seconds)
+            secs, b = _softmax_oracle_sample(X, rows)
+            line["cpu_baseline"] = _softmax_baseline_record(X, rows, secs, b)
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.workload == "softmax":
+        return run_softmax_reference(args) if args.impl == "reference" else run_softmax(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.configs:

@@ -273,7 +273,6 @@ struct StagedShared {
     float2 pairs[2][kMaxCluster];  // (slice max, slice sum) of every rank, two rows in turn
     float redm[kComputeWarps];
     float reds[kComputeWarps];
-    int redn[kComputeWarps];
     int abort_flag;
 };
 static_assert(sizeof(StagedShared) <= kHeaderBytes, "staged kernel header");
@@ -338,7 +337,15 @@ __device__ __forceinline__ void staged_init(StagedShared &sh, const StagedParams
 }
 
 __device__ __forceinline__ float max4(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
-__device__ __forceinline__ int nan4(float4 v) { return isnan(v.x) | isnan(v.y) | isnan(v.z) | isnan(v.w); }
+// e^d computed as 2^(d log2 e) with the hardware base-2 exponential (ex2.approx: relative
+// error about 2^-22 in the result; subnormal results kept).  Rounding d log2 e adds a relative
+// error of about |d| u to the result (u = 2^-24), the same order as rounding d = x - max itself.
+__device__ __forceinline__ float exp_of(float d)
+{
+    float r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(d * 1.44269504088896341f));
+    return r;
+}
 
 // Reductions over a team of TT threads (TT = 8, 16, 32 lanes of one warp, or 2-8 whole
 // warps).  Within a warp, xor-shuffles over aligned groups of min(TT, 32) lanes; across the
@@ -361,27 +368,18 @@ __device__ __forceinline__ float group_sum(float v)
 }
 
 template <int TT>
-__device__ __forceinline__ int group_any(int v)
-{
-#pragma unroll
-    for (int o = (TT < 32 ? TT : 32) / 2; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-template <int TT>
-__device__ __forceinline__ void team_reduce_max_any(float &m, int &nan, StagedShared &sh, int team, int warp, int lane)
+__device__ __forceinline__ float team_reduce_max(float m, StagedShared &sh, int team, int warp, int lane)
 {
     m = group_max<TT>(m);
-    nan = group_any<TT>(nan);
     if constexpr (TT > 32) {
         constexpr int T = TT / 32;
-        if (lane == 0) sh.redm[warp] = m, sh.redn[warp] = nan;
+        if (lane == 0) sh.redm[warp] = m;
         named_bar_sync(1 + team, TT);
         m = sh.redm[team * T];
-        nan = sh.redn[team * T];
 #pragma unroll
-        for (int w = 1; w < T; ++w) m = fmaxf(m, sh.redm[team * T + w]), nan |= sh.redn[team * T + w];
+        for (int w = 1; w < T; ++w) m = fmaxf(m, sh.redm[team * T + w]);
     }
+    return m;
 }
 
 template <int TT>
@@ -397,6 +395,23 @@ __device__ __forceinline__ float team_reduce_sum(float v, StagedShared &sh, int 
         for (int w = 1; w < T; ++w) v += sh.reds[team * T + w];
     }
     return v;
+}
+
+// Scale for a slice whose terms are exp(x - m) (m the slice maximum), given every slice's
+// (maximum, sum) pair: exp(m - M) / S with M the row maximum and S the row sum rescaled to
+// it.  A NaN sum (the slice held a NaN, or a +inf maximum) or a row with no finite maximum
+// gives NaN; a slice that is all -inf gets 0.
+__device__ __forceinline__ float slice_scale(const float2 *pairs, uint32_t csize, float m)
+{
+    float M = -INFINITY;
+    for (uint32_t c = 0; c < csize; ++c) M = fmaxf(M, pairs[c].x);
+    float S = 0.0f;
+    for (uint32_t c = 0; c < csize; ++c) {
+        const float2 pr = pairs[c];
+        S += pr.y * (pr.x == -INFINITY ? 0.0f : expf(pr.x - M));  // NaN * 0 stays NaN
+    }
+    if (!isfinite(M)) return NAN;
+    return (m == -INFINITY ? 0.0f : expf(m - M)) / S;
 }
 
 // Rows (or, in a cluster, row slices) of at most TT * VEC * 4 columns.  The 256 compute
@@ -489,20 +504,20 @@ __global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_team(const
                 }
                 const float tv = live && has_tail ? xg[nb + tt] : -INFINITY;
                 float m = tv;
-                int nan = isnan(tv);
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) nan |= nan4(v[k]), m = fmaxf(m, max4(v[k]));
-                team_reduce_max_any<TT>(m, nan, sh, team, warp, lane);
-                const bool none = (m == -INFINITY);  // all -inf (or empty): every term is 0
+                for (int k = 0; k < VEC; ++k) m = fmaxf(m, max4(v[k]));
+                m = team_reduce_max<TT>(m, sh, team, warp, lane);
+                // A NaN entry, a +inf maximum or an all -inf row makes a term NaN, hence the sum
+                // and every output of the row.  A cluster slice that is all -inf sums to 0.
+                const float mu = (kCluster && m == -INFINITY) ? 0.0f : m;
                 float sum = 0.0f;
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) {
                     float4 &e = v[k];
-                    e.x = none ? 0.0f : expf(e.x - m), e.y = none ? 0.0f : expf(e.y - m);
-                    e.z = none ? 0.0f : expf(e.z - m), e.w = none ? 0.0f : expf(e.w - m);
+                    e.x = exp_of(e.x - mu), e.y = exp_of(e.y - mu), e.z = exp_of(e.z - mu), e.w = exp_of(e.w - mu);
                     sum += (e.x + e.y) + (e.z + e.w);
                 }
-                const float te = has_tail && !none ? expf(tv - m) : 0.0f;
+                const float te = exp_of(tv - mu);
                 sum = team_reduce_sum<TT>(sum + te, sh, team, warp, lane);
 
                 float f;
@@ -512,23 +527,13 @@ __global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_team(const
                     if (tt == 0) {
                         mbar_arrive_expect_tx(xbar, csize * 8u);
                         const uint32_t slot = smem_u32(&sh.pairs[j][rank]);
-                        const float sv = nan ? NAN : sum;
                         for (uint32_t c = 0; c < csize; ++c)
-                            st_async_f32x2(map_to_cta(slot, c), m, sv, map_to_cta(xbar, c));
+                            st_async_f32x2(map_to_cta(slot, c), m, sum, map_to_cta(xbar, c));
                     }
                     staged_wait<true>(xbar, (row_ctr >> 1) & 1u, sh, p, SITE_SM_XCHG);
-                    float M = -INFINITY;
-                    for (uint32_t c = 0; c < csize; ++c) M = fmaxf(M, sh.pairs[j][c].x);
-                    float S = 0.0f;
-                    int bad = 0;
-                    for (uint32_t c = 0; c < csize; ++c) {
-                        const float2 pr = sh.pairs[j][c];
-                        bad |= isnan(pr.y);
-                        S += pr.x == -INFINITY ? 0.0f : pr.y * expf(pr.x - M);
-                    }
-                    f = (!bad && isfinite(M)) ? (none ? 0.0f : expf(m - M) / S) : NAN;
+                    f = slice_scale(sh.pairs[j], csize, m);
                 } else {
-                    f = (!nan && isfinite(m)) ? __frcp_rn(sum) : NAN;
+                    f = __frcp_rn(sum);
                 }
                 if (live) {
                     float4 *y4 = reinterpret_cast<float4 *>(yg);
@@ -611,43 +616,32 @@ __global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_long_slice
             const bool has_tail = tid < len - nb;
             const float tv = has_tail ? xg[nb + tid] : -INFINITY;
             float m = tv, sum = 0.0f;
-            int nan = isnan(tv);
             if (resident) {
                 for (uint32_t c = 0; c < nch; ++c) {
                     wait_full(q + c);
                     const float4 *x4 = reinterpret_cast<const float4 *>(slot_ptr(q + c));
                     const uint32_t f4 = chunk_f4(c);
 #pragma unroll 4
-                    for (uint32_t i = tid; i < f4; i += kComputeThreads) {
-                        const float4 v = x4[i];
-                        nan |= nan4(v);
-                        m = fmaxf(m, max4(v));
-                    }
+                    for (uint32_t i = tid; i < f4; i += kComputeThreads) m = fmaxf(m, max4(x4[i]));
                 }
-                team_reduce_max_any<kComputeThreads>(m, nan, sh, 0, warp, lane);
-                const bool none = (m == -INFINITY);  // all -inf (or empty): every term is 0
+                m = team_reduce_max<kComputeThreads>(m, sh, 0, warp, lane);
+                const float mu = m == -INFINITY ? 0.0f : m;  // an all -inf slice sums to 0
                 for (uint32_t c = 0; c < nch; ++c) {
                     float4 *x4 = reinterpret_cast<float4 *>(slot_ptr(q + c));
                     const uint32_t f4 = chunk_f4(c);
 #pragma unroll 4
                     for (uint32_t i = tid; i < f4; i += kComputeThreads) {
                         float4 v = x4[i];
-                        if (none) {
-                            v = make_float4(0.f, 0.f, 0.f, 0.f);
-                        } else {
-                            v.x = expf(v.x - m), v.y = expf(v.y - m), v.z = expf(v.z - m), v.w = expf(v.w - m);
-                        }
+                        v.x = exp_of(v.x - mu), v.y = exp_of(v.y - mu), v.z = exp_of(v.z - mu), v.w = exp_of(v.w - mu);
                         x4[i] = v;
                         sum += (v.x + v.y) + (v.z + v.w);
                     }
                 }
                 fence_proxy_async_smem();  // the slots are refilled by bulk copies after release
-                if (has_tail && !none) sum += expf(tv - m);
-                sum = team_reduce_sum<kComputeThreads>(sum, sh, 0, warp, lane);
+                sum = team_reduce_sum<kComputeThreads>(sum + exp_of(tv - mu), sh, 0, warp, lane);
             } else {
-                // online pass: running (m, sum) per thread, sum relative to m
-                if (m == -INFINITY) m = -INFINITY, sum = 0.0f;
-                else sum = 1.0f;  // the tail element itself
+                // online pass: running (m, sum) per thread, sum relative to m (to 0 while m is -inf)
+                sum = exp_of(tv - (m == -INFINITY ? 0.0f : m));
                 for (uint32_t c = 0; c < nch; ++c) {
                     wait_full(q + c);
                     const float4 *x4 = reinterpret_cast<const float4 *>(slot_ptr(q + c));
@@ -655,22 +649,21 @@ __global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_long_slice
 #pragma unroll 2
                     for (uint32_t i = tid; i < f4; i += kComputeThreads) {
                         const float4 v = x4[i];
-                        nan |= nan4(v);
                         const float mv = max4(v);
                         if (mv > m) {
-                            sum = m == -INFINITY ? 0.0f : sum * expf(m - mv);
+                            sum *= m == -INFINITY ? 0.0f : expf(m - mv);  // NaN * 0 stays NaN
                             m = mv;
                         }
-                        if (m != -INFINITY) sum += (expf(v.x - m) + expf(v.y - m)) + (expf(v.z - m) + expf(v.w - m));
+                        const float mu = m == -INFINITY ? 0.0f : m;
+                        sum += (exp_of(v.x - mu) + exp_of(v.y - mu)) + (exp_of(v.z - mu) + exp_of(v.w - mu));
                     }
                     release(q + c);
                 }
-                float mt = m;
-                team_reduce_max_any<kComputeThreads>(m, nan, sh, 0, warp, lane);
-                sum = mt == -INFINITY ? 0.0f : sum * expf(mt - m);  // rescale to the slice maximum
+                const float mt = m;
+                m = team_reduce_max<kComputeThreads>(m, sh, 0, warp, lane);
+                sum *= (mt == -INFINITY || m == -INFINITY) ? 1.0f : expf(mt - m);  // to the slice maximum
                 sum = team_reduce_sum<kComputeThreads>(sum, sh, 0, warp, lane);
             }
-            const bool none = (m == -INFINITY);
 
             // (max, sum) of every slice of the row, from every rank of the cluster
             const uint32_t j = row_ctr & 1u;
@@ -678,24 +671,13 @@ __global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_long_slice
             if (tid == 0) {
                 mbar_arrive_expect_tx(xbar, csize * 8u);
                 const uint32_t slot = smem_u32(&sh.pairs[j][rank]);
-                const float sv = nan ? NAN : sum;
-                for (uint32_t r = 0; r < csize; ++r) st_async_f32x2(map_to_cta(slot, r), m, sv, map_to_cta(xbar, r));
+                for (uint32_t r = 0; r < csize; ++r) st_async_f32x2(map_to_cta(slot, r), m, sum, map_to_cta(xbar, r));
             }
             staged_wait<true>(xbar, (row_ctr >> 1) & 1u, sh, p, SITE_SM_XCHG);
-            float M = -INFINITY;
-            for (uint32_t r = 0; r < csize; ++r) M = fmaxf(M, sh.pairs[j][r].x);
-            float S = 0.0f;
-            int bad = 0;
-            for (uint32_t r = 0; r < csize; ++r) {
-                const float2 pr = sh.pairs[j][r];
-                bad |= isnan(pr.y);
-                S += pr.x == -INFINITY ? 0.0f : pr.y * expf(pr.x - M);
-            }
-            const bool ok = !bad && isfinite(M);
+            const float f = slice_scale(sh.pairs[j], csize, m);
 
             float4 *y4 = reinterpret_cast<float4 *>(yg);
             if (resident) {
-                const float f = ok ? (none ? 0.0f : expf(m - M) / S) : NAN;
                 for (uint32_t c = 0; c < nch; ++c) {
                     const float4 *x4 = reinterpret_cast<const float4 *>(slot_ptr(q + c));
                     const uint32_t f4 = chunk_f4(c);
@@ -708,9 +690,10 @@ __global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_long_slice
                     }
                     release(q + c);
                 }
-                if (has_tail) __stcs(yg + nb + tid, (none ? 0.0f : expf(tv - m)) * f);
+                if (has_tail) __stcs(yg + nb + tid, exp_of(tv - (m == -INFINITY ? 0.0f : m)) * f);
             } else {
-                const float g = ok ? __frcp_rn(S) : NAN;
+                // second read: exp(x - m) * f with m the slice maximum, as in resident mode
+                const float mu = m == -INFINITY ? 0.0f : m;
                 for (uint32_t c = 0; c < nch; ++c) {
                     wait_full(q + nch + c);
                     const float4 *x4 = reinterpret_cast<const float4 *>(slot_ptr(q + nch + c));
@@ -719,12 +702,12 @@ __global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_long_slice
 #pragma unroll 2
                     for (uint32_t i = tid; i < f4; i += kComputeThreads) {
                         const float4 v = x4[i];
-                        __stcs(yc + i, make_float4(expf(v.x - M) * g, expf(v.y - M) * g, expf(v.z - M) * g,
-                                                   expf(v.w - M) * g));
+                        __stcs(yc + i, make_float4(exp_of(v.x - mu) * f, exp_of(v.y - mu) * f, exp_of(v.z - mu) * f,
+                                                   exp_of(v.w - mu) * f));
                     }
                     release(q + nch + c);
                 }
-                if (has_tail) __stcs(yg + nb + tid, expf(tv - M) * g);
+                if (has_tail) __stcs(yg + nb + tid, exp_of(tv - mu) * f);
             }
         }
     }
