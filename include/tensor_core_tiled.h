@@ -253,6 +253,34 @@ TCT_API gemm_status softmax_rows_f32(const float *X, float *Y, int64_t M, int64_
                                      void *stream);
 
 /*
+ * gemm_f16_f32_host -- gemm_f16_f32 with A, B and C in host memory (same layouts, leading
+ * dimensions and conventions).  B is copied to the device first; A then follows in row blocks
+ * (8 blocks of whole 256-row tiles), each block is multiplied on `stream` as soon as its rows
+ * have arrived, and its rows of C are copied back while later blocks are still in flight, so
+ * the two copy directions and the tensor-core work overlap.  The copies run on two library
+ * streams; the device copies of A, B and C come from the library's stream-ordered pool.  Host
+ * memory should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to be
+ * asynchronous; pageable memory gives the same result with serialised copies.
+ * Stream-ordered: the work starts after everything queued on `stream` before the call, and
+ * work queued on `stream` after it starts once C is complete in host memory; A, B and C must
+ * stay valid until then.  The pages have no such call: they time device-resident operands;
+ * this is the end-to-end form of the product for callers whose data lives in host memory.
+ * Returns the statuses of gemm_f16_f32.
+ */
+TCT_API gemm_status gemm_f16_f32_host(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                                      int64_t lda, int64_t ldb, int64_t ldc, void *stream);
+
+/*
+ * softmax_rows_f32_host -- softmax_rows_f32 with X and Y in host memory (Y may be X with
+ * ldy == ldx).  X is copied to one device buffer in 8 row blocks, each block is softmaxed in
+ * place on `stream` as soon as it has arrived, and copied back to Y while later blocks are in
+ * flight.  Stream and memory rules as for gemm_f16_f32_host; the page's fused softmax has no
+ * host-buffer form.  Returns the statuses of softmax_rows_f32.
+ */
+TCT_API gemm_status softmax_rows_f32_host(const float *X, float *Y, int64_t M, int64_t N, int64_t ldx, int64_t ldy,
+                                          void *stream);
+
+/*
  * Reads and clears the device error word of the current device: GEMM_OK, or
  * GEMM_ERR_DEVICE_TIMEOUT if a kernel launched since the last read gave up on a pipeline
  * wait (its output is then incomplete).  Synchronises the current device first.

@@ -29,6 +29,8 @@ EXPORTED = (
     "gemm_f32acc",
     "gemm_ex",
     "softmax_rows_f32",
+    "gemm_f16_f32_host",
+    "softmax_rows_f32_host",
     "gemm_f16_f32_plan",
     "gemm_f16_f32_work_item",
     "gemm_tile_coord",
@@ -96,6 +98,10 @@ def load():
                             ctypes.POINTER(GemmEpilogue), vp, ctypes.POINTER(GemmOptions)]
     lib.softmax_rows_f32.restype = ctypes.c_int
     lib.softmax_rows_f32.argtypes = [vp, vp, i64, i64, i64, i64, vp]
+    lib.softmax_rows_f32_host.restype = ctypes.c_int
+    lib.softmax_rows_f32_host.argtypes = [vp, vp, i64, i64, i64, i64, vp]
+    lib.gemm_f16_f32_host.restype = ctypes.c_int
+    lib.gemm_f16_f32_host.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
     lib.gemm_f16_f32_ex.restype = ctypes.c_int
     lib.gemm_f16_f32_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, ctypes.POINTER(GemmOptions)]
     lib.gemm_f16_f32_plan.restype = ctypes.c_int
@@ -331,3 +337,13 @@ def softmax(X, out=None, stream=None):
     if st:
         raise GemmError(st, "softmax_rows_f32")
     return out
+
+
+def gemm_f16_f32_host(A, B, C, M, N, K, lda, ldb, ldc, stream=0):
+    """Raw C-ABI call of the host-buffer GEMM (host pointers as ints); returns the status."""
+    return load().gemm_f16_f32_host(A, B, C, M, N, K, lda, ldb, ldc, stream or None)
+
+
+def softmax_rows_f32_host(X, Y, M, N, ldx, ldy, stream=0):
+    """Raw C-ABI call of the host-buffer row softmax (host pointers as ints); returns the status."""
+    return load().softmax_rows_f32_host(X, Y, M, N, ldx, ldy, stream or None)

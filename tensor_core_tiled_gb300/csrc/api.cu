@@ -751,3 +751,174 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
     std::memset(&tp, 0, sizeof(tp));
     return to_status(tct::launch_gemm(ta, tb, tp, p, 0, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
 }
+
+// ---------------------------------------------------------------- host-buffer pipelines
+
+namespace {
+
+constexpr int kHostChunks = 8;        // row blocks a host-buffer call is split into
+constexpr int64_t kHostChunkAlign = 256;  // GEMM row blocks: whole CTA-pair tiles
+
+// Per-device copy streams and events of the host-buffer calls.  One call at a time enqueues
+// on them (the mutex); waits already enqueued keep the event state of their own call, so the
+// events are reused by the next call.
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, inputs_shared = nullptr, done = nullptr;
+    cudaEvent_t in[kHostChunks] = {}, out[kHostChunks] = {};
+};
+std::mutex g_host_mu;
+HostPipe g_host[kMaxDevices];
+
+gemm_status host_pipe(HostPipe **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    HostPipe &h = g_host[dev];
+    if (!h.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        bool ok = cudaStreamCreateWithFlags(&h.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&h.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.start, ef) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.inputs_shared, ef) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.done, ef) == cudaSuccess;
+        for (int i = 0; ok && i < kHostChunks; ++i)
+            ok = cudaEventCreateWithFlags(&h.in[i], ef) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h.out[i], ef) == cudaSuccess;
+        if (!ok) return GEMM_ERR_CUDA;
+        h.ready = true;
+    }
+    *out = &h;
+    return GEMM_OK;
+}
+
+// Row blocks of a host-buffer call: ceil(M / kHostChunks) rounded up to `align`.
+int64_t host_chunk_rows(int64_t M, int64_t align)
+{
+    return std::max<int64_t>(align, round_up((M + kHostChunks - 1) / kHostChunks, align));
+}
+
+// Ends a host-buffer call: the caller's stream waits for both copy streams, then releases the
+// device temporary (also on the error path, so nothing in flight loses its memory).
+gemm_status host_finish(HostPipe *hp, cudaStream_t s, void *ws, gemm_status result)
+{
+    bool ok = cudaEventRecord(hp->done, hp->d2h) == cudaSuccess && cudaStreamWaitEvent(s, hp->done, 0) == cudaSuccess &&
+              cudaEventRecord(hp->start, hp->h2d) == cudaSuccess && cudaStreamWaitEvent(s, hp->start, 0) == cudaSuccess;
+    ok = cudaFreeAsync(ws, s) == cudaSuccess && ok;
+    return result != GEMM_OK ? result : (ok ? GEMM_OK : GEMM_ERR_CUDA);
+}
+
+#define TCT_CUDA_OK(x)                                                 \
+    do {                                                               \
+        if ((x) != cudaSuccess) return host_finish(hp, s, ws, GEMM_ERR_CUDA); \
+    } while (0)
+
+}  // namespace
+
+extern "C" gemm_status gemm_f16_f32_host(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                                         int64_t lda, int64_t ldb, int64_t ldc, void *stream)
+{
+    gemm_status st = check_args(A, B, C, M, N, K, lda, ldb, ldc, 0, GEMM_DTYPE_F32);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceInfo dev;
+    st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaMemPool_t pool = nullptr;
+    st = device_pool(&pool);
+    if (st != GEMM_OK) return st;
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostPipe *hp = nullptr;
+    st = host_pipe(&hp);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // Device copies with 16-byte row pitches, so that the GEMM reads them in place.
+    const int64_t ka = round_up(std::max<int64_t>(K, 1), 8), nb = round_up(N, 8), nc = round_up(N, 4);
+    const size_t a_bytes = static_cast<size_t>(M * ka * 2), b_bytes = static_cast<size_t>(K * nb * 2);
+    const size_t c_bytes = static_cast<size_t>(M * nc * 4);
+    const size_t a_off = round_up(static_cast<int64_t>(b_bytes), 256);
+    const size_t c_off = a_off + round_up(static_cast<int64_t>(a_bytes), 256);
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, c_off + c_bytes, pool, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    char *base = static_cast<char *>(ws);
+    auto *dB = reinterpret_cast<uint16_t *>(base);
+    auto *dA = reinterpret_cast<uint16_t *>(base + a_off);
+    auto *dC = reinterpret_cast<float *>(base + c_off);
+
+    // B first (every row block needs all of it), then A block by block on the copy stream;
+    // each block's product runs on the caller's stream as soon as its rows have arrived, and
+    // its rows of C go back on the second copy stream while the next block is multiplied.
+    TCT_CUDA_OK(cudaEventRecord(hp->start, s));
+    TCT_CUDA_OK(cudaStreamWaitEvent(hp->h2d, hp->start, 0));
+    TCT_CUDA_OK(cudaStreamWaitEvent(hp->d2h, hp->start, 0));
+    if (K > 0)
+        TCT_CUDA_OK(cudaMemcpy2DAsync(dB, nb * 2, B, ldb * 2, N * 2, K, cudaMemcpyHostToDevice, hp->h2d));
+    TCT_CUDA_OK(cudaEventRecord(hp->inputs_shared, hp->h2d));
+    TCT_CUDA_OK(cudaStreamWaitEvent(s, hp->inputs_shared, 0));
+    const int64_t rows = host_chunk_rows(M, kHostChunkAlign);
+    int j = 0;
+    for (int64_t r0 = 0; r0 < M; r0 += rows, ++j) {
+        const int64_t mr = std::min(rows, M - r0);
+        if (K > 0)
+            TCT_CUDA_OK(cudaMemcpy2DAsync(dA + r0 * ka, ka * 2, static_cast<const uint16_t *>(A) + r0 * lda, lda * 2,
+                                          K * 2, mr, cudaMemcpyHostToDevice, hp->h2d));
+        TCT_CUDA_OK(cudaEventRecord(hp->in[j], hp->h2d));
+        TCT_CUDA_OK(cudaStreamWaitEvent(s, hp->in[j], 0));
+        st = run_gemm(0, dA + r0 * ka, dB, dC + r0 * nc, GEMM_DTYPE_F32, mr, N, K, ka, nb, nc, nullptr, s, nullptr);
+        if (st != GEMM_OK) return host_finish(hp, s, ws, st);
+        TCT_CUDA_OK(cudaEventRecord(hp->out[j], s));
+        TCT_CUDA_OK(cudaStreamWaitEvent(hp->d2h, hp->out[j], 0));
+        TCT_CUDA_OK(cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, dC + r0 * nc, nc * 4, N * 4, mr, cudaMemcpyDeviceToHost,
+                                      hp->d2h));
+    }
+    return host_finish(hp, s, ws, GEMM_OK);
+}
+
+extern "C" gemm_status softmax_rows_f32_host(const float *X, float *Y, int64_t M, int64_t N, int64_t ldx, int64_t ldy,
+                                             void *stream)
+{
+    if (M < 0 || N < 0 || M > kMaxDim || N > kMaxDim || ldx < N || ldy < N) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!X || !Y || reinterpret_cast<uintptr_t>(X) % 4 || reinterpret_cast<uintptr_t>(Y) % 4) return GEMM_ERR_INVALID_ARG;
+    if (X == Y && ldx != ldy) return GEMM_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    gemm_status st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaMemPool_t pool = nullptr;
+    st = device_pool(&pool);
+    if (st != GEMM_OK) return st;
+    unsigned *err = nullptr;
+    if (tct::error_word_address(&err) != cudaSuccess) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostPipe *hp = nullptr;
+    st = host_pipe(&hp);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // One device matrix with 16-byte row pitches, softmaxed in place block by block.
+    const int64_t nd = round_up(N, 4);
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(M * nd * 4), pool, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    float *dX = static_cast<float *>(ws);
+    TCT_CUDA_OK(cudaEventRecord(hp->start, s));
+    TCT_CUDA_OK(cudaStreamWaitEvent(hp->h2d, hp->start, 0));
+    TCT_CUDA_OK(cudaStreamWaitEvent(hp->d2h, hp->start, 0));
+    const int64_t rows = host_chunk_rows(M, 1);
+    const uint64_t timeout_ns = static_cast<uint64_t>(kDefaultTimeoutMs) * 1000000ull;
+    int j = 0;
+    for (int64_t r0 = 0; r0 < M; r0 += rows, ++j) {
+        const int64_t mr = std::min(rows, M - r0);
+        TCT_CUDA_OK(cudaMemcpy2DAsync(dX + r0 * nd, nd * 4, X + r0 * ldx, ldx * 4, N * 4, mr, cudaMemcpyHostToDevice,
+                                      hp->h2d));
+        TCT_CUDA_OK(cudaEventRecord(hp->in[j], hp->h2d));
+        TCT_CUDA_OK(cudaStreamWaitEvent(s, hp->in[j], 0));
+        TCT_CUDA_OK(tct::launch_softmax_rows(dX + r0 * nd, dX + r0 * nd, mr, N, nd, nd, dev.sms, err, timeout_ns, s));
+        TCT_CUDA_OK(cudaEventRecord(hp->out[j], s));
+        TCT_CUDA_OK(cudaStreamWaitEvent(hp->d2h, hp->out[j], 0));
+        TCT_CUDA_OK(cudaMemcpy2DAsync(Y + r0 * ldy, ldy * 4, dX + r0 * nd, nd * 4, N * 4, mr, cudaMemcpyDeviceToHost,
+                                      hp->d2h));
+    }
+    return host_finish(hp, s, ws, GEMM_OK);
+}

@@ -54,6 +54,15 @@ def test_invalid_arguments_rejected_before_any_device_work(tct_lib):
     ]
     for args in bad:
         assert tct.gemm_f16_f32(*args, 0) == tct.GEMM_ERR_INVALID_ARG, args
+        assert tct.gemm_f16_f32_host(*args, 0) == tct.GEMM_ERR_INVALID_ARG, args
+    assert tct.gemm_f16_f32_host(0, 0, 0, 0, 5, 7, 7, 5, 5, 0) == tct.GEMM_OK
+    for fn in (tct.softmax_rows_f32, tct.softmax_rows_f32_host):
+        assert fn(p, p, -1, 4, 4, 4, 0) == tct.GEMM_ERR_INVALID_ARG
+        assert fn(p, p, 4, 8, 7, 8, 0) == tct.GEMM_ERR_INVALID_ARG      # ldx < N
+        assert fn(p, p, 4, 8, 8, 12, 0) == tct.GEMM_ERR_INVALID_ARG     # in place, ldx != ldy
+        assert fn(p + 2, p + 64, 4, 8, 8, 8, 0) == tct.GEMM_ERR_INVALID_ARG
+        assert fn(0, p, 4, 8, 8, 8, 0) == tct.GEMM_ERR_INVALID_ARG
+        assert fn(0, 0, 0, 8, 8, 8, 0) == tct.GEMM_OK
     # empty output is a no-op that needs no device
     assert tct.gemm_f16_f32(0, 0, 0, 0, 5, 7, 7, 5, 5, 0) == tct.GEMM_OK
     assert tct.gemm_f16_f32(0, 0, 0, 5, 0, 7, 7, 0, 0, 0) == tct.GEMM_OK
