@@ -11,10 +11,11 @@
 // compute warps reduce the staged rows and write the result with 16-byte streaming stores.
 //   * N <= 1024: a slot holds several rows; one compute warp per row.
 //   * N <= 12288: a slot holds one row (or a 16 KB piece of it); the eight warps share it.
-//   * longer rows: a cluster of up to 16 CTAs splits each row; every CTA reduces its slice
-//     to (max, sum), sends the pair to every CTA of the cluster through distributed shared
-//     memory (st.async, counted on the receiver's mbarrier), and rescales its slice by
-//     exp(max_slice - max_row) / sum_row.
+//   * longer rows: a cluster of CTAs splits each row (up to 8 CTAs with 8192-column slices in
+//     registers, then up to 16 CTAs with slices of about 20480 columns in shared memory);
+//     every CTA reduces its slice to (max, sum), sends the pair to every CTA of the cluster
+//     through distributed shared memory (st.async, counted on the receiver's mbarrier), and
+//     rescales its slice by exp(max_slice - max_row) / sum_row.
 // Other layouts (and rows beyond 16 slices of 96 KB) take the plain kernels below: a warp per
 // row held in registers, a CTA per row staged in shared memory, or two passes over the row.
 // exp(-inf) = 0; a row holding a NaN, whose maximum is +inf, or that is all -inf has no
@@ -550,7 +551,7 @@ __global__ void __launch_bounds__(kStagedThreads, kCtasPerSm) softmax_team(const
     if constexpr (kCluster) cluster_sync_all();  // no CTA leaves while a peer may still write to it
 }
 
-// Rows longer than 16 * 8192 columns: a cluster of 16 CTAs per row, rank r owning columns
+// Rows longer than 8 * 8192 columns: a cluster of up to 16 CTAs per row, rank r owning columns
 // [r * slice, min(N, (r + 1) * slice)), streamed through a ring of 16 KB slots.  When the
 // slice fits in the ring (resident mode) it is read once: the (max, sum) pass writes
 // exp(x - max) back into the slots and the output pass scales them.  Otherwise (streaming
@@ -746,6 +747,8 @@ const TeamVariant kTeamVariants[] = {
     {8192, 256, softmax_team<256, 8, false>},
 };
 constexpr int64_t kTeamMaxCols = 8192;  // also the slice length of the cluster team kernel
+constexpr int kTeamClusterMax = 8;      // CTAs per row of the cluster team kernel
+constexpr int64_t kLongSliceCols = 20480;  // target slice of the long-slice kernel (80 KB)
 StagedKernel const kClusterTeam = softmax_team<256, 8, true>;
 StagedKernel const kClusterLong = softmax_long_slices;
 
@@ -878,10 +881,14 @@ cudaError_t launch_softmax_rows(const float *X, float *Y, int64_t M, int64_t N, 
         return cudaGetLastError();
     }
 
-    // A cluster per row: slices of at most kTeamMaxCols columns (registers), or for longer
-    // rows up to one ring of 16 KB slots (shared memory).
-    const bool team = N <= static_cast<int64_t>(kMaxCluster) * kTeamMaxCols;
-    int csize = static_cast<int>((N + kTeamMaxCols - 1) / kTeamMaxCols);
+    // A cluster per row: up to kTeamClusterMax CTAs holding slices of at most kTeamMaxCols
+    // columns in registers; longer rows in slices of about kLongSliceCols columns staged in
+    // shared memory (at most 5 of the 6 ring slots, so the next row's first slot streams in
+    // meanwhile), at most kMaxCluster CTAs.  Measured on GB300: clusters of 7 CTAs stream
+    // markedly slower than clusters of 8, so 7 becomes 8.
+    const bool team = N <= static_cast<int64_t>(kTeamClusterMax) * kTeamMaxCols;
+    int csize = static_cast<int>(team ? (N + kTeamMaxCols - 1) / kTeamMaxCols : (N + kLongSliceCols - 1) / kLongSliceCols);
+    if (!team && csize == 7) csize = 8;
     if (csize > kMaxCluster) csize = kMaxCluster;
     p.slice = (((N + csize - 1) / csize) + 3) & ~int64_t(3);
     StagedKernel kernel;

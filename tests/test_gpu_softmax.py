@@ -78,15 +78,17 @@ def _run(x, inplace=False):
     return out.cpu().numpy()
 
 
-# (M, N, seed) for 16-byte-aligned rows.  Up to 8192 columns a team of 1, 2, 4 or 8 warps
-# holds a row in registers (several rows staged per ring slot); up to 16 * 8192 columns a
-# cluster of ceil(N / 8192) CTAs splits each row the same way; up to 16 * 24576 columns a
-# cluster of 16 CTAs stages each slice in 16 KB shared-memory slots, and reads it twice
-# when it exceeds the ring.  The tall shapes wrap every CTA's slot ring several times.
+# (M, N, seed) for 16-byte-aligned rows.  Up to 8192 columns a team of 8 to 256 threads
+# holds a row in registers (several rows staged per ring slot); up to 8 * 8192 columns a
+# cluster of ceil(N / 8192) CTAs splits each row the same way; beyond, a cluster of
+# ceil(N / 20480) CTAs (7 taken as 8, at most 16) stages each slice in 16 KB shared-memory
+# slots, and reads it twice when it exceeds the 6-slot ring (past 16 * 24576 columns).
+# The tall shapes wrap every CTA's slot ring several times.
 SHAPES = [(1, 1, 10), (7, 1, 11), (33, 5, 12), (300, 37, 13), (129, 128, 14), (64, 129, 15), (257, 256, 16),
           (100, 511, 17), (65, 1000, 18), (40, 1024, 19), (80000, 100, 40), (31, 1025, 20), (17, 2048, 21),
           (9, 2049, 22), (20, 3000, 23), (5, 4096, 24), (5, 4097, 25), (3, 8192, 26), (8000, 2000, 41),
-          (3, 8193, 27), (2, 51200, 28), (2, 51201, 29), (1000, 30000, 42), (2, 131072, 43), (2, 131073, 44),
+          (3, 8193, 27), (2, 51200, 28), (2, 51201, 29), (1000, 30000, 42), (2, 65536, 45), (2, 65537, 46), (2, 131072, 43),
+          (2, 131073, 44), (2, 143360, 47), (3, 163841, 48), (2, 327680, 49), (2, 327681, 50),
           (2, 200003, 30), (2, 393216, 31), (2, 393217, 32), (3, 1 << 20, 33), (2, 1000003, 34)]
 
 
@@ -170,8 +172,8 @@ def test_empty_and_invalid():
     assert torch.all(X == 0)
 
 
-@pytest.mark.parametrize("N", [3, 8, 100, 128, 1000, 1024, 2047, 4096, 8192, 8196, 30000, 131072, 131076,
-                               393216, 500000, 1 << 20])
+@pytest.mark.parametrize("N", [3, 8, 100, 128, 1000, 1024, 2047, 4096, 8192, 8196, 30000, 65536, 65540,
+                               131072, 131076, 143360, 393216, 500000, 1 << 20])
 def test_exact_zero_inf_rows(N):
     """Rows of 0 and -inf: exp gives exactly 1 and 0, so the softmax is exactly 1/k on the k
     zeros, in every kernel; compared bit for bit (k = 0 gives a NaN row)."""
