@@ -41,7 +41,8 @@ constexpr double kHbmBytesPerSec = 6.5e12;
 constexpr double kL2BytesPerSec = 20e12;
 // Measured on GB300: the second half's write, its transfer to the owner and the owner's
 // store are serial after the halves finish, about two tile epilogues plus a flag handoff.
-constexpr double kFixupSec = 12e-6;
+constexpr double kFixupSec = 12e-6;       // split tile combined through workspace (measured)
+constexpr double kFixupReduceSec = 3e-6;  // split tile combined by TMA reduce-add into C
 // A tile is only split in two when each half has at least this many k-blocks.
 constexpr int64_t kMinSplitIters = 4;
 
@@ -216,7 +217,7 @@ struct Split {
 // tiles split into two k-halves on two units (half a wave, plus the owner's add of the other
 // half).  Memory time assumes HBM bandwidth in proportion to the share of busy units.
 Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stages, double rate, int64_t units,
-                  int want_sk)
+                  int want_sk, double fixup_sec)
 {
     Split sp{};
     const int64_t tile_m = kTileM * cg;
@@ -246,7 +247,7 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
         const double busy_split = static_cast<double>(2 * rest) / units;
         const double t_tail_mem = (full > 0 ? bytes * full / tiles / kHbmBytesPerSec : 0.0) +
                                   bytes * rest / tiles / (kHbmBytesPerSec * busy_split);
-        const double t_sp = std::max(ew * tile_sec, t_tail_mem) + kFixupSec +
+        const double t_sp = std::max(ew * tile_sec, t_tail_mem) + fixup_sec +
                             2.0 * rest * tile_bytes / kL2BytesPerSec;
         if (want_sk == 2 || t_sp < t_dp) {
             sp.units = units;
@@ -263,9 +264,11 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
 // Choice among the compiled variants by modelled time: wave quantisation, the per-tile rate
 // of each variant, and HBM time for bandwidth-bound shapes.
 // pair_slots: co-resident CTA pairs (from the device, or sms / 2 when planning offline).
+// reduce_split: split tiles may be combined by TMA reduce-add into C (plain FP32 epilogue,
+// TMA-addressable C), the cheaper combination.
 gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int sms, int pair_slots,
                       const gemm_options *opt, const void *A, const void *B, gemm_plan *pl, bool allow_split = true,
-                      int layout = 0)
+                      int layout = 0, bool reduce_split = true)
 {
     std::memset(pl, 0, sizeof(*pl));
     const int want_cg = opt ? opt->cta_group : 0;
@@ -282,7 +285,8 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
         if (cap > 0) units = std::min<int64_t>(units, std::max<int64_t>(1, cap / c.cta_group));
         if (units < 1) continue;
         const int st = want_st ? want_st : c.stages;
-        const Split sp = model_split(M, N, K, c.cta_group, c.tile_n, st, c.rate, units, want_sk);
+        const Split sp = model_split(M, N, K, c.cta_group, c.tile_n, st, c.rate, units, want_sk,
+                                     reduce_split ? kFixupReduceSec : kFixupSec);
         if (!best || sp.time < best_sp.time) {
             best = &c;
             best_sp = sp;
@@ -349,6 +353,7 @@ tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t 
     p.workspace = nullptr;
     p.flags = nullptr;
     p.fault_inject = 0;
+    p.split_mode = 0;
     return p;
 }
 
@@ -379,6 +384,22 @@ gemm_status encode_parts(CUtensorMap *m, const float *base, int64_t rows, int ti
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// 2-D FP32 tensor map over C for split tiles combined by TMA reduce-add: boxes of 32 columns
+// (128 bytes, 128-byte swizzle, the epilogue's staging layout) by 32 rows.
+gemm_status encode_c_reduce(CUtensorMap *m, void *C, int64_t M, int64_t N, int64_t ldc)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    gemm_status st = get_encoder(&enc);
+    if (st != GEMM_OK) return st;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -436,8 +457,13 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
         return to_status(tct::launch_fill_epilogue(p, dev.sms, s));
     }
 
+    // Split tiles add into C by TMA reduce-add when the epilogue is the plain FP32 store and C
+    // is TMA-addressable (16-byte aligned base and row pitch); otherwise through workspace.
+    const bool plain = !epi || (epi->alpha == 1.0f && epi->beta == 0.0f && !epi->bias);
+    const bool reduce_ok =
+        plain && c_type == GEMM_DTYPE_F32 && reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0;
     gemm_plan pl;
-    st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), opt, A, B, &pl, true, layout);
+    st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), opt, A, B, &pl, true, layout, reduce_ok);
     if (st != GEMM_OK) return st;
 
     // Stored shapes: A is M x K, or K x M when transposed; B is K x N, or N x K.
@@ -452,7 +478,7 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
     const int64_t lda_p = round_up(a_cols, 8), ldb_p = round_up(b_cols, 8);
     const int64_t a_bytes = pl.pack_a ? round_up(a_rows * lda_p * 2, 256) : 0;
     const int64_t b_bytes = pl.pack_b ? round_up(b_rows * ldb_p * 2, 256) : 0;
-    const int64_t w_bytes = split_parts_bytes(pl), f_bytes = split_flags_bytes(pl);
+    const int64_t w_bytes = reduce_ok ? 0 : split_parts_bytes(pl), f_bytes = split_flags_bytes(pl);
     void *ws = nullptr;
     if (a_bytes + b_bytes + w_bytes + f_bytes > 0) {
         cudaMemPool_t pool = nullptr;
@@ -494,11 +520,16 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
         p.fault_inject = opt ? opt->fault_inject : 0;
         CUtensorMap tp;
         std::memset(&tp, 0, sizeof(tp));
-        if (w_bytes) {
+        if (pl.stream_k_tiles > 0) {
             uint8_t *w = static_cast<uint8_t *>(ws) + a_bytes + b_bytes;
-            p.workspace = reinterpret_cast<float *>(w);
             p.flags = reinterpret_cast<unsigned int *>(w + w_bytes);
-            st = encode_parts(&tp, p.workspace, static_cast<int64_t>(pl.stream_k_tiles) * pl.tile_m, pl.tile_n);
+            if (reduce_ok) {
+                p.split_mode = 1;
+                st = encode_c_reduce(&tp, C, M, N, ldc);
+            } else {
+                p.workspace = reinterpret_cast<float *>(w);
+                st = encode_parts(&tp, p.workspace, static_cast<int64_t>(pl.stream_k_tiles) * pl.tile_m, pl.tile_n);
+            }
         }
         if (st == GEMM_OK)
             st = to_status(tct::launch_gemm(ta, tb, tp, p, layout, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));

@@ -39,7 +39,13 @@ struct KernelParams {
     int32_t split_tiles;
     float *workspace;
     unsigned int *flags;
-    int32_t fault_inject;  // bit 0: never publish a split tile's second half (timeout test)
+    int32_t fault_inject;  // bit 0: never publish a split tile (its part, or its zeroed C rows)
+    // How split tiles are combined.  0: the second half goes through workspace and the owner
+    // adds it (any epilogue).  1 (plain FP32 epilogue, C TMA-addressable): the owner zeroes
+    // its rows of the tile in C at kernel start and raises flag[part * cta_group + rank]; both
+    // halves then add their accumulators into C with TMA reduce-add (the tensor map in the
+    // part-map slot), so C = (0 + a) + b = (0 + b) + a whichever half lands first.
+    int32_t split_mode;
 };
 
 enum WorkMode : int32_t {

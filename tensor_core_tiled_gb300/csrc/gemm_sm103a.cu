@@ -258,6 +258,46 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst 
     }
 }
 
+// One accumulator buffer added into C by TMA reduce-add (split tiles under split_mode 1):
+// each 32 x 32 block is staged in the 128-byte-swizzled layout the C tensor map names and
+// reduced into C at (row0, col0 + 32 * ch); the hardware clips boxes that reach past C.
+// `release` is called by lane 0 once every column has been read from TMEM.
+template <int BN, typename Release>
+__device__ __forceinline__ void reduce_accumulator(uint32_t t_row, const void *tmap_c, int64_t row0, int64_t col0,
+                                                   int64_t rows, int64_t cols, float *stage, int lane,
+                                                   Release release)
+{
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + ch * 32, r);
+        tmem_wait_ld();
+        if (ch == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release();
+        }
+        if (ch > 0) {  // the previous block has been read out of the staging buffer
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+        }
+        float4 *srow = reinterpret_cast<float4 *>(stage + lane * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            srow[j ^ (lane & 7)] =
+                make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
+                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        fence_proxy_async_smem();  // this lane's generic writes before the async-proxy read
+        __syncwarp();
+        const int64_t c = col0 + ch * 32;
+        if (lane == 0 && row0 < rows && c < cols) {
+            tma_reduce_add_2d(tmap_c, static_cast<int32_t>(c), static_cast<int32_t>(row0), smem_u32(stage));
+            bulk_commit_group();
+        }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+}
+
 // Waits until *flag is raised (by another CTA), bounded like the pipeline waits.
 __device__ __forceinline__ bool wait_flag(const unsigned int *flag, uint64_t limit_ns, volatile int *abort_flag)
 {
@@ -500,6 +540,38 @@ __global__ void __launch_bounds__(192, 1)
         // ------------------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         float *stage = sEpi + (warp - 2) * 32 * 32;
+        if (p.split_mode == 1 && !(p.fault_inject & 1)) {
+            // The owner of a split tile zeroes its rows of the tile in C while the first tile's
+            // k-loop runs, then raises the tile's flag for this CTA rank; both halves add into
+            // C once they see it.  (A unit owns at most one split tile.)  Fault injection skips
+            // this, so that both halves' waits run out and C keeps its old contents there.
+            WorkItem z;
+            for (int i = 0; work_item(p, unit, i, z); ++i) {
+                if (z.mode != WORK_FIXUP) continue;
+                const TileCoord c = tile_coord(z.tile, p.num_m, p.num_n, p.group_m);
+                const int64_t r0 = static_cast<int64_t>(c.m) * (Cf::BM * CG) + rank * Cf::BM + q * 32;
+                const int64_t c0 = static_cast<int64_t>(c.n) * BN;
+                float *Cz = static_cast<float *>(p.C);
+                for (int rr = 0; rr < 32 && r0 + rr < p.M; ++rr) {
+                    float *crow = Cz + (r0 + rr) * p.ldc;
+                    for (int cc = lane * 4; cc < BN; cc += 128) {
+                        const int64_t col = c0 + cc;
+                        if (col + 3 < p.N) {
+                            *reinterpret_cast<float4 *>(crow + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+                        } else {
+                            for (int e = 0; e < 4; ++e)
+                                if (col + e < p.N) crow[col + e] = 0.f;
+                        }
+                    }
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(part_bar);
+                if (warp == 2 && lane == 0 && wait_or_abort<false>(part_bar, 0u, limit, abort_flag, SITE_EPI_PARTS))
+                    flag_release_gpu(p.flags + z.part * CG + rank, 1u);
+                break;
+            }
+        }
         int it = 0;
         WorkItem w;
         for (; work_item(p, unit, it, w); ++it) {
@@ -516,6 +588,24 @@ __global__ void __launch_bounds__(192, 1)
                       p.c_type, p.epi != 0, p.alpha, p.beta, p.bias,            p.bias_type};
             int64_t row_base = static_cast<int64_t>(c.m) * (Cf::BM * CG) + lane_rows;
             int64_t col_base = static_cast<int64_t>(c.n) * BN;
+            const uint32_t t_row0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
+            if (p.split_mode == 1 && w.mode != WORK_STORE) {
+                // Either half of a split tile: add the accumulator into C, zeroed by the owner.
+                ok = wait_flag(p.flags + w.part * CG + rank, limit, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                fence_proxy_async_all();  // the owner's zeros (generic writes) before the reduce
+                if constexpr (kPair) {
+                    const uint32_t te = map_to_cta(tempty_bar(b), 0);
+                    reduce_accumulator<BN>(t_row0, &tmP, row_base, col_base, p.M, p.N, stage, lane,
+                                           [&] { mbar_arrive_cluster(te); });
+                } else {
+                    const uint32_t te = tempty_bar(b);
+                    reduce_accumulator<BN>(t_row0, &tmP, row_base, col_base, p.M, p.N, stage, lane,
+                                           [&] { mbar_arrive(te); });
+                }
+                continue;
+            }
             if (w.mode == WORK_PARTIAL) {
                 // second half of a split tile for its owner: the whole tile, tile-local rows
                 d = TileDst{p.workspace + w.part * kTileElems, BN, Cf::BM * CG, BN, true, false, nullptr,

@@ -165,6 +165,25 @@ __device__ __forceinline__ void tmem_wait_ld()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 2-D TMA reduce-add of a shared-memory box into global memory (element type and box from the
+// tensor map; boxes reaching past the tensor are clipped).  Completion is tracked by the
+// thread's bulk-async groups.
+__device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, int32_t c0, int32_t c1, uint32_t src)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until the shared-memory sources of this thread's committed bulk groups have been read.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Waits until this thread's committed bulk groups have completed (writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Bulk (non-tensor) copy of `bytes` contiguous bytes from global memory into this CTA's
 // shared memory, counted on the mbarrier `bar`.  Both addresses must be 16-byte aligned
 // and `bytes` a multiple of 16.

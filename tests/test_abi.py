@@ -149,10 +149,14 @@ def test_planner_on_gb300_shapes(tct_lib):
     assert p["stream_k_tiles"] == 1024 - 13 * 76
     assert p["effective_waves"] == pytest.approx(13.5)
     assert p["pack_a"] == 0 and p["pack_b"] == 0
-    # 4096^3: splitting the 28 tail tiles would cost more than the half tile it saves (the
-    # k-loop is short), so 4 whole waves; with 4x the k-loop the split pays
+    # 4096^3: 256 tiles = 3 whole waves + 28; the 28 tail tiles split into k-halves on 56 pairs
+    # (both halves add into C by TMA reduce-add, a few microseconds), 3.5 waves of time
     p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms)
-    assert (p["cta_group"], p["tile_n"], p["waves"], p["stream_k_tiles"]) == (2, 256, 4, 0)
+    assert (p["cta_group"], p["tile_n"], p["waves"], p["stream_k_tiles"]) == (2, 256, 4, 28)
+    assert p["effective_waves"] == 3.5
+    # 6144^3: 576 = 7 waves + 44 tiles, too many to halve onto 76 pairs: 8 whole waves
+    p = tct.gemm_f16_f32_plan(6144, 6144, 6144, num_sms=sms)
+    assert (p["waves"], p["stream_k_tiles"]) == (8, 0)
     p = tct.gemm_f16_f32_plan(4096, 4096, 16384, num_sms=sms)
     assert p["stream_k_tiles"] == 256 - 3 * 76 and p["effective_waves"] == 3.5
     p = tct.gemm_f16_f32_plan(4096, 4096, 16384, num_sms=sms, stream_k=1)

@@ -3,9 +3,11 @@
 Every pipeline and cross-CTA wait in the kernel is bounded by `timeout_ms`; when one runs
 out, the kernel records GEMM_ERR_DEVICE_TIMEOUT in a device word, winds down (drains its
 own copies and MMAs, frees tensor memory) and returns.  The test injects the failure from
-the host: with fault_inject bit 0 the unit computing the second k-half of each split tile
-never publishes it, so each owner's wait for it -- a flag nothing sets -- runs out.  The
-host reads the status, and the same context then computes a correct product.
+the host: with fault_inject bit 0 a split tile is never published -- with the plain FP32
+epilogue its owner never zeroes and flags its rows of C, so both halves' waits to add into
+C run out; with an epilogue the second half's unit never publishes its part, so the
+owner's wait runs out.  Either way the wait is on a flag nothing sets.  The host reads the
+status, and the same context then computes a correct product.
 """
 import time
 
@@ -35,7 +37,8 @@ def _dev16(x):
 
 @pytest.mark.parametrize("opts", [dict(cta_group=2, tile_n=256, max_ctas=150),
                                   dict(cta_group=1, tile_n=256, max_ctas=140)])
-def test_unpublished_part_times_out_and_context_survives(opts):
+@pytest.mark.parametrize("through_workspace", [False, True])
+def test_unpublished_part_times_out_and_context_survives(opts, through_workspace):
     M, N, K = 2000, 3000, 1000
     plan = tct.gemm_f16_f32_plan(M, N, K, stream_k=2, **opts)
     assert 0 < plan["stream_k_tiles"] < plan["tiles"]
@@ -45,7 +48,10 @@ def test_unpublished_part_times_out_and_context_survives(opts):
     assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
     C = torch.full((M, N), float("nan"), device="cuda")
     t0 = time.time()
-    tct.matmul(dA, dB, C, stream_k=2, timeout_ms=50, fault_inject=1, **opts)
+    if through_workspace:  # a bias (of zeros) makes the epilogue non-plain: workspace combination
+        tct.gemm(dA, dB, C, bias=torch.zeros(N, device="cuda"), stream_k=2, timeout_ms=50, fault_inject=1, **opts)
+    else:
+        tct.matmul(dA, dB, C, stream_k=2, timeout_ms=50, fault_inject=1, **opts)
     status = tct.gemm_f16_f32_get_error()  # synchronises
     elapsed = time.time() - t0
     assert status == tct.GEMM_ERR_DEVICE_TIMEOUT
