@@ -209,6 +209,7 @@ double wave_util(int64_t M, int64_t N, int64_t tm, int64_t tn, int64_t slots, in
 struct Split {
     int64_t units, tiles, waves, dp_tiles, split_tiles;
     double time, eff_waves;
+    double compute;  // the compute part of `time` (tile time x effective waves)
 };
 
 // Work split and modelled time of one variant.  Whole waves of tiles go data-parallel; the
@@ -239,6 +240,7 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
     sp.split_tiles = 0;
     sp.time = t_dp;
     sp.eff_waves = static_cast<double>(waves);
+    sp.compute = waves * tile_sec;
     const int64_t full = tiles / units, rest = tiles - full * units;
     const bool can_split = rest > 0 && 2 * rest <= units && kb / 2 >= (want_sk == 2 ? 1 : kMinSplitIters) &&
                            want_sk != 1 && tct::variant_split_ok(cg, tile_n, stages);
@@ -256,6 +258,7 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
             sp.split_tiles = rest;
             sp.time = t_sp;
             sp.eff_waves = ew;
+            sp.compute = ew * tile_sec;
         }
     }
     return sp;
@@ -287,7 +290,12 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
         const int st = want_st ? want_st : c.stages;
         const Split sp = model_split(M, N, K, c.cta_group, c.tile_n, st, c.rate, units, want_sk,
                                      reduce_split ? kFixupReduceSec : kFixupSec);
-        if (!best || sp.time < best_sp.time) {
+        // Within 1% (e.g. every candidate bound by the same HBM time) the one with less compute
+        // time wins: it has the most slack (measured: 1-CTA 128x128 tiles stream the skinny
+        // 128 x 16384 x 16384 shape 5% faster than CTA-pair 256x256 tiles, half of whose rows
+        // are empty).
+        const bool tie = best && sp.time <= best_sp.time * 1.01 && best_sp.time <= sp.time * 1.01;
+        if (!best || (tie ? sp.compute < best_sp.compute : sp.time < best_sp.time)) {
             best = &c;
             best_sp = sp;
         }

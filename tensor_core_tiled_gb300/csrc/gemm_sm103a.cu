@@ -673,8 +673,12 @@ __global__ void __launch_bounds__(192, 1)
 
 // Row copy into buffers whose rows start on 16-byte boundaries (TMA's stride rule), for up
 // to two operands in one launch: blockIdx.y < rows0 copies row blockIdx.y of operand 0, the
-// rest copy rows of operand 1.  Each thread moves 8 consecutive elements of one row: 8
-// two-byte loads (the source rows may start anywhere) and one 16-byte store.
+// rest copy rows of operand 1.  Each thread moves 8 consecutive elements (16 bytes) of one
+// row.  A source row may start on any 2-byte boundary, so the 16 bytes generally straddle
+// two aligned 16-byte blocks: both are loaded whole and the bytes realigned with funnel
+// shifts.  Each of the two blocks holds at least one byte of the 8 elements, so no load
+// reaches outside the 16-byte blocks the row occupies.  A row's last, partial group of
+// elements is copied element by element.
 struct PackJob {
     const uint16_t *src;
     int64_t ld_src;
@@ -693,12 +697,21 @@ __global__ void pack_rows_f16(const PackJob j0, const PackJob j1)
     const uint16_t *s = j.src + r * j.ld_src + c8;
     uint16_t *d = j.dst + r * j.ld_dst + c8;
     if (c8 + 8 <= j.cols) {
-        uint4 v;
-        v.x = static_cast<uint32_t>(s[0]) | (static_cast<uint32_t>(s[1]) << 16);
-        v.y = static_cast<uint32_t>(s[2]) | (static_cast<uint32_t>(s[3]) << 16);
-        v.z = static_cast<uint32_t>(s[4]) | (static_cast<uint32_t>(s[5]) << 16);
-        v.w = static_cast<uint32_t>(s[6]) | (static_cast<uint32_t>(s[7]) << 16);
-        *reinterpret_cast<uint4 *>(d) = v;
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(s);
+        const uint32_t off = static_cast<uint32_t>(addr & 15u);  // 0, 2, ..., 14
+        const uint4 *blk = reinterpret_cast<const uint4 *>(addr - off);
+        const uint4 lo = __ldg(blk);
+        const uint4 hi = off ? __ldg(blk + 1) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        const uint32_t q = off >> 2, sh = (off & 3u) * 8u;
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t a = q == 0 ? w[i] : q == 1 ? w[i + 1] : q == 2 ? w[i + 2] : w[i + 3];
+            const uint32_t b = q == 0 ? w[i + 1] : q == 1 ? w[i + 2] : q == 2 ? w[i + 3] : w[i + 4];
+            o[i] = __funnelshift_r(a, b, sh);
+        }
+        *reinterpret_cast<uint4 *>(d) = make_uint4(o[0], o[1], o[2], o[3]);
     } else {
         for (int64_t i = 0; i < j.cols - c8; ++i) d[i] = s[i];
     }
