@@ -168,8 +168,10 @@ typedef struct gemm_plan {
     int32_t pack_a, pack_b;         /* 1 if the operand would be repacked first       */
     int32_t cta_group;              /* CTAs sharing one tile (1 or 2)                 */
     int32_t units;                  /* persistent work units (CTAs or CTA pairs)      */
-    int32_t stream_k_tiles;         /* tiles whose k-loop is split in two halves      */
+    int32_t stream_k_tiles;         /* tiles whose k-loop is split in two parts       */
     double effective_waves;         /* tile-times per unit: whole waves + split share */
+    int32_t split_kb;               /* k-block where a split tile's second part starts */
+    int32_t split_parts_per_unit;   /* second parts a helper unit takes in turn (>= 1) */
 } gemm_plan;
 
 TCT_API gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,

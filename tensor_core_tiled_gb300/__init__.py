@@ -59,7 +59,8 @@ class GemmPlan(ctypes.Structure):
                 ("tiles", ctypes.c_int64), ("waves", ctypes.c_int64), ("wave_efficiency", ctypes.c_double),
                 ("smem_bytes", ctypes.c_int32), ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32),
                 ("cta_group", ctypes.c_int32), ("units", ctypes.c_int32), ("stream_k_tiles", ctypes.c_int32),
-                ("effective_waves", ctypes.c_double)]
+                ("effective_waves", ctypes.c_double), ("split_kb", ctypes.c_int32),
+                ("split_parts_per_unit", ctypes.c_int32)]
 
 
 class GemmEpilogue(ctypes.Structure):

@@ -208,17 +208,21 @@ double wave_util(int64_t M, int64_t N, int64_t tm, int64_t tn, int64_t slots, in
 
 struct Split {
     int64_t units, tiles, waves, dp_tiles, split_tiles;
+    int64_t split_kb, parts;  // owner's k-blocks of a split tile; second parts per helper
     double time, eff_waves;
     double compute;  // the compute part of `time` (tile time x effective waves)
 };
 
 // Work split and modelled time of one variant.  Whole waves of tiles go data-parallel; the
 // last, partial wave either runs as whole tiles (a full extra wave of time, "02_gpu_execution
-// _model.py" part 5) or, when at most half the units would be busy in it, has each of its
-// tiles split into two k-halves on two units (half a wave, plus the owner's add of the other
-// half).  Memory time assumes HBM bandwidth in proportion to the share of busy units.
+// _model.py" part 5) or has each of its `rest` tiles split into two k-parts: the owner unit
+// takes the first split_kb k-blocks, and the units - rest other units ("helpers") each take
+// the second parts of p = ceil(rest / helpers) tiles in turn, split_kb balancing the owner's
+// split_kb against a helper's p * (kb - split_kb).  p = 1 is the even halving (at most half
+// the units in the last wave); larger p needs the reduce-add combination (workspace holds
+// one part per helper).  Memory time assumes HBM bandwidth in proportion to busy units.
 Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stages, double rate, int64_t units,
-                  int want_sk, double fixup_sec)
+                  int want_sk, double fixup_sec, bool reduce_split)
 {
     Split sp{};
     const int64_t tile_m = kTileM * cg;
@@ -242,20 +246,29 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
     sp.eff_waves = static_cast<double>(waves);
     sp.compute = waves * tile_sec;
     const int64_t full = tiles / units, rest = tiles - full * units;
-    const bool can_split = rest > 0 && 2 * rest <= units && kb / 2 >= (want_sk == 2 ? 1 : kMinSplitIters) &&
-                           want_sk != 1 && tct::variant_split_ok(cg, tile_n, stages);
+    const int64_t helpers = units - rest;
+    const int64_t p = helpers > 0 ? tct::ceil_div(rest, helpers) : 0;
+    const int64_t kb_o = p > 0 ? tct::ceil_div(p * kb, p + 1) : 0;  // owner part >= a helper's total
+    const int64_t min_iters = want_sk == 2 ? 1 : kMinSplitIters;
+    const bool can_split = rest > 0 && helpers > 0 && (reduce_split || p == 1) && kb - kb_o >= 1 &&
+                           kb_o >= min_iters && want_sk != 1 && tct::variant_split_ok(cg, tile_n, stages);
     if (can_split) {
-        const double ew = full + 0.5;
-        const double busy_split = static_cast<double>(2 * rest) / units;
+        const double t_tail = static_cast<double>(std::max(kb_o, p * (kb - kb_o))) / kb;
+        const double ew = full + t_tail;
+        const double busy_split = static_cast<double>(rest + std::min(helpers, rest)) / units;
         const double t_tail_mem = (full > 0 ? bytes * full / tiles / kHbmBytesPerSec : 0.0) +
                                   bytes * rest / tiles / (kHbmBytesPerSec * busy_split);
-        const double t_sp = std::max(ew * tile_sec, t_tail_mem) + fixup_sec +
+        // a helper combines each of its p parts (measured: 9 short parts per helper at 3072^3
+        // cost more than the whole extra wave they replace)
+        const double t_sp = std::max(ew * tile_sec, t_tail_mem) + fixup_sec * p +
                             2.0 * rest * tile_bytes / kL2BytesPerSec;
         if (want_sk == 2 || t_sp < t_dp) {
             sp.units = units;
             sp.waves = tct::ceil_div(tiles, units);
             sp.dp_tiles = full * units;
             sp.split_tiles = rest;
+            sp.split_kb = kb_o;
+            sp.parts = p;
             sp.time = t_sp;
             sp.eff_waves = ew;
             sp.compute = ew * tile_sec;
@@ -289,7 +302,7 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
         if (units < 1) continue;
         const int st = want_st ? want_st : c.stages;
         const Split sp = model_split(M, N, K, c.cta_group, c.tile_n, st, c.rate, units, want_sk,
-                                     reduce_split ? kFixupReduceSec : kFixupSec);
+                                     reduce_split ? kFixupReduceSec : kFixupSec, reduce_split);
         // Within 1% (e.g. every candidate bound by the same HBM time) the one with less compute
         // time wins: it has the most slack (measured: 1-CTA 128x128 tiles stream the skinny
         // 128 x 16384 x 16384 shape 5% faster than CTA-pair 256x256 tiles, half of whose rows
@@ -323,6 +336,8 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
     pl->units = static_cast<int32_t>(best_sp.units);
     pl->stream_k_tiles = static_cast<int32_t>(best_sp.split_tiles);
     pl->effective_waves = best_sp.eff_waves;
+    pl->split_kb = static_cast<int32_t>(best_sp.split_kb);
+    pl->split_parts_per_unit = static_cast<int32_t>(best_sp.parts);
     return GEMM_OK;
 }
 
@@ -358,6 +373,7 @@ tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t 
     p.units = pl.units;
     p.dp_tiles = static_cast<int32_t>(pl.tiles - pl.stream_k_tiles);
     p.split_tiles = pl.stream_k_tiles;
+    p.split_kb = pl.split_kb;
     p.workspace = nullptr;
     p.flags = nullptr;
     p.fault_inject = 0;

@@ -37,6 +37,7 @@ struct KernelParams {
     int32_t units;
     int32_t dp_tiles;
     int32_t split_tiles;
+    int32_t split_kb;  // first k-block of a split tile's second part (the owner takes [0, split_kb))
     float *workspace;
     unsigned int *flags;
     int32_t fault_inject;  // bit 0: never publish a split tile (its part, or its zeroed C rows)
@@ -78,20 +79,27 @@ inline bool work_item(const KernelParams &p, int32_t u, int32_t idx, WorkItem &i
         it.mode = WORK_STORE;
         return true;
     }
-    if (idx != waves || u >= 2 * p.split_tiles) return false;
-    const int32_t j = u < p.split_tiles ? u : u - p.split_tiles;
-    const int32_t half = p.num_kb / 2;
+    // Split tail tile j = dp_tiles + j' (j' < split_tiles): unit j' owns k-blocks
+    // [0, split_kb); the units_left = units - split_tiles other units are helpers, helper h
+    // taking [split_kb, num_kb) of tails h, h + units_left, h + 2 * units_left, ... in turn.
+    if (p.split_tiles <= 0) return false;
+    if (u < p.split_tiles) {
+        if (idx != waves) return false;
+        it.tile = p.dp_tiles + u;
+        it.part = u;
+        it.kb0 = 0;
+        it.kb1 = p.split_kb;
+        it.mode = WORK_FIXUP;
+        return true;
+    }
+    const int32_t helpers = p.units - p.split_tiles;
+    const int32_t j = (u - p.split_tiles) + (idx - waves) * helpers;
+    if (j >= p.split_tiles) return false;
     it.tile = p.dp_tiles + j;
     it.part = j;
-    if (u < p.split_tiles) {
-        it.kb0 = 0;
-        it.kb1 = half;
-        it.mode = WORK_FIXUP;
-    } else {
-        it.kb0 = half;
-        it.kb1 = p.num_kb;
-        it.mode = WORK_PARTIAL;
-    }
+    it.kb0 = p.split_kb;
+    it.kb1 = p.num_kb;
+    it.mode = WORK_PARTIAL;
     return true;
 }
 

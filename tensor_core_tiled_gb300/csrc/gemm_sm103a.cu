@@ -644,7 +644,8 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (w.mode == WORK_PARTIAL) {
                 // Publish this CTA's rows of the part to the owner once all four warps have
-                // written theirs (a unit writes at most one part, so the barrier's first phase).
+                // written theirs (through workspace a helper writes one part at most, so the
+                // barrier's first phase).
                 __threadfence();
                 fence_proxy_async_all();
                 __syncwarp();

@@ -154,9 +154,11 @@ def test_planner_on_gb300_shapes(tct_lib):
     p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms)
     assert (p["cta_group"], p["tile_n"], p["waves"], p["stream_k_tiles"]) == (2, 256, 4, 28)
     assert p["effective_waves"] == 3.5
-    # 6144^3: 576 = 7 waves + 44 tiles, too many to halve onto 76 pairs: 8 whole waves
+    # 6144^3: 576 = 7 waves + 44 tiles on 76 pairs: 32 helpers take the second parts of 2
+    # tail tiles each, so the owners keep ceil(2 * 96 / 3) = 64 of the 96 k-blocks
     p = tct.gemm_f16_f32_plan(6144, 6144, 6144, num_sms=sms)
-    assert (p["waves"], p["stream_k_tiles"]) == (8, 0)
+    assert (p["waves"], p["stream_k_tiles"], p["split_kb"], p["split_parts_per_unit"]) == (8, 44, 64, 2)
+    assert p["effective_waves"] == pytest.approx(7 + 64 / 96)
     p = tct.gemm_f16_f32_plan(4096, 4096, 16384, num_sms=sms)
     assert p["stream_k_tiles"] == 256 - 3 * 76 and p["effective_waves"] == 3.5
     p = tct.gemm_f16_f32_plan(4096, 4096, 16384, num_sms=sms, stream_k=1)
@@ -190,11 +192,15 @@ def test_planner_on_gb300_shapes(tct_lib):
     ((128, 16384, 16384), {}), ((1000, 1100, 700), {"stream_k": 2}), ((777, 1500, 515), {"stream_k": 2, "cta_group": 1}),
     ((300, 200, 150), {"stream_k": 2}), ((1, 1000, 640), {"stream_k": 2, "cta_group": 1, "tile_n": 128}),
     ((2000, 3000, 5000), {"stream_k": 2, "max_ctas": 50}), ((1792, 1792, 1792), {}), ((6144, 6144, 6144), {}),
+    ((3072, 3072, 3072), {"stream_k": 2}), ((2048, 2048, 2048), {"stream_k": 2}), ((1792, 1792, 1792), {"stream_k": 2}),
+    ((5000, 7000, 3000), {"stream_k": 2, "cta_group": 1, "tile_n": 128}),
 ])
 def test_work_items_cover_every_k_block_once(tct_lib, shape, opts):
     """The library's own work split: each (tile, k-block) pair of the plan belongs to exactly
-    one work item of one unit; every split tile has exactly one owner (first k-half, mode 1)
-    and one writer of its second half (mode 2), sharing one workspace slot."""
+    one work item of one unit; every split tile has exactly one owner (its first split_kb
+    k-blocks, mode 1) and one helper for the rest (mode 2), sharing one part slot; a helper
+    takes split_parts_per_unit second parts at most, and no unit's k-blocks exceed the
+    owner's share of the tail."""
     M, N, K = shape
     sms = 152
     p = tct.gemm_f16_f32_plan(M, N, K, num_sms=sms, **opts)
@@ -226,3 +232,9 @@ def test_work_items_cover_every_k_block_once(tct_lib, shape, opts):
         wu, wpart, wkb0, wkb1 = writers[tile]
         assert wu != u and wpart == part and kb0 == 0 and kb1 == wkb0 and wkb1 == kb
     assert sorted(v[1] for v in owners.values()) == list(range(p["stream_k_tiles"]))
+    if p["stream_k_tiles"]:
+        per_helper = {}
+        for tile, (wu, wpart, wkb0, wkb1) in writers.items():
+            assert wkb0 == p["split_kb"]
+            per_helper[wu] = per_helper.get(wu, 0) + (wkb1 - wkb0)
+        assert max(per_helper.values()) <= p["split_parts_per_unit"] * (kb - p["split_kb"]) <= p["split_kb"]

@@ -237,14 +237,19 @@ STREAM_K_CASES = [
     ((2000, 3000, 5000), dict(stream_k=2, cta_group=1, tile_n=256, max_ctas=140)),
     ((1, 1000, 640), dict(stream_k=2, cta_group=1, tile_n=128)),
     ((4096, 4096, 1000), dict(stream_k=2, cta_group=2, tile_n=256)),
+    # tails larger than half the units: helpers take 2, 6 and 9 second parts in turn
+    ((6144, 6144, 1000), dict(stream_k=2)),
+    ((2048, 2048, 2048), dict(stream_k=2)),
+    ((3072, 3072, 1024), dict(stream_k=2)),
+    ((1500, 5000, 777), dict(stream_k=2, cta_group=1, tile_n=128)),
 ]
 
 
 @pytest.mark.parametrize("shape,opts", STREAM_K_CASES)
 def test_stream_k_split(shape, opts):
-    """Tiles whose k-loop is split into two halves on two units: the second half through the
-    workspace and the owner's add give the oracle's result, bit-exact on integer inputs, and
-    the same bits on every run."""
+    """Tiles whose k-loop is split in two parts on two units (both parts added into C by TMA
+    reduce-add; a helper may take several tiles' second parts in turn) give the oracle's
+    result, bit-exact on integer inputs, and the same bits on every run."""
     M, N, K = shape
     plan = tct.gemm_f16_f32_plan(M, N, K, **opts)
     assert plan["stream_k_tiles"] > 0
