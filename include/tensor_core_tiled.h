@@ -9,17 +9,18 @@
  * skipped).  All matrices are row-major with explicit leading dimensions.
  *
  * Conventions shared by every entry point below:
- *   - Pointers A, B, C are device-accessible addresses (cudaMalloc, torch CUDA tensors).
- *     The caller owns all memory.  C must not overlap A or B.
+ *   - Pointers A, B, C are device-accessible addresses (cudaMalloc, torch CUDA tensors),
+ *     except in the *_host entry points, which take host memory.  The caller owns all
+ *     memory.  C must not overlap A or B.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All
  *     work is enqueued on it; no call synchronises the host.
- *   - C is overwritten (no beta term).  M == 0 or N == 0 is a no-op.  K == 0 writes zeros
- *     (the empty sum) into the M x N block of C.
+ *   - C is overwritten (gemm_ex adds the beta * C term).  M == 0 or N == 0 is a no-op.
+ *     K == 0 writes zeros (the empty sum) into the M x N block of C.
  *   - Errors in the arguments are reported immediately through the return value and
  *     nothing is enqueued.  Device-side errors (a pipeline wait that exceeded its time
  *     limit) are recorded in a per-device error word read by gemm_f16_f32_get_error().
- *   - Not thread-safe against concurrent first calls on the same device (the first call
- *     per device caches device properties).
+ *   - Calls may come from several host threads: per-device state (properties, memory
+ *     pool, copy streams of the *_host calls) is created once under a lock.
  */
 #ifndef TENSOR_CORE_TILED_H
 #define TENSOR_CORE_TILED_H
@@ -53,10 +54,10 @@ typedef enum gemm_status {
  * Any alignment and any leading dimension are accepted.  When lda or ldb is not a
  * multiple of 8 elements, or A or B is not 16-byte aligned, the operand is first copied
  * on `stream` into a stream-ordered temporary whose rows are 16-byte aligned.  Temporaries
- * (these copies and the stream-K partial tiles, see gemm_options) come from a library-owned
- * stream-ordered memory pool per device (cudaMallocFromPoolAsync / cudaFreeAsync on
- * `stream`) that keeps freed memory for reuse until the process exits.  The result does
- * not depend on which path ran.
+ * (these copies, and the flags -- with an epilogue also the parts -- of split tiles, see
+ * gemm_options) come from a library-owned stream-ordered memory pool per device
+ * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`) that keeps freed memory for reuse
+ * until the process exits.  The result does not depend on which path ran.
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (negative or oversized dims, lda < K, ldb < N,
  * ldc < N, NULL pointer with a non-empty extent), GEMM_ERR_UNSUPPORTED_DEVICE or
  * GEMM_ERR_CUDA.
@@ -75,15 +76,20 @@ TCT_API gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t
  *   timeout_ms: limit on any single device pipeline wait (default 2000 ms).
  *   cta_group : 1 = one CTA per 128-row tile, 2 = a CTA pair per 256-row tile.
  *   stream_k  : 1 = whole tiles only; 2 = split each tile of the last, partial wave into
- *               two k-halves on two units whenever that wave fills at most half the units
- *               (the second half goes through a stream-ordered workspace and is added by the
- *               first half's unit, always in the same order, so results are reproducible);
- *               0 = let the planner decide.
- *   fault_inject: test hook for the device-side timeout path; 0 in normal use.  Bit 0: the
- *               unit computing the second k-half of a split tile never publishes it, so the
- *               tile's owner waits until timeout_ms runs out, records
- *               GEMM_ERR_DEVICE_TIMEOUT (read by gemm_f16_f32_get_error) and returns without
- *               storing that tile.  Nothing faults, traps or hangs; later calls are unaffected.
+ *               two k-parts: its owner unit takes the first split_kb k-blocks and one of the
+ *               units left over takes the rest (a helper may take several tiles' second
+ *               parts in turn; see gemm_plan).  With the plain FP32 epilogue and a C whose
+ *               base and row pitch are 16-byte multiples, the owner zeroes the tile in C and
+ *               both parts are added into it by TMA reduce-add; otherwise the second part goes
+ *               through a stream-ordered workspace and the owner adds it.  Every tile has two
+ *               contributions, so the sum does not depend on their order and results are
+ *               reproducible.  0 = let the planner decide.
+ *   fault_inject: test hook for the device-side timeout path; 0 in normal use.  Bit 0: split
+ *               tiles are never published (the owner neither zeroes nor flags its tile, or
+ *               the helper never flags its part), so the waits for them run until timeout_ms,
+ *               record GEMM_ERR_DEVICE_TIMEOUT (read by gemm_f16_f32_get_error) and return
+ *               without storing those tiles.  Nothing faults, traps or hangs; later calls are
+ *               unaffected.
  */
 typedef struct gemm_options {
     int32_t group_m;
@@ -189,9 +195,9 @@ TCT_API gemm_status gemm_tile_coord(int64_t t, int64_t num_m, int64_t num_n, int
 /*
  * One work item of a persistent unit (a CTA, or a CTA pair when cta_group is 2): k-blocks
  * [kb0, kb1) of linear tile `tile`.  mode 0: store the tile to C.  A tile of the last,
- * partial wave may be split into two k-halves: mode 1 (its owner, the first half) adds the
- * second half, read from workspace slot `part`, then stores to C; mode 2 writes the second
- * half to slot `part` for the owner.
+ * partial wave may be split into two k-parts: mode 1 is its owner (k-blocks [0, split_kb)),
+ * mode 2 the helper computing the rest; `part` numbers the split tile (its flag, and its
+ * workspace slot when the parts are combined through workspace).
  */
 typedef struct gemm_work {
     int32_t tile, kb0, kb1;
@@ -244,7 +250,9 @@ TCT_API gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float *C,
 /*
  * softmax_rows_f32 -- Y[i][j] = exp(X[i][j] - max_k X[i][k]) / sum_k exp(X[i][k] - max_k X[i][k])
  * for every row of an M x N FP32 matrix: the fused row softmax of "06_triton_style.py"
- * demo 3 (one read of X and one write of Y; rows longer than 51200 elements are read twice).
+ * demo 3: one read of X and one write of Y, except for rows too long to stage on chip
+ * (beyond 393216 columns when X and Y rows start on 16-byte boundaries, beyond 51200
+ * otherwise), which are read twice.
  *   X, Y : FP32 device pointers, row-major, leading dimensions ldx, ldy >= N, 4-byte
  *          aligned; Y may be X itself (ldy == ldx), other overlaps are undefined.
  * exp(-inf) = 0; a row holding a NaN, whose maximum is +inf, or whose entries are all -inf
