@@ -528,6 +528,79 @@ def run_configs(args):
                 "l2_flushed": fits, "repack": bool(pl["pack_a"] or pl["pack_b"])}
         print(json.dumps(line), flush=True)
         del A, B, C
+    # operand storage and type at 8192^3: the four layouts of gemm_f32acc, FP16 then BF16
+    n = 8192
+    for dt in (torch.float16, torch.bfloat16):
+        g = torch.Generator(device=dev).manual_seed(0)
+        A = torch.randn(n, n, device=dev, generator=g).to(dt)
+        B = torch.randn(n, n, device=dev, generator=g).to(dt)
+        At, Bt = A.t().contiguous(), B.t().contiguous()
+        C = torch.empty(n, n, device=dev)
+        for name, a, b in (("NN", A, B), ("TN", At.t(), B), ("NT", A, Bt.t()), ("TT", At.t(), Bt.t())):
+            for _ in range(3):
+                tct.matmul(a, b, C)
+            reps = max(5, min(args.steps, 30))
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for e0, e1 in pairs:
+                e0.record()
+                tct.matmul(a, b, C)
+                e1.record()
+            torch.cuda.synchronize()
+            ms = statistics.median([e0.elapsed_time(e1) for e0, e1 in pairs])
+            print(json.dumps({"workload": f"layout {name} {str(dt).split('.')[-1]} {n}^3", "us": ms * 1e3,
+                              "tflops": 2 * n ** 3 / ms / 1e9, "frac_of_burst": 2 * n ** 3 / ms / 1e9 / peak_burst}),
+                  flush=True)
+        del A, B, At, Bt, C
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    return 0
+
+
+# Row-length sweep of the softmax: (M, N, leading dimension), 2^26 elements (256 MiB each
+# way, above L2) unless stated; the last rows are not 16-byte aligned (ld = N + 1).
+SOFTMAX_CONFIGS = [(4096, 1024, 1024)] + [((1 << 26) // n, n, n) for n in (
+    128, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072, 262144, 1 << 20)] + [
+    ((1 << 26) // 1000, 1000, 1001), ((1 << 26) // 20000, 20000, 20001)]
+
+
+def run_softmax_configs(args):
+    """Every softmax shape: median device time over launches (L2 flushed before each), GB/s of
+    algorithmic traffic (read + write MN floats) and its fraction of the HBM copy peak."""
+    import torch
+
+    import tensor_core_tiled_gb300 as tct
+    from tensor_core_tiled_gb300 import build as lib_build
+
+    lib_build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peak, _ = hbm_peak()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    for M, N, ld in SOFTMAX_CONFIGS:
+        g = torch.Generator(device=dev).manual_seed(0)
+        X = torch.randn(M * ld, device=dev, generator=g)
+        Y = torch.empty_like(X)
+
+        def launch():
+            st = tct.softmax_rows_f32(X.data_ptr(), Y.data_ptr(), M, N, ld, ld, sp)
+            if st:
+                raise tct.GemmError(st, "softmax_rows_f32")
+
+        for _ in range(3):
+            launch()
+        reps = max(5, min(args.steps, 30))
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for e0, e1 in pairs:
+            flush.fill_(1.0)
+            e0.record()
+            launch()
+            e1.record()
+        torch.cuda.synchronize()
+        ms = statistics.median([e0.elapsed_time(e1) for e0, e1 in pairs])
+        gbs = 8.0 * M * N / ms / 1e6
+        print(json.dumps({"workload": f"softmax {M}x{N}" + (f" (ld {ld}, rows not 16-byte aligned)" if ld != N else ""),
+                          "M": M, "N": N, "ld": ld, "us": ms * 1e3, "gbs": gbs, "frac_of_hbm": gbs / peak}), flush=True)
+        del X, Y
     assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
     return 0
 
@@ -750,7 +823,9 @@ def run_softmax(args):
 def main():
     args = parse()
     if args.workload == "softmax":
-        return run_softmax_reference(args) if args.impl == "reference" else run_softmax(args)
+        if args.impl == "reference":
+            return run_softmax_reference(args)
+        return run_softmax_configs(args) if args.configs else run_softmax(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.configs:
