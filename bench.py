@@ -438,7 +438,7 @@ def run_ours(args):
                          "kernel_ms_mean": mean_launch, "kernel_ms_min": min(launch_ms)},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(dA.numel() * 2 + dB.numel() * 2),
                     "d2h_bytes_per_step": int(dC.numel() * 4), "steps": e2e_steps, "ms_per_step": e2e_ms,
-                    "api": "gemm_f16_f32_host (pinned host buffers; row blocks pipelined over H2D, GEMM, D2H)"},
+                    "api": "gemm_f16_f32_host (pinned host buffers; 4x4 blocks pipelined over H2D, GEMM, D2H)"},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "secondary": {"workload": f"gemm_f16_f32 {m2}x{n2}x{k2}, seed 2, L2 flushed before each launch",

@@ -264,9 +264,10 @@ TCT_API gemm_status softmax_rows_f32(const float *X, float *Y, int64_t M, int64_
 
 /*
  * gemm_f16_f32_host -- gemm_f16_f32 with A, B and C in host memory (same layouts, leading
- * dimensions and conventions).  B is copied to the device first; A then follows in row blocks
- * (8 blocks of whole 256-row tiles), each block is multiplied on `stream` as soon as its rows
- * have arrived, and its rows of C are copied back while later blocks are still in flight, so
+ * dimensions and conventions).  A is cut into up to 4 row blocks and B into up to 4 column
+ * blocks (whole 256-wide tiles); they are copied to the device interleaved (A0, B0, B1, A1,
+ * A2, B2, ...), each block of C is multiplied on `stream` as soon as its row block of A and
+ * column block of B have arrived, and copied back while later blocks are still in flight, so
  * the two copy directions and the tensor-core work overlap.  The copies run on two library
  * streams; the device copies of A, B and C come from the library's stream-ordered pool.  Host
  * memory should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to be

@@ -811,8 +811,9 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
 
 namespace {
 
-constexpr int kHostChunks = 8;        // row blocks a host-buffer call is split into
-constexpr int64_t kHostChunkAlign = 256;  // GEMM row blocks: whole CTA-pair tiles
+constexpr int kHostChunks = 8;        // row blocks of the host-buffer softmax
+constexpr int kHostGemmBlocks = 4;    // row blocks of A and column blocks of B in the host GEMM
+constexpr int64_t kHostChunkAlign = 256;  // GEMM blocks: whole CTA-pair tiles
 
 // Per-device copy streams and events of the host-buffer calls.  One call at a time enqueues
 // on them (the mutex); waits already enqueued keep the event state of their own call, so the
@@ -820,8 +821,10 @@ constexpr int64_t kHostChunkAlign = 256;  // GEMM row blocks: whole CTA-pair til
 struct HostPipe {
     bool ready = false;
     cudaStream_t h2d = nullptr, d2h = nullptr;
-    cudaEvent_t start = nullptr, inputs_shared = nullptr, done = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
     cudaEvent_t in[kHostChunks] = {}, out[kHostChunks] = {};
+    cudaEvent_t a_in[kHostGemmBlocks] = {}, b_in[kHostGemmBlocks] = {};
+    cudaEvent_t c_out[kHostGemmBlocks * kHostGemmBlocks] = {};
 };
 std::mutex g_host_mu;
 HostPipe g_host[kMaxDevices];
@@ -836,11 +839,15 @@ gemm_status host_pipe(HostPipe **out)
         bool ok = cudaStreamCreateWithFlags(&h.h2d, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaStreamCreateWithFlags(&h.d2h, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaEventCreateWithFlags(&h.start, ef) == cudaSuccess &&
-                  cudaEventCreateWithFlags(&h.inputs_shared, ef) == cudaSuccess &&
                   cudaEventCreateWithFlags(&h.done, ef) == cudaSuccess;
         for (int i = 0; ok && i < kHostChunks; ++i)
             ok = cudaEventCreateWithFlags(&h.in[i], ef) == cudaSuccess &&
                  cudaEventCreateWithFlags(&h.out[i], ef) == cudaSuccess;
+        for (int i = 0; ok && i < kHostGemmBlocks; ++i)
+            ok = cudaEventCreateWithFlags(&h.a_in[i], ef) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h.b_in[i], ef) == cudaSuccess;
+        for (int i = 0; ok && i < kHostGemmBlocks * kHostGemmBlocks; ++i)
+            ok = cudaEventCreateWithFlags(&h.c_out[i], ef) == cudaSuccess;
         if (!ok) return GEMM_ERR_CUDA;
         h.ready = true;
     }
@@ -902,31 +909,56 @@ extern "C" gemm_status gemm_f16_f32_host(const void *A, const void *B, float *C,
     auto *dA = reinterpret_cast<uint16_t *>(base + a_off);
     auto *dC = reinterpret_cast<float *>(base + c_off);
 
-    // B first (every row block needs all of it), then A block by block on the copy stream;
-    // each block's product runs on the caller's stream as soon as its rows have arrived, and
-    // its rows of C go back on the second copy stream while the next block is multiplied.
+    // Blocks: up to kHostGemmBlocks row blocks of A and column blocks of B, on whole-tile
+    // boundaries.  The copy stream sends them interleaved along the diagonal (A0, B0, B1, A1,
+    // A2, B2, ...); as soon as the inputs of block C(i, j) are on the device its product runs
+    // on the caller's stream and its rows go back on the second copy stream, so the
+    // device-to-host copies start after the first A and B blocks, not after all of B.
+    const int64_t rb = round_up(tct::ceil_div(M, kHostGemmBlocks), kHostChunkAlign);
+    const int64_t cb = round_up(tct::ceil_div(N, kHostGemmBlocks), kHostChunkAlign);
+    const int P = static_cast<int>(tct::ceil_div(M, rb)), Q = static_cast<int>(tct::ceil_div(N, cb));
     TCT_CUDA_OK(cudaEventRecord(hp->start, s));
     TCT_CUDA_OK(cudaStreamWaitEvent(hp->h2d, hp->start, 0));
     TCT_CUDA_OK(cudaStreamWaitEvent(hp->d2h, hp->start, 0));
-    if (K > 0)
-        TCT_CUDA_OK(cudaMemcpy2DAsync(dB, nb * 2, B, ldb * 2, N * 2, K, cudaMemcpyHostToDevice, hp->h2d));
-    TCT_CUDA_OK(cudaEventRecord(hp->inputs_shared, hp->h2d));
-    TCT_CUDA_OK(cudaStreamWaitEvent(s, hp->inputs_shared, 0));
-    const int64_t rows = host_chunk_rows(M, kHostChunkAlign);
-    int j = 0;
-    for (int64_t r0 = 0; r0 < M; r0 += rows, ++j) {
-        const int64_t mr = std::min(rows, M - r0);
-        if (K > 0)
-            TCT_CUDA_OK(cudaMemcpy2DAsync(dA + r0 * ka, ka * 2, static_cast<const uint16_t *>(A) + r0 * lda, lda * 2,
-                                          K * 2, mr, cudaMemcpyHostToDevice, hp->h2d));
-        TCT_CUDA_OK(cudaEventRecord(hp->in[j], hp->h2d));
-        TCT_CUDA_OK(cudaStreamWaitEvent(s, hp->in[j], 0));
-        st = run_gemm(0, dA + r0 * ka, dB, dC + r0 * nc, GEMM_DTYPE_F32, mr, N, K, ka, nb, nc, nullptr, s, nullptr);
-        if (st != GEMM_OK) return host_finish(hp, s, ws, st);
-        TCT_CUDA_OK(cudaEventRecord(hp->out[j], s));
-        TCT_CUDA_OK(cudaStreamWaitEvent(hp->d2h, hp->out[j], 0));
-        TCT_CUDA_OK(cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, dC + r0 * nc, nc * 4, N * 4, mr, cudaMemcpyDeviceToHost,
-                                      hp->d2h));
+    auto send_a = [&](int i) {
+        const int64_t r0 = i * rb, mr = std::min(rb, M - r0);
+        if (K > 0 && cudaMemcpy2DAsync(dA + r0 * ka, ka * 2, static_cast<const uint16_t *>(A) + r0 * lda, lda * 2,
+                                       K * 2, mr, cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
+            return false;
+        return cudaEventRecord(hp->a_in[i], hp->h2d) == cudaSuccess;
+    };
+    auto send_b = [&](int j) {
+        const int64_t c0 = j * cb, nw = std::min(cb, N - c0);
+        if (K > 0 && cudaMemcpy2DAsync(dB + c0, nb * 2, static_cast<const uint16_t *>(B) + c0, ldb * 2, nw * 2, K,
+                                       cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
+            return false;
+        return cudaEventRecord(hp->b_in[j], hp->h2d) == cudaSuccess;
+    };
+    auto block = [&](int i, int j) {
+        const int64_t r0 = i * rb, mr = std::min(rb, M - r0), c0 = j * cb, nw = std::min(cb, N - c0);
+        if (cudaStreamWaitEvent(s, hp->a_in[i], 0) != cudaSuccess || cudaStreamWaitEvent(s, hp->b_in[j], 0) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        const gemm_status g =
+            run_gemm(0, dA + r0 * ka, dB + c0, dC + r0 * nc + c0, GEMM_DTYPE_F32, mr, nw, K, ka, nb, nc, nullptr, s, nullptr);
+        if (g != GEMM_OK) return g;
+        cudaEvent_t done = hp->c_out[i * kHostGemmBlocks + j];
+        if (cudaEventRecord(done, s) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, done, 0) != cudaSuccess ||
+            cudaMemcpy2DAsync(C + r0 * ldc + c0, ldc * 4, dC + r0 * nc + c0, nc * 4, nw * 4, mr, cudaMemcpyDeviceToHost,
+                              hp->d2h) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        return GEMM_OK;
+    };
+    for (int t = 0; t < std::max(P, Q); ++t) {
+        // A_t then B_t on even steps, B_t then A_t on odd ones; then every block they complete
+        const bool a_first = (t % 2) == 0;
+        if (a_first && t < P && !send_a(t)) return host_finish(hp, s, ws, GEMM_ERR_CUDA);
+        if (t < Q && !send_b(t)) return host_finish(hp, s, ws, GEMM_ERR_CUDA);
+        if (!a_first && t < P && !send_a(t)) return host_finish(hp, s, ws, GEMM_ERR_CUDA);
+        for (int j = 0; j < std::min(t, Q); ++j)  // row t against the earlier column blocks
+            if (t < P && (st = block(t, j)) != GEMM_OK) return host_finish(hp, s, ws, st);
+        for (int i = 0; i < std::min(t, P); ++i)  // column t against the earlier row blocks
+            if (t < Q && (st = block(i, t)) != GEMM_OK) return host_finish(hp, s, ws, st);
+        if (t < P && t < Q && (st = block(t, t)) != GEMM_OK) return host_finish(hp, s, ws, st);
     }
     return host_finish(hp, s, ws, GEMM_OK);
 }
