@@ -352,6 +352,7 @@ void set_epilogue(tct::KernelParams &p, void *C, int c_type, int64_t ldc, const 
     p.beta = epi ? epi->beta : 0.0f;
     p.bias = epi ? epi->bias : nullptr;
     p.bias_type = epi ? epi->bias_type : GEMM_DTYPE_F32;
+    p.bias_vec = (p.bias && reinterpret_cast<uintptr_t>(p.bias) % (4 * type_bytes(p.bias_type)) == 0) ? 1 : 0;
     p.epi = (p.alpha != 1.0f || p.beta != 0.0f || p.bias != nullptr) ? 1 : 0;
 }
 

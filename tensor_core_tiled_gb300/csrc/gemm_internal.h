@@ -26,6 +26,7 @@ struct KernelParams {
     float alpha, beta;
     const void *bias;
     int32_t bias_type;
+    int32_t bias_vec;  // 1 when bias is aligned for 4-element vector loads
     uint64_t timeout_ns;
     // Work split.  `units` CTAs (cta_group 1) or CTA pairs (cta_group 2) first take whole
     // tiles 0 .. dp_tiles-1 (tile u + i * units goes to unit u).  The last split_tiles tiles

@@ -142,6 +142,7 @@ struct TileDst {
     float alpha, beta;
     const void *bias;
     int bias_type;
+    bool bias_vec;  // bias aligned for 4-element vector loads
 };
 
 __device__ __forceinline__ float load_typed(const void *p, int type, int64_t i)
@@ -156,21 +157,53 @@ __device__ __forceinline__ unsigned short to_16bit(float v, int type)
     return type == 1 ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
 }
 
-// Epilogue and store of 4 consecutive outputs (row grow, columns gcol..gcol+3), any type.
-__device__ __forceinline__ void store_general(const TileDst &d, int64_t grow, int64_t gcol, float4 v)
+// Elements i .. i+3 of a typed array (those below `count`; the rest read as 0), with one
+// 16- or 8-byte load when `vec` allows it and all four are present.
+__device__ __forceinline__ float4 load4_typed(const void *p, int type, int64_t i, bool vec, int64_t count)
 {
-    float x[4] = {v.x, v.y, v.z, v.w};
-    const bool full = d.vec && gcol + 3 < d.cols;
-    if (d.epi) {
+    if (vec && count >= 4) {
+        if (type == 2) return __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i));
+        const uint2 h = __ldg(reinterpret_cast<const uint2 *>(static_cast<const unsigned short *>(p) + i));
+        const unsigned short u[4] = {static_cast<unsigned short>(h.x & 0xffffu), static_cast<unsigned short>(h.x >> 16),
+                                     static_cast<unsigned short>(h.y & 0xffffu), static_cast<unsigned short>(h.y >> 16)};
+        float f[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if (!full && gcol + e >= d.cols) continue;
-            float y = d.alpha * x[e];
-            if (d.beta != 0.0f) y = fmaf(d.beta, load_typed(d.base, d.out_type, grow * d.ld + gcol + e), y);
-            if (d.bias) y += load_typed(d.bias, d.bias_type, gcol + e);
-            x[e] = y;
-        }
+        for (int e = 0; e < 4; ++e)
+            f[e] = type == 1 ? __bfloat162float(__ushort_as_bfloat16(u[e])) : __half2float(__ushort_as_half(u[e]));
+        return make_float4(f[0], f[1], f[2], f[3]);
     }
+    float f[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        if (e < count) f[e] = load_typed(p, type, i + e);
+    return make_float4(f[0], f[1], f[2], f[3]);
+}
+
+// The epilogue on 4 outputs: alpha * acc + beta * c + bias (c and bias already loaded).
+__device__ __forceinline__ float4 apply_epilogue(const TileDst &d, float4 v, float4 c, float4 b)
+{
+    float4 y = make_float4(d.alpha * v.x, d.alpha * v.y, d.alpha * v.z, d.alpha * v.w);
+    if (d.beta != 0.0f)
+        y = make_float4(fmaf(d.beta, c.x, y.x), fmaf(d.beta, c.y, y.y), fmaf(d.beta, c.z, y.z), fmaf(d.beta, c.w, y.w));
+    if (d.bias) y = make_float4(y.x + b.x, y.y + b.y, y.z + b.z, y.w + b.w);
+    return y;
+}
+
+// Epilogue and store of 4 consecutive outputs (row grow, columns gcol..gcol+3), any type.
+// With `applied` the epilogue has been applied to v already.
+__device__ __forceinline__ void store_general(const TileDst &d, int64_t grow, int64_t gcol, float4 v,
+                                              bool applied = false)
+{
+    const bool full = d.vec && gcol + 3 < d.cols;
+    if (d.epi && !applied) {
+        const int64_t count = d.cols - gcol;
+        const float4 c = d.beta != 0.0f ? load4_typed(d.base, d.out_type, grow * d.ld + gcol, d.vec, count)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 b = d.bias ? load4_typed(d.bias, d.bias_type, gcol, d.bias_vec, count)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        v = apply_epilogue(d, v, c, b);
+    }
+    float x[4] = {v.x, v.y, v.z, v.w};
     if (d.out_type == 2) {
         float *dst = static_cast<float *>(d.base) + grow * d.ld + gcol;
         if (full) {
@@ -225,6 +258,22 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst 
         // Coalesced, predicated stores: 8 lanes cover one 128-byte row segment.
         const int jj = lane & 7;
         const int64_t gcol = col_base + ch * 32 + jj * 4;
+        // Epilogue inputs, loaded before any store of this block: the bias of this lane's 4
+        // columns (the same for its 8 rows), and C's current values when beta != 0 (all 8 rows
+        // at once, so the loads overlap instead of waiting behind the stores to C).
+        float4 bias4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 cin[8];
+        if (d.epi) {
+            const int64_t count = d.cols - gcol;
+            if (d.bias) bias4 = load4_typed(d.bias, d.bias_type, gcol, d.bias_vec, count);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int64_t grow = row_base + t * 4 + (lane >> 3);
+                cin[t] = (d.beta != 0.0f && grow < d.rows)
+                             ? load4_typed(d.base, d.out_type, grow * d.ld + gcol, d.vec, count)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
 #pragma unroll
         for (int rr0 = 0; rr0 < 32; rr0 += 4) {
             const int rr = rr0 + (lane >> 3);
@@ -237,7 +286,9 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst 
                 v.w += a.w;
             }
             const int64_t grow = row_base + rr;
-            if (grow < d.rows && (d.epi || d.out_type != 2)) {
+            if (grow < d.rows && d.epi) {
+                store_general(d, grow, gcol, apply_epilogue(d, v, cin[rr0 / 4], bias4), true);
+            } else if (grow < d.rows && d.out_type != 2) {
                 store_general(d, grow, gcol, v);
             } else if (grow < d.rows) {
                 float *dst = static_cast<float *>(d.base) + grow * d.ld + gcol;
@@ -584,8 +635,8 @@ __global__ void __launch_bounds__(192, 1)
             const TileCoord c = tile_coord(w.tile, p.num_m, p.num_n, p.group_m);
             const int64_t lane_rows = static_cast<int64_t>(rank) * Cf::BM + q * 32;  // tile-local
             constexpr int64_t kTileElems = static_cast<int64_t>(Cf::BM * CG) * BN;
-            TileDst d{p.C,     p.ldc,   p.M,    p.N,    p.vec_store != 0, true,       nullptr,
-                      p.c_type, p.epi != 0, p.alpha, p.beta, p.bias,            p.bias_type};
+            TileDst d{p.C,      p.ldc,      p.M,     p.N,    p.vec_store != 0, true,        nullptr,
+                      p.c_type, p.epi != 0, p.alpha, p.beta, p.bias,            p.bias_type, p.bias_vec != 0};
             int64_t row_base = static_cast<int64_t>(c.m) * (Cf::BM * CG) + lane_rows;
             int64_t col_base = static_cast<int64_t>(c.n) * BN;
             const uint32_t t_row0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
@@ -609,7 +660,7 @@ __global__ void __launch_bounds__(192, 1)
             if (w.mode == WORK_PARTIAL) {
                 // second half of a split tile for its owner: the whole tile, tile-local rows
                 d = TileDst{p.workspace + w.part * kTileElems, BN, Cf::BM * CG, BN, true, false, nullptr,
-                            2, false, 1.0f, 0.0f, nullptr, 2};
+                            2, false, 1.0f, 0.0f, nullptr, 2, false};
                 row_base = lane_rows;
                 col_base = 0;
             } else if (w.mode == WORK_FIXUP) {
@@ -721,7 +772,8 @@ __global__ void pack_rows_f16(const PackJob j0, const PackJob j1)
 // K == 0: the empty sum, through the epilogue (C = beta * C + bias[col], or zeros).
 __global__ void fill_epilogue(const KernelParams p)
 {
-    TileDst d{p.C, p.ldc, p.M, p.N, false, true, nullptr, p.c_type, p.epi != 0, p.alpha, p.beta, p.bias, p.bias_type};
+    TileDst d{p.C,     p.ldc,      p.M,     p.N,    false,  true,        nullptr,
+              p.c_type, p.epi != 0, p.alpha, p.beta, p.bias, p.bias_type, p.bias_vec != 0};
     const int64_t cols4 = (static_cast<int64_t>(p.N) + 3) / 4;
     const int64_t total = static_cast<int64_t>(p.M) * cols4;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
