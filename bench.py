@@ -551,6 +551,30 @@ def run_configs(args):
                               "tflops": 2 * n ** 3 / ms / 1e9, "frac_of_burst": 2 * n ** 3 / ms / 1e9 / peak_burst}),
                   flush=True)
         del A, B, At, Bt, C
+    # epilogue variants at 8192^3 (gemm_ex): output type, alpha, beta * C, bias
+    g = torch.Generator(device=dev).manual_seed(0)
+    A = torch.randn(n, n, device=dev, generator=g).half()
+    B = torch.randn(n, n, device=dev, generator=g).half()
+    bias = torch.randn(n, device=dev, generator=g)
+    for name, dt, kw in (("FP32 out", torch.float32, {}), ("FP16 out", torch.float16, {}),
+                         ("BF16 out", torch.bfloat16, {}), ("alpha 0.5, FP32 out", torch.float32, {"alpha": 0.5}),
+                         ("beta 1 (reads C), FP32 out", torch.float32, {"beta": 1.0}),
+                         ("bias, FP32 out", torch.float32, {"bias": bias}),
+                         ("beta 1, FP16 out", torch.float16, {"beta": 1.0}),
+                         ("bias, BF16 out", torch.bfloat16, {"bias": bias})):
+        C = torch.randn(n, n, device=dev, generator=g).to(dt)
+        for _ in range(3):
+            tct.gemm(A, B, C, **kw)
+        reps = max(5, min(args.steps, 30))
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for e0, e1 in pairs:
+            e0.record()
+            tct.gemm(A, B, C, **kw)
+            e1.record()
+        torch.cuda.synchronize()
+        ms = statistics.median([e0.elapsed_time(e1) for e0, e1 in pairs])
+        print(json.dumps({"workload": f"epilogue {name} {n}^3", "us": ms * 1e3, "tflops": 2 * n ** 3 / ms / 1e9,
+                          "frac_of_burst": 2 * n ** 3 / ms / 1e9 / peak_burst}), flush=True)
     assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
     return 0
 

@@ -179,6 +179,20 @@ __device__ __forceinline__ float4 load4_typed(const void *p, int type, int64_t i
     return make_float4(f[0], f[1], f[2], f[3]);
 }
 
+// Four values from their loaded bits: FP32 bits, or (`packed16`) four 16-bit values packed
+// in .x and .y.
+__device__ __forceinline__ float4 raw_to_float4(uint4 r, int type, bool packed16)
+{
+    if (!packed16) return make_float4(__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w));
+    const unsigned short u[4] = {static_cast<unsigned short>(r.x & 0xffffu), static_cast<unsigned short>(r.x >> 16),
+                                 static_cast<unsigned short>(r.y & 0xffffu), static_cast<unsigned short>(r.y >> 16)};
+    float f[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        f[e] = type == 1 ? __bfloat162float(__ushort_as_bfloat16(u[e])) : __half2float(__ushort_as_half(u[e]));
+    return make_float4(f[0], f[1], f[2], f[3]);
+}
+
 // The epilogue on 4 outputs: alpha * acc + beta * c + bias (c and bias already loaded).
 __device__ __forceinline__ float4 apply_epilogue(const TileDst &d, float4 v, float4 c, float4 b)
 {
@@ -236,6 +250,8 @@ template <int BN, typename Release>
 __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst &d, int64_t row_base,
                                                   int64_t col_base, float *stage, int lane, Release release)
 {
+    const bool read_c = d.epi && d.beta != 0.0f;
+    const int jj = lane & 7;
     for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + ch * 32, r);
@@ -256,22 +272,34 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst 
                             __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
         __syncwarp();
         // Coalesced, predicated stores: 8 lanes cover one 128-byte row segment.
-        const int jj = lane & 7;
         const int64_t gcol = col_base + ch * 32 + jj * 4;
         // Epilogue inputs, loaded before any store of this block: the bias of this lane's 4
-        // columns (the same for its 8 rows), and C's current values when beta != 0 (all 8 rows
-        // at once, so the loads overlap instead of waiting behind the stores to C).
+        // columns (the same for its 8 rows), and C's current values when beta != 0 -- all 8
+        // rows at once and unconverted, so that the loads are in flight together instead of
+        // waiting behind the stores to C or behind each other's conversions.
         float4 bias4 = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 cin[8];
-        if (d.epi) {
-            const int64_t count = d.cols - gcol;
-            if (d.bias) bias4 = load4_typed(d.bias, d.bias_type, gcol, d.bias_vec, count);
+        if (d.epi && d.bias) bias4 = load4_typed(d.bias, d.bias_type, gcol, d.bias_vec, d.cols - gcol);
+        if (read_c) {
+            if (d.out_type != 2 && d.vec && d.cols - gcol >= 4) {
+                // 16-bit C: all eight loads first, then the conversions
+                uint2 raw[8];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int64_t grow = row_base + t * 4 + (lane >> 3);
-                cin[t] = (d.beta != 0.0f && grow < d.rows)
-                             ? load4_typed(d.base, d.out_type, grow * d.ld + gcol, d.vec, count)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int t = 0; t < 8; ++t) {
+                    const int64_t grow = row_base + t * 4 + (lane >> 3);
+                    raw[t] = grow < d.rows ? __ldg(reinterpret_cast<const uint2 *>(
+                                                 static_cast<const unsigned short *>(d.base) + grow * d.ld + gcol))
+                                           : make_uint2(0u, 0u);
+                }
+#pragma unroll
+                for (int t = 0; t < 8; ++t) cin[t] = raw_to_float4(make_uint4(raw[t].x, raw[t].y, 0u, 0u), d.out_type, true);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int64_t grow = row_base + t * 4 + (lane >> 3);
+                    cin[t] = grow < d.rows ? load4_typed(d.base, d.out_type, grow * d.ld + gcol, d.vec, d.cols - gcol)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
         }
 #pragma unroll
@@ -287,7 +315,8 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst 
             }
             const int64_t grow = row_base + rr;
             if (grow < d.rows && d.epi) {
-                store_general(d, grow, gcol, apply_epilogue(d, v, cin[rr0 / 4], bias4), true);
+                const float4 c = read_c ? cin[rr0 / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                store_general(d, grow, gcol, apply_epilogue(d, v, c, bias4), true);
             } else if (grow < d.rows && d.out_type != 2) {
                 store_general(d, grow, gcol, v);
             } else if (grow < d.rows) {
