@@ -324,6 +324,9 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
     pl->tile_k = kTileK;
     pl->stages = stages;
     pl->group_m = opt && opt->group_m ? opt->group_m : kDefaultGroupM;
+    // The kernel indexes tiles with 32-bit integers (no allocation on one device holds a C
+    // with 2^31 tiles of 128 x 128 or more; such sizes can only be a caller's mistake).
+    if (best_sp.tiles >= (int64_t{1} << 31)) return GEMM_ERR_INVALID_ARG;
     pl->grid = static_cast<int32_t>(best_sp.units * cg);
     pl->tiles = best_sp.tiles;
     pl->waves = best_sp.waves;

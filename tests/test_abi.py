@@ -63,6 +63,12 @@ def test_invalid_arguments_rejected_before_any_device_work(tct_lib):
         assert fn(p + 2, p + 64, 4, 8, 8, 8, 0) == tct.GEMM_ERR_INVALID_ARG
         assert fn(0, p, 4, 8, 8, 8, 0) == tct.GEMM_ERR_INVALID_ARG
         assert fn(0, 0, 0, 8, 8, 8, 0) == tct.GEMM_OK
+    # more output tiles than the kernel's 32-bit tile index: rejected by the planner
+    huge = (1 << 31) - 1
+    with pytest.raises(tct.GemmError):
+        tct.gemm_f16_f32_plan(huge, huge, 64, num_sms=152)
+    assert tct.load().gemm_f16_f32_plan(huge, huge, 64, 64, huge, 152, None,
+                                        ctypes.byref(tct.GemmPlan())) == tct.GEMM_ERR_INVALID_ARG
     # empty output is a no-op that needs no device
     assert tct.gemm_f16_f32(0, 0, 0, 0, 5, 7, 7, 5, 5, 0) == tct.GEMM_OK
     assert tct.gemm_f16_f32(0, 0, 0, 5, 0, 7, 7, 0, 0, 0) == tct.GEMM_OK
