@@ -78,8 +78,9 @@ TCT_API gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t
  *   stream_k  : 1 = whole tiles only; 2 = split each tile of the last, partial wave into
  *               two k-parts: its owner unit takes the first split_kb k-blocks and one of the
  *               units left over takes the rest (a helper may take several tiles' second
- *               parts in turn; see gemm_plan).  With the plain FP32 epilogue and a C whose
- *               base and row pitch are 16-byte multiples, the owner zeroes the tile in C and
+ *               parts in turn; see gemm_plan).  With the plain FP32 epilogue, a C whose
+ *               base and row pitch are 16-byte multiples and N a multiple of 4 (the TMA
+ *               writes whole 16-byte units of a row), the owner zeroes the tile in C and
  *               both parts are added into it by TMA reduce-add; otherwise the second part goes
  *               through a stream-ordered workspace and the owner adds it.  Every tile has two
  *               contributions, so the sum does not depend on their order and results are
@@ -160,7 +161,9 @@ TCT_API gemm_status gemm_ex(int32_t ab_type, int32_t op_a, int32_t op_b, const v
 
 /*
  * Launch plan the library would use for a problem (host only, no GPU needed when
- * num_sms > 0 is given; num_sms <= 0 queries the current device).
+ * num_sms > 0 is given; num_sms <= 0 queries the current device), for gemm_f16_f32 with
+ * 16-byte aligned bases and ldc a multiple of 4: split tiles are planned as combined by TMA
+ * reduce-add when N is a multiple of 4, through workspace otherwise.
  */
 typedef struct gemm_plan {
     int32_t tile_m, tile_n, tile_k; /* output tile and k-block                        */

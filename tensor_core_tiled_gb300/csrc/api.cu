@@ -382,6 +382,7 @@ tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t 
     p.flags = nullptr;
     p.fault_inject = 0;
     p.split_mode = 0;
+    p.c_tma = 0;
     return p;
 }
 
@@ -415,9 +416,10 @@ gemm_status encode_parts(CUtensorMap *m, const float *base, int64_t rows, int ti
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// 2-D FP32 tensor map over C for split tiles combined by TMA reduce-add: boxes of 32 columns
-// (128 bytes, 128-byte swizzle, the epilogue's staging layout) by 32 rows.
-gemm_status encode_c_reduce(CUtensorMap *m, void *C, int64_t M, int64_t N, int64_t ldc)
+// 2-D FP32 tensor map over C for the TMA stores of whole tiles and the TMA reduce-add of
+// split tiles: boxes of 32 columns (128 bytes, 128-byte swizzle, the epilogue's staging
+// layout) by 32 rows.
+gemm_status encode_c_map(CUtensorMap *m, void *C, int64_t M, int64_t N, int64_t ldc)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     gemm_status st = get_encoder(&enc);
@@ -429,6 +431,15 @@ gemm_status encode_c_reduce(CUtensorMap *m, void *C, int64_t M, int64_t N, int64
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Whether TMA may write FP32 C: a 16-byte aligned base and row pitch, and N a multiple of 4.
+// TMA stores and reduce-adds clip a box at the tensor's edge in whole 16-byte units of the
+// row (measured on GB300: with N = 4q + r, r > 0, columns up to 4q + 3 are written), so a
+// row that ends inside a 16-byte unit would have its padding written.
+bool c_tma_ok(const void *C, int64_t N, int64_t ldc)
+{
+    return reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0 && N % 4 == 0;
 }
 
 // Co-resident CTA pairs on the current device for the pair kernels (queried once).
@@ -485,11 +496,11 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
         return to_status(tct::launch_fill_epilogue(p, dev.sms, s));
     }
 
-    // Split tiles add into C by TMA reduce-add when the epilogue is the plain FP32 store and C
-    // is TMA-addressable (16-byte aligned base and row pitch); otherwise through workspace.
+    // With the plain FP32 epilogue and a C the TMA can write, tiles are written by TMA stores
+    // and split tiles add into C by TMA reduce-add; otherwise tiles are stored by the epilogue
+    // warps and split tiles combine through workspace.
     const bool plain = !epi || (epi->alpha == 1.0f && epi->beta == 0.0f && !epi->bias);
-    const bool reduce_ok =
-        plain && c_type == GEMM_DTYPE_F32 && reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0;
+    const bool reduce_ok = plain && c_type == GEMM_DTYPE_F32 && c_tma_ok(C, N, ldc);
     gemm_plan pl;
     st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), opt, A, B, &pl, true, layout, reduce_ok);
     if (st != GEMM_OK) return st;
@@ -548,12 +559,15 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
         p.fault_inject = opt ? opt->fault_inject : 0;
         CUtensorMap tp;
         std::memset(&tp, 0, sizeof(tp));
-        if (pl.stream_k_tiles > 0) {
+        if (reduce_ok) {
+            p.c_tma = 1;
+            st = encode_c_map(&tp, C, M, N, ldc);
+        }
+        if (pl.stream_k_tiles > 0 && st == GEMM_OK) {
             uint8_t *w = static_cast<uint8_t *>(ws) + a_bytes + b_bytes;
             p.flags = reinterpret_cast<unsigned int *>(w + w_bytes);
             if (reduce_ok) {
                 p.split_mode = 1;
-                st = encode_c_reduce(&tp, C, M, N, ldc);
             } else {
                 p.workspace = reinterpret_cast<float *>(w);
                 st = encode_parts(&tp, p.workspace, static_cast<int64_t>(pl.stream_k_tiles) * pl.tile_m, pl.tile_n);
@@ -638,9 +652,11 @@ gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int6
         sms = dev.sms;
         pairs = device_pair_slots(&dev);
     }
-    // Alignment of the base pointers is unknown here: assume 16-byte aligned bases.
+    // Alignment of the base pointers is unknown here: assume 16-byte aligned bases (and ldc
+    // a multiple of 4, so that C is TMA-writable exactly when N is a multiple of 4).
     const void *aligned = reinterpret_cast<const void *>(uintptr_t{256});
-    return make_plan(M, N, K, lda, ldb, sms, pairs, opt, aligned, aligned, out);
+    return make_plan(M, N, K, lda, ldb, sms, pairs, opt, aligned, aligned, out, true, 0,
+                     c_tma_ok(aligned, N, round_up(N, 4)));
 }
 
 gemm_status gemm_f16_f32_work_item(int64_t M, int64_t N, int64_t K, int32_t num_sms, const gemm_options *opt,
@@ -805,9 +821,14 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
     st = encode_16bit_2d(&ta, a_use, M, K, lda_use, kTileM, false);
     if (st == GEMM_OK) st = encode_16bit_2d(&tb, b_use, K, N, ldb_use, kTileK, false);
     if (st != GEMM_OK) return st;
-    const tct::KernelParams p = make_params(pl, C, M, N, K, ldc, kDefaultTimeoutMs);
-    CUtensorMap tp;  // no split tiles on this path
+    tct::KernelParams p = make_params(pl, C, M, N, K, ldc, kDefaultTimeoutMs);
+    CUtensorMap tp;  // no split tiles on this path: the C map, for TMA stores, when C allows it
     std::memset(&tp, 0, sizeof(tp));
+    if (c_tma_ok(C, N, ldc)) {
+        p.c_tma = 1;
+        st = encode_c_map(&tp, C, M, N, ldc);
+        if (st != GEMM_OK) return st;
+    }
     return to_status(tct::launch_gemm(ta, tb, tp, p, 0, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
 }
 

@@ -48,6 +48,9 @@ struct KernelParams {
     // halves then add their accumulators into C with TMA reduce-add (the tensor map in the
     // part-map slot), so C = (0 + a) + b = (0 + b) + a whichever half lands first.
     int32_t split_mode;
+    // 1 when the part-map slot holds the FP32 tensor map over C (plain FP32 epilogue, C
+    // TMA-addressable): whole tiles are then written by TMA stores as well.
+    int32_t c_tma;
 };
 
 enum WorkMode : int32_t {

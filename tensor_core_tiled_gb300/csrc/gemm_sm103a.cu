@@ -338,14 +338,18 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst 
     }
 }
 
-// One accumulator buffer added into C by TMA reduce-add (split tiles under split_mode 1):
-// each 32 x 32 block is staged in the 128-byte-swizzled layout the C tensor map names and
-// reduced into C at (row0, col0 + 32 * ch); the hardware clips boxes that reach past C.
+// One accumulator buffer written to FP32 C by TMA (plain epilogue, TMA-addressable C): each
+// 32 x 32 block is staged in the 128-byte-swizzled layout the C tensor map names and stored
+// (kReduce false) or added (kReduce true: both halves of a split tile under split_mode 1) at
+// (row0, col0 + 32 * ch); the hardware clips boxes that reach past C.  With kOwnBlocks,
+// `stage` holds BN / 32 blocks of 32 x 32 floats (1024-byte aligned), one per block of the
+// accumulator, so the copies go out back to back; otherwise it is one block, reused once
+// the previous copy has read it.  Returns once the copies have read shared memory, and with
+// kOwnBlocks (a unit's last accumulator) once they have completed.
 // `release` is called by lane 0 once every column has been read from TMEM.
-template <int BN, typename Release>
-__device__ __forceinline__ void reduce_accumulator(uint32_t t_row, const void *tmap_c, int64_t row0, int64_t col0,
-                                                   int64_t rows, int64_t cols, float *stage, int lane,
-                                                   Release release)
+template <int BN, bool kReduce, bool kOwnBlocks, typename Release>
+__device__ __forceinline__ void bulk_accumulator(uint32_t t_row, const void *tmap_c, int64_t row0, int64_t col0,
+                                                 int64_t rows, int64_t cols, float *stage, int lane, Release release)
 {
     for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t r[32];
@@ -356,11 +360,12 @@ __device__ __forceinline__ void reduce_accumulator(uint32_t t_row, const void *t
             __syncwarp();
             if (lane == 0) release();
         }
-        if (ch > 0) {  // the previous block has been read out of the staging buffer
+        float *block = kOwnBlocks ? stage + ch * 32 * 32 : stage;
+        if (!kOwnBlocks && ch > 0) {  // the previous block has been read out of the staging buffer
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
         }
-        float4 *srow = reinterpret_cast<float4 *>(stage + lane * 32);
+        float4 *srow = reinterpret_cast<float4 *>(block + lane * 32);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             srow[j ^ (lane & 7)] =
@@ -370,11 +375,19 @@ __device__ __forceinline__ void reduce_accumulator(uint32_t t_row, const void *t
         __syncwarp();
         const int64_t c = col0 + ch * 32;
         if (lane == 0 && row0 < rows && c < cols) {
-            tma_reduce_add_2d(tmap_c, static_cast<int32_t>(c), static_cast<int32_t>(row0), smem_u32(stage));
+            if constexpr (kReduce)
+                tma_reduce_add_2d(tmap_c, static_cast<int32_t>(c), static_cast<int32_t>(row0), smem_u32(block));
+            else
+                tma_store_2d(tmap_c, static_cast<int32_t>(c), static_cast<int32_t>(row0), smem_u32(block));
             bulk_commit_group();
         }
     }
-    if (lane == 0) bulk_wait_all();
+    if (lane == 0) {
+        if constexpr (kOwnBlocks)
+            bulk_wait_all();
+        else
+            bulk_wait_read_all();
+    }
     __syncwarp();
 }
 
@@ -669,21 +682,36 @@ __global__ void __launch_bounds__(192, 1)
             int64_t row_base = static_cast<int64_t>(c.m) * (Cf::BM * CG) + lane_rows;
             int64_t col_base = static_cast<int64_t>(c.n) * BN;
             const uint32_t t_row0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
+            // Plain FP32 epilogue with a TMA-addressable C: the accumulator goes out by TMA
+            // stores, or by TMA reduce-adds for either half of a split tile (C zeroed by the
+            // tile's owner).  A unit's last accumulator is staged in the stage buffers -- its
+            // MMAs have completed, so no stage is read or written again -- with a block of its
+            // own for each 32 columns; the others share this warp's staging block.
+            auto release = [&] {
+                if constexpr (kPair)
+                    mbar_arrive_cluster(map_to_cta(tempty_bar(b), 0));
+                else
+                    mbar_arrive(tempty_bar(b));
+            };
+            WorkItem next;
+            const bool own_blocks = Cf::SPLIT_OK && !work_item(p, unit, it + 1, next);
+            float *blocks = reinterpret_cast<float *>(sA) + (warp - 2) * 32 * BN;
             if (p.split_mode == 1 && w.mode != WORK_STORE) {
-                // Either half of a split tile: add the accumulator into C, zeroed by the owner.
                 ok = wait_flag(p.flags + w.part * CG + rank, limit, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 fence_proxy_async_all();  // the owner's zeros (generic writes) before the reduce
-                if constexpr (kPair) {
-                    const uint32_t te = map_to_cta(tempty_bar(b), 0);
-                    reduce_accumulator<BN>(t_row0, &tmP, row_base, col_base, p.M, p.N, stage, lane,
-                                           [&] { mbar_arrive_cluster(te); });
-                } else {
-                    const uint32_t te = tempty_bar(b);
-                    reduce_accumulator<BN>(t_row0, &tmP, row_base, col_base, p.M, p.N, stage, lane,
-                                           [&] { mbar_arrive(te); });
-                }
+                if (own_blocks)
+                    bulk_accumulator<BN, true, true>(t_row0, &tmP, row_base, col_base, p.M, p.N, blocks, lane, release);
+                else
+                    bulk_accumulator<BN, true, false>(t_row0, &tmP, row_base, col_base, p.M, p.N, stage, lane, release);
+                continue;
+            }
+            if (p.c_tma && w.mode == WORK_STORE) {
+                if (own_blocks)
+                    bulk_accumulator<BN, false, true>(t_row0, &tmP, row_base, col_base, p.M, p.N, blocks, lane, release);
+                else
+                    bulk_accumulator<BN, false, false>(t_row0, &tmP, row_base, col_base, p.M, p.N, stage, lane, release);
                 continue;
             }
             if (w.mode == WORK_PARTIAL) {
@@ -735,6 +763,8 @@ __global__ void __launch_bounds__(192, 1)
                     flag_release_gpu(p.flags + w.part * CG + rank, 1u);
             }
         }
+        if (lane == 0) bulk_wait_all();  // every TMA store or reduce of this warp has completed
+        __syncwarp();
     }
 
     tc_fence_before();

@@ -176,6 +176,16 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, int32_t c0, 
                  : "memory");
 }
 
+// 2-D tiled TMA store of one box from shared memory; elements outside the tensor are not
+// written.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int32_t c0, int32_t c1, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until the shared-memory sources of this thread's committed bulk groups have been read.

@@ -154,6 +154,38 @@ def test_leading_dims_offsets_and_guard_zones(M, N, K, pad_a, pad_b, pad_c, off)
     assert within_tol(body[:, :N], R, K)
 
 
+@pytest.mark.parametrize("M,N,K,ldc,opts", [
+    (300, 201, 150, 204, dict(stream_k=1)),
+    (300, 201, 150, 204, dict(stream_k=2)),
+    (5, 7, 154, 8, {}),
+    (257, 516, 100, 520, dict(stream_k=1)),
+    (257, 516, 100, 520, dict(stream_k=2)),
+    (3000, 2050, 700, 2052, dict(stream_k=2)),
+    (1000, 1024, 64, 1024, dict(stream_k=2, cta_group=1, tile_n=128)),
+])
+def test_aligned_c_padding_bits_untouched(M, N, K, ldc, opts):
+    """A 16-byte aligned C with ldc % 4 == 0, whole tiles and split tiles: the columns
+    between N and ldc and the rows around C keep their bits (-0.0, which an added zero would
+    turn into +0.0), also when N is not a multiple of 4 and the last 16 bytes of a row are
+    only partly inside the M x N block."""
+    rng = np.random.default_rng(19)
+    A, B = inputs.normal_pair(rng, M, N, K)
+    guard = 1024
+    c_buf = torch.full((guard + M * ldc + guard,), -0.0, dtype=torch.float32, device="cuda")
+    c_base = c_buf.data_ptr() + guard * 4
+    dA, dB = dev16(A), dev16(B)
+    st = tct.gemm_f16_f32_ex(dA.data_ptr(), dB.data_ptr(), c_base, M, N, K, K, N, ldc,
+                             torch.cuda.current_stream().cuda_stream, **opts)
+    assert st == tct.GEMM_OK
+    torch.cuda.synchronize()
+    bits = c_buf.view(torch.int32).cpu().numpy()
+    neg0 = np.int32(-2 ** 31)
+    assert np.all(bits[:guard] == neg0) and np.all(bits[guard + M * ldc:] == neg0)
+    body = bits[guard:guard + M * ldc].reshape(M, ldc)
+    assert np.all(body[:, N:] == neg0)
+    assert within_tol(body[:, :N].view(np.float32), oracle.gemm_f32(A, B), K)
+
+
 @pytest.mark.parametrize("M,N,K", [(70001, 24, 33), (60000, 25, 10001)])
 def test_repack_more_rows_than_one_launch_covers(M, N, K):
     """Operands with unaligned rows are repacked by a kernel whose grid covers at most 65535
