@@ -19,6 +19,7 @@ write MN), with the page's own 4096 x 1024 case (L2 flushed before each launch) 
 """
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -103,10 +104,15 @@ def hbm_peak():
 
 
 def kernel_hash(sources=KERNEL_SOURCES):
+    """Hash of the device sources' code: comments and layout are left out, so that an edit
+    of a comment does not retire a profile taken on the same code."""
     h = hashlib.sha256()
     for name in sources:
-        with open(os.path.join(ROOT, "tensor_core_tiled_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "tensor_core_tiled_gb300", "csrc", name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -176,8 +176,9 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, int32_t c0, 
                  : "memory");
 }
 
-// 2-D tiled TMA store of one box from shared memory; elements outside the tensor are not
-// written.
+// 2-D tiled TMA store of one box from shared memory.  Elements outside the tensor are not
+// written, except that the innermost dimension is clipped in whole 16-byte units (measured
+// on GB300 for FP32 boxes: a row of N = 4q + r elements, r > 0, is written up to 4q + 3).
 __device__ __forceinline__ void tma_store_2d(const void *tmap, int32_t c0, int32_t c1, uint32_t src)
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
