@@ -416,30 +416,36 @@ gemm_status encode_parts(CUtensorMap *m, const float *base, int64_t rows, int ti
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// 2-D FP32 tensor map over C for the TMA stores of whole tiles and the TMA reduce-add of
-// split tiles: boxes of 32 columns (128 bytes, 128-byte swizzle, the epilogue's staging
-// layout) by 32 rows.
-gemm_status encode_c_map(CUtensorMap *m, void *C, int64_t M, int64_t N, int64_t ldc)
+// 2-D tensor map over C in its own type, for the TMA stores of whole tiles and the TMA
+// reduce-add of split tiles: boxes of 128 bytes of a row (32 FP32 or 64 FP16/BF16 columns,
+// 128-byte swizzle, the epilogue's staging layout) by 32 rows.
+gemm_status encode_c_map(CUtensorMap *m, void *C, int c_type, int64_t M, int64_t N, int64_t ldc)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     gemm_status st = get_encoder(&enc);
     if (st != GEMM_OK) return st;
+    const int esz = type_bytes(c_type);
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * 4};
-    cuuint32_t box[2] = {32, 32};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * esz};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 32};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUtensorMapDataType dt = c_type == GEMM_DTYPE_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : c_type == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = enc(m, dt, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// Whether TMA may write FP32 C: a 16-byte aligned base and row pitch, and N a multiple of 4.
-// TMA stores and reduce-adds clip a box at the tensor's edge in whole 16-byte units of the
-// row (measured on GB300: with N = 4q + r, r > 0, columns up to 4q + 3 are written), so a
-// row that ends inside a 16-byte unit would have its padding written.
-bool c_tma_ok(const void *C, int64_t N, int64_t ldc)
+// Whether TMA may write C of type c_type: a 16-byte aligned base and row pitch, and rows of
+// whole 16-byte units.  TMA stores and reduce-adds clip a box at the tensor's edge in whole
+// 16-byte units of the row (measured on GB300 for FP32: with N = 4q + r, r > 0, columns up
+// to 4q + 3 are written), so a row that ends inside a 16-byte unit would have its padding
+// written.
+bool c_tma_ok(const void *C, int c_type, int64_t N, int64_t ldc)
 {
-    return reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0 && N % 4 == 0;
+    const int per16 = 16 / type_bytes(c_type);
+    return reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % per16 == 0 && N % per16 == 0;
 }
 
 // Co-resident CTA pairs on the current device for the pair kernels (queried once).
@@ -496,11 +502,12 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
         return to_status(tct::launch_fill_epilogue(p, dev.sms, s));
     }
 
-    // With the plain FP32 epilogue and a C the TMA can write, tiles are written by TMA stores
-    // and split tiles add into C by TMA reduce-add; otherwise tiles are stored by the epilogue
-    // warps and split tiles combine through workspace.
+    // When TMA can write C, whole tiles go out by TMA stores, and with the plain FP32
+    // epilogue split tiles add into C by TMA reduce-add; otherwise tiles are stored by the
+    // epilogue warps, and split tiles combine through workspace.
     const bool plain = !epi || (epi->alpha == 1.0f && epi->beta == 0.0f && !epi->bias);
-    const bool reduce_ok = plain && c_type == GEMM_DTYPE_F32 && c_tma_ok(C, N, ldc);
+    const bool c_tma = c_tma_ok(C, c_type, N, ldc);
+    const bool reduce_ok = plain && c_type == GEMM_DTYPE_F32 && c_tma;
     gemm_plan pl;
     st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), opt, A, B, &pl, true, layout, reduce_ok);
     if (st != GEMM_OK) return st;
@@ -557,11 +564,12 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
         tct::KernelParams p = make_params(pl, nullptr, M, N, K, ldc, tmo);
         set_epilogue(p, C, c_type, ldc, epi);
         p.fault_inject = opt ? opt->fault_inject : 0;
-        CUtensorMap tp;
+        CUtensorMap tp, tc;
         std::memset(&tp, 0, sizeof(tp));
-        if (reduce_ok) {
+        std::memset(&tc, 0, sizeof(tc));
+        if (c_tma) {
             p.c_tma = 1;
-            st = encode_c_map(&tp, C, M, N, ldc);
+            st = encode_c_map(&tc, C, c_type, M, N, ldc);
         }
         if (pl.stream_k_tiles > 0 && st == GEMM_OK) {
             uint8_t *w = static_cast<uint8_t *>(ws) + a_bytes + b_bytes;
@@ -574,7 +582,7 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
             }
         }
         if (st == GEMM_OK)
-            st = to_status(tct::launch_gemm(ta, tb, tp, p, layout, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
+            st = to_status(tct::launch_gemm(ta, tb, tp, tc, p, layout, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
     }
     if (ws) {
         if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
@@ -656,7 +664,7 @@ gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int6
     // a multiple of 4, so that C is TMA-writable exactly when N is a multiple of 4).
     const void *aligned = reinterpret_cast<const void *>(uintptr_t{256});
     return make_plan(M, N, K, lda, ldb, sms, pairs, opt, aligned, aligned, out, true, 0,
-                     c_tma_ok(aligned, N, round_up(N, 4)));
+                     c_tma_ok(aligned, GEMM_DTYPE_F32, N, round_up(N, 4)));
 }
 
 gemm_status gemm_f16_f32_work_item(int64_t M, int64_t N, int64_t K, int32_t num_sms, const gemm_options *opt,
@@ -822,14 +830,15 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
     if (st == GEMM_OK) st = encode_16bit_2d(&tb, b_use, K, N, ldb_use, kTileK, false);
     if (st != GEMM_OK) return st;
     tct::KernelParams p = make_params(pl, C, M, N, K, ldc, kDefaultTimeoutMs);
-    CUtensorMap tp;  // no split tiles on this path: the C map, for TMA stores, when C allows it
+    CUtensorMap tp, tc;  // no split tiles on this path; the C map, for TMA stores, when C allows it
     std::memset(&tp, 0, sizeof(tp));
-    if (c_tma_ok(C, N, ldc)) {
+    std::memset(&tc, 0, sizeof(tc));
+    if (c_tma_ok(C, GEMM_DTYPE_F32, N, ldc)) {
         p.c_tma = 1;
-        st = encode_c_map(&tp, C, M, N, ldc);
+        st = encode_c_map(&tc, C, GEMM_DTYPE_F32, M, N, ldc);
         if (st != GEMM_OK) return st;
     }
-    return to_status(tct::launch_gemm(ta, tb, tp, p, 0, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
+    return to_status(tct::launch_gemm(ta, tb, tp, tc, p, 0, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
 }
 
 // ---------------------------------------------------------------- host-buffer pipelines

@@ -45,11 +45,11 @@ struct KernelParams {
     // How split tiles are combined.  0: the second half goes through workspace and the owner
     // adds it (any epilogue).  1 (plain FP32 epilogue, C TMA-addressable): the owner zeroes
     // its rows of the tile in C at kernel start and raises flag[part * cta_group + rank]; both
-    // halves then add their accumulators into C with TMA reduce-add (the tensor map in the
-    // part-map slot), so C = (0 + a) + b = (0 + b) + a whichever half lands first.
+    // halves then add their accumulators into C with TMA reduce-add (the tensor map over C),
+    // so C = (0 + a) + b = (0 + b) + a whichever half lands first.
     int32_t split_mode;
-    // 1 when the part-map slot holds the FP32 tensor map over C (plain FP32 epilogue, C
-    // TMA-addressable): whole tiles are then written by TMA stores as well.
+    // 1 when the tensor map over C is valid (C's base and row pitch 16-byte aligned, N a
+    // whole number of 16-byte units): whole tiles are then written by TMA stores.
     int32_t c_tma;
 };
 
@@ -143,9 +143,12 @@ int variant_split_ok(int cta_group, int tile_n, int stages);
 // Co-resident clusters of the variant on the current device (-1 if the query fails).
 int variant_max_clusters(int cta_group, int tile_n, int stages);
 
-// tp: 2-D FP32 map of the split-tile parts (box tile_n x 32), unused when split_tiles == 0.
-cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const KernelParams &p,
-                        int layout, int cta_group, int tile_n, int stages, int grid, cudaStream_t stream);
+// tp: 2-D FP32 map of the split-tile parts (box tile_n x 32), used when split tiles combine
+// through workspace (split_mode 0).  tc: 2-D map over C in its own type (boxes of 128 bytes
+// x 32 rows, 128-byte swizzle), used when p.c_tma is set.
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const CUtensorMap &tc,
+                        const KernelParams &p, int layout, int cta_group, int tile_n, int stages, int grid,
+                        cudaStream_t stream);
 
 // Copies up to two FP16 operands (a NULL src skips one) into buffers with 16-byte aligned rows,
 // in one launch.

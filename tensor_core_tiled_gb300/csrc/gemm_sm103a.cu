@@ -65,13 +65,14 @@ struct Cfg {
     static constexpr int STAGE_TX = CG * (A_STAGE + B_STAGE);  // bytes counted on one full barrier
     static constexpr int EPI_WARPS = 4;
     static constexpr int EPI_BYTES = EPI_WARPS * 32 * 32 * 4;
-    static constexpr int NUM_BARS = 2 * STAGES + 6 + EPI_WARPS;
+    static constexpr int BIAS_BYTES = EPI_WARPS * BN_ * 4;  // a tile's bias, per epilogue warp
+    static constexpr int NUM_BARS = 2 * STAGES + 6 + 2 * EPI_WARPS;
     // A split tile's part (32 rows x BN FP32 per epilogue warp) is loaded into the stage
     // buffers, which are idle by then; only variants with room for it split tiles.
     static constexpr bool SPLIT_OK = STAGES * (A_STAGE + B_STAGE) >= EPI_WARPS * 32 * BN * 4;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM_BYTES =
-        1024 + STAGES * (A_STAGE + B_STAGE) + EPI_BYTES + NUM_BARS * 8 + 16;
+        1024 + STAGES * (A_STAGE + B_STAGE) + EPI_BYTES + BIAS_BYTES + NUM_BARS * 8 + 16;
     static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per tile");
     static_assert(BN_CTA % 64 == 0 && BN <= 256, "B columns per CTA must be whole 64-column boxes");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
@@ -338,47 +339,132 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst 
     }
 }
 
-// One accumulator buffer written to FP32 C by TMA (plain epilogue, TMA-addressable C): each
-// 32 x 32 block is staged in the 128-byte-swizzled layout the C tensor map names and stored
-// (kReduce false) or added (kReduce true: both halves of a split tile under split_mode 1) at
-// (row0, col0 + 32 * ch); the hardware clips boxes that reach past C.  With kOwnBlocks,
-// `stage` holds BN / 32 blocks of 32 x 32 floats (1024-byte aligned), one per block of the
-// accumulator, so the copies go out back to back; otherwise it is one block, reused once
-// the previous copy has read it.  Returns once the copies have read shared memory, and with
-// kOwnBlocks (a unit's last accumulator) once they have completed.
-// `release` is called by lane 0 once every column has been read from TMEM.
-template <int BN, bool kReduce, bool kOwnBlocks, typename Release>
-__device__ __forceinline__ void bulk_accumulator(uint32_t t_row, const void *tmap_c, int64_t row0, int64_t col0,
-                                                 int64_t rows, int64_t cols, float *stage, int lane, Release release)
+// Two floats rounded to the 16-bit type (FP16 0, BF16 1) and packed, the first in the low half.
+__device__ __forceinline__ uint32_t pack_16bit(float a, float b, int type)
 {
-    for (int ch = 0; ch < BN / 32; ++ch) {
+    return static_cast<uint32_t>(to_16bit(a, type)) | (static_cast<uint32_t>(to_16bit(b, type)) << 16);
+}
+
+// One accumulator buffer written to C by TMA, when the tensor map over C can write it (C's
+// base and row pitch 16-byte aligned, rows of whole 16-byte units).  The warp's 32 rows go
+// out in blocks of 32 rows x 128 bytes: 32 FP32 columns (kWide false) or 64 FP16/BF16
+// columns (kWide true), staged in the 128-byte-swizzled layout the tensor map names.  Each
+// lane holds one row of 32 accumulator columns at a time (tcgen05.ld 32x32b) and applies
+// the epilogue, alpha * acc + beta * C + bias[col], with the same operations as
+// store_general (the bias from `sbias`, the tile's bias columns as floats, staged by the
+// warp before the tile's accumulator was ready).  When beta != 0, C's block is first TMA-loaded into the staging block
+// (barrier `cbar`, phase count `cphase`) and each lane overwrites its row there.  Lane 0
+// then stores the block (kReduce false) or adds it (kReduce true: either half of a split
+// tile under split_mode 1, plain FP32 only) at (row0, first column of the block); the
+// hardware clips boxes that reach past C.  With kOwnBlocks, `stage` holds one 4 KB block
+// (1024-byte aligned) per block of the accumulator, all C loads are issued at once and the
+// copies go out back to back; otherwise it is one block, reused once the previous copy has
+// read it.  Returns false if a C load did not arrive in time (after recording the timeout);
+// else once the copies have read shared memory, and with kOwnBlocks once they have completed.
+// `release` is called by lane 0 once every column has been read from TMEM.
+template <int BN, bool kReduce, bool kOwnBlocks, bool kWide, typename Release>
+__device__ __forceinline__ bool bulk_accumulator(uint32_t t_row, const void *tmap_c, int64_t row0, int64_t col0,
+                                                 const TileDst &d, const float *sbias, float *stage, int lane,
+                                                 uint32_t cbar, uint32_t &cphase, uint64_t limit,
+                                                 volatile int *abort_flag, Release release)
+{
+    static_assert(!(kReduce && kWide), "reduce-add of FP32 only");
+    constexpr int kCols = kWide ? 64 : 32;  // columns per staged block (128-byte rows)
+    constexpr int kChunk = kWide ? 8 : 4;   // columns per 16-byte unit
+    constexpr int kUnits = 32 / kChunk;     // 16-byte units per 32 accumulator columns
+    constexpr int kBlocks = BN / kCols;
+    const bool read_c = d.epi && d.beta != 0.0f;
+    const bool rows_in = row0 < d.rows;
+    auto block_in = [&](int blk) { return rows_in && col0 + blk * kCols < d.cols; };
+    auto load_c = [&](int blk, float *dst) {  // lane 0: C's block into dst, counted on cbar
+        tma_load_2d(smem_u32(dst), tmap_c, static_cast<int32_t>(col0 + blk * kCols), static_cast<int32_t>(row0), cbar);
+    };
+    bool ok = true;
+    if (kOwnBlocks && read_c) {
+        int n = 0;
+        for (int blk = 0; blk < kBlocks; ++blk) n += block_in(blk) ? 1 : 0;
+        if (n > 0) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(cbar, n * 4096u);
+                for (int blk = 0; blk < kBlocks; ++blk)
+                    if (block_in(blk)) load_c(blk, stage + blk * 32 * 32);
+            }
+            ok = wait_or_abort<false>(cbar, cphase & 1u, limit, abort_flag, SITE_EPI_PARTS);
+            ++cphase;
+        }
+    }
+    // The accumulator is read 32 columns at a time (a wide block takes two reads).
+    for (int sb = 0; sb < BN / 32; ++sb) {
+        const int blk = kWide ? sb >> 1 : sb;
+        const int half = kWide ? sb & 1 : 0;
+        const int64_t c0 = col0 + blk * kCols;  // first column of the staged block
+        float *block = kOwnBlocks ? stage + blk * 32 * 32 : stage;
+        if (!kOwnBlocks && half == 0) {
+            if (blk > 0) {  // the previous block has been read out of the staging buffer
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+            }
+            if (read_c && block_in(blk)) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(cbar, 4096u);
+                    load_c(blk, block);
+                }
+            }
+        }
         uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + ch * 32, r);
+        tmem_ld_32x32b_x32(t_row + sb * 32, r);
         tmem_wait_ld();
-        if (ch == BN / 32 - 1) {
+        if (sb == BN / 32 - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) release();
         }
-        float *block = kOwnBlocks ? stage + ch * 32 * 32 : stage;
-        if (!kOwnBlocks && ch > 0) {  // the previous block has been read out of the staging buffer
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
+        if (!kOwnBlocks && half == 0 && read_c && block_in(blk)) {
+            ok = wait_or_abort<false>(cbar, cphase & 1u, limit, abort_flag, SITE_EPI_PARTS) && ok;
+            ++cphase;
         }
-        float4 *srow = reinterpret_cast<float4 *>(block + lane * 32);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        uint4 *srow = reinterpret_cast<uint4 *>(block + lane * 32);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            srow[j ^ (lane & 7)] =
-                make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
-                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        fence_proxy_async_smem();  // this lane's generic writes before the async-proxy read
+        for (int u = 0; u < kUnits; ++u) {
+            const int j = half * kUnits + u;  // 16-byte unit of the staged row
+            const float *bj = sbias + blk * kCols + j * kChunk;  // bias of the unit's columns
+            const uint4 craw = read_c ? srow[j ^ (lane & 7)] : make_uint4(0u, 0u, 0u, 0u);
+            uint4 out;
+            if constexpr (!kWide) {
+                float4 v = make_float4(__uint_as_float(r[4 * u + 0]), __uint_as_float(r[4 * u + 1]),
+                                       __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+                if (d.epi) {
+                    const float4 b = d.bias ? *reinterpret_cast<const float4 *>(bj) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v = apply_epilogue(d, v, raw_to_float4(craw, 2, false), b);
+                }
+                out = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
+            } else {
+                float4 lo = make_float4(__uint_as_float(r[8 * u + 0]), __uint_as_float(r[8 * u + 1]),
+                                        __uint_as_float(r[8 * u + 2]), __uint_as_float(r[8 * u + 3]));
+                float4 hi = make_float4(__uint_as_float(r[8 * u + 4]), __uint_as_float(r[8 * u + 5]),
+                                        __uint_as_float(r[8 * u + 6]), __uint_as_float(r[8 * u + 7]));
+                if (d.epi) {
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 b_lo = d.bias ? *reinterpret_cast<const float4 *>(bj) : z;
+                    const float4 b_hi = d.bias ? *reinterpret_cast<const float4 *>(bj + 4) : z;
+                    lo = apply_epilogue(d, lo, raw_to_float4(make_uint4(craw.x, craw.y, 0u, 0u), d.out_type, true), b_lo);
+                    hi = apply_epilogue(d, hi, raw_to_float4(make_uint4(craw.z, craw.w, 0u, 0u), d.out_type, true), b_hi);
+                }
+                out = make_uint4(pack_16bit(lo.x, lo.y, d.out_type), pack_16bit(lo.z, lo.w, d.out_type),
+                                 pack_16bit(hi.x, hi.y, d.out_type), pack_16bit(hi.z, hi.w, d.out_type));
+            }
+            srow[j ^ (lane & 7)] = out;
+        }
+        if (kWide && half == 0) continue;  // the block's second half is still to come
+        fence_proxy_async_smem();          // this lane's generic writes before the async-proxy read
         __syncwarp();
-        const int64_t c = col0 + ch * 32;
-        if (lane == 0 && row0 < rows && c < cols) {
+        if (lane == 0 && block_in(blk)) {
             if constexpr (kReduce)
-                tma_reduce_add_2d(tmap_c, static_cast<int32_t>(c), static_cast<int32_t>(row0), smem_u32(block));
+                tma_reduce_add_2d(tmap_c, static_cast<int32_t>(c0), static_cast<int32_t>(row0), smem_u32(block));
             else
-                tma_store_2d(tmap_c, static_cast<int32_t>(c), static_cast<int32_t>(row0), smem_u32(block));
+                tma_store_2d(tmap_c, static_cast<int32_t>(c0), static_cast<int32_t>(row0), smem_u32(block));
             bulk_commit_group();
         }
     }
@@ -389,6 +475,7 @@ __device__ __forceinline__ void bulk_accumulator(uint32_t t_row, const void *tma
             bulk_wait_read_all();
     }
     __syncwarp();
+    return ok;
 }
 
 // Waits until *flag is raised (by another CTA), bounded like the pipeline waits.
@@ -411,7 +498,8 @@ __device__ __forceinline__ bool wait_flag(const unsigned int *flag, uint64_t lim
 template <int CG, int BN, int STAGES, bool AT, bool BT, bool BF16>
 __global__ void __launch_bounds__(192, 1)
     gemm_tcgen05_f32acc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmP, const KernelParams p)
+                        const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmC,
+                        const KernelParams p)
 {
     using Cf = Cfg<CG, BN, STAGES, AT, BT, BF16>;
     constexpr bool kPair = CG == 2;
@@ -421,7 +509,8 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t *sA = smem;
     uint8_t *sB = sA + STAGES * Cf::A_STAGE;
     float *sEpi = reinterpret_cast<float *>(sB + STAGES * Cf::B_STAGE);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sEpi) + Cf::EPI_BYTES);
+    float *sBias = sEpi + Cf::EPI_BYTES / 4;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sBias) + Cf::BIAS_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cf::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -433,6 +522,8 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
     const uint32_t part_bar = bar0 + 8u * (2 * STAGES + 5);  // epilogue warps done with a part
     auto pload_bar = [&](int e) { return bar0 + 8u * (2 * STAGES + 6 + e); };  // part load, warp e
+    // C load of epilogue warp e (beta != 0 with TMA-written C)
+    auto cload_bar = [&](int e) { return bar0 + 8u * (2 * STAGES + 6 + Cf::EPI_WARPS + e); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -451,7 +542,10 @@ __global__ void __launch_bounds__(192, 1)
         }
         mbar_init(drain_bar, 1);
         mbar_init(part_bar, Cf::EPI_WARPS);
-        for (int e = 0; e < Cf::EPI_WARPS; ++e) mbar_init(pload_bar(e), 1);
+        for (int e = 0; e < Cf::EPI_WARPS; ++e) {
+            mbar_init(pload_bar(e), 1);
+            mbar_init(cload_bar(e), 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -633,6 +727,7 @@ __global__ void __launch_bounds__(192, 1)
         // ------------------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         float *stage = sEpi + (warp - 2) * 32 * 32;
+        float *sbias = sBias + (warp - 2) * BN;  // the current tile's bias columns (TMA path)
         if (p.split_mode == 1 && !(p.fault_inject & 1)) {
             // The owner of a split tile zeroes its rows of the tile in C while the first tile's
             // k-loop runs, then raises the tile's flag for this CTA rank; both halves add into
@@ -666,15 +761,24 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
         int it = 0;
+        uint32_t cphase = 0;  // C loads completed on this warp's cload barrier
         WorkItem w;
         for (; work_item(p, unit, it, w); ++it) {
             const int b = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
+            const TileCoord c = tile_coord(w.tile, p.num_m, p.num_n, p.group_m);
+            if (p.c_tma && p.bias && w.mode == WORK_STORE) {
+                // The tile's bias, as floats, into this warp's copy while the MMAs still run.
+                for (int i = lane; i < BN; i += 32) {
+                    const int64_t col = static_cast<int64_t>(c.n) * BN + i;
+                    sbias[i] = col < p.N ? load_typed(p.bias, p.bias_type, col) : 0.0f;
+                }
+                __syncwarp();
+            }
             bool ok = wait_or_abort<kPair>(tfull_bar(b), use & 1u, limit, abort_flag, SITE_EPI_TMEM_FULL);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const TileCoord c = tile_coord(w.tile, p.num_m, p.num_n, p.group_m);
             const int64_t lane_rows = static_cast<int64_t>(rank) * Cf::BM + q * 32;  // tile-local
             constexpr int64_t kTileElems = static_cast<int64_t>(Cf::BM * CG) * BN;
             TileDst d{p.C,      p.ldc,      p.M,     p.N,    p.vec_store != 0, true,        nullptr,
@@ -682,11 +786,12 @@ __global__ void __launch_bounds__(192, 1)
             int64_t row_base = static_cast<int64_t>(c.m) * (Cf::BM * CG) + lane_rows;
             int64_t col_base = static_cast<int64_t>(c.n) * BN;
             const uint32_t t_row0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
-            // Plain FP32 epilogue with a TMA-addressable C: the accumulator goes out by TMA
-            // stores, or by TMA reduce-adds for either half of a split tile (C zeroed by the
-            // tile's owner).  A unit's last accumulator is staged in the stage buffers -- its
-            // MMAs have completed, so no stage is read or written again -- with a block of its
-            // own for each 32 columns; the others share this warp's staging block.
+            // C that TMA can write: a whole tile goes out by TMA stores after its epilogue, and
+            // (plain FP32 epilogue) either half of a split tile by TMA reduce-adds into C,
+            // zeroed by the tile's owner.  A unit's last accumulator is staged in the stage
+            // buffers -- its MMAs have completed, so no stage is read or written again -- with
+            // a block of its own for each 128-byte column block; the others share this warp's
+            // staging block.
             auto release = [&] {
                 if constexpr (kPair)
                     mbar_arrive_cluster(map_to_cta(tempty_bar(b), 0));
@@ -695,6 +800,7 @@ __global__ void __launch_bounds__(192, 1)
             };
             WorkItem next;
             const bool own_blocks = Cf::SPLIT_OK && !work_item(p, unit, it + 1, next);
+            const uint32_t cb = cload_bar(warp - 2);
             float *blocks = reinterpret_cast<float *>(sA) + (warp - 2) * 32 * BN;
             if (p.split_mode == 1 && w.mode != WORK_STORE) {
                 ok = wait_flag(p.flags + w.part * CG + rank, limit, abort_flag);
@@ -702,16 +808,31 @@ __global__ void __launch_bounds__(192, 1)
                 if (!ok) break;
                 fence_proxy_async_all();  // the owner's zeros (generic writes) before the reduce
                 if (own_blocks)
-                    bulk_accumulator<BN, true, true>(t_row0, &tmP, row_base, col_base, p.M, p.N, blocks, lane, release);
+                    ok = bulk_accumulator<BN, true, true, false>(t_row0, &tmC, row_base, col_base, d, sbias, blocks, lane, cb,
+                                                                 cphase, limit, abort_flag, release);
                 else
-                    bulk_accumulator<BN, true, false>(t_row0, &tmP, row_base, col_base, p.M, p.N, stage, lane, release);
+                    ok = bulk_accumulator<BN, true, false, false>(t_row0, &tmC, row_base, col_base, d, sbias, stage, lane, cb,
+                                                                  cphase, limit, abort_flag, release);
+                if (!ok) break;
                 continue;
             }
             if (p.c_tma && w.mode == WORK_STORE) {
-                if (own_blocks)
-                    bulk_accumulator<BN, false, true>(t_row0, &tmP, row_base, col_base, p.M, p.N, blocks, lane, release);
-                else
-                    bulk_accumulator<BN, false, false>(t_row0, &tmP, row_base, col_base, p.M, p.N, stage, lane, release);
+                if (p.c_type == 2) {
+                    if (own_blocks)
+                        ok = bulk_accumulator<BN, false, true, false>(t_row0, &tmC, row_base, col_base, d, sbias, blocks, lane,
+                                                                      cb, cphase, limit, abort_flag, release);
+                    else
+                        ok = bulk_accumulator<BN, false, false, false>(t_row0, &tmC, row_base, col_base, d, sbias, stage, lane,
+                                                                       cb, cphase, limit, abort_flag, release);
+                } else {
+                    if (own_blocks)
+                        ok = bulk_accumulator<BN, false, true, true>(t_row0, &tmC, row_base, col_base, d, sbias, blocks, lane,
+                                                                     cb, cphase, limit, abort_flag, release);
+                    else
+                        ok = bulk_accumulator<BN, false, false, true>(t_row0, &tmC, row_base, col_base, d, sbias, stage, lane,
+                                                                      cb, cphase, limit, abort_flag, release);
+                }
+                if (!ok) break;
                 continue;
             }
             if (w.mode == WORK_PARTIAL) {
@@ -864,7 +985,7 @@ static cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunc
 
 template <int CG, int BN, int STAGES, bool AT, bool BT, bool BF16>
 static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp,
-                                  const KernelParams &p, int grid, cudaStream_t stream)
+                                  const CUtensorMap &tc, const KernelParams &p, int grid, cudaStream_t stream)
 {
     auto kern = gemm_tcgen05_f32acc<CG, BN, STAGES, AT, BT, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -873,7 +994,7 @@ static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, 
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config<CG, BN, STAGES>(grid, stream, attr);
     if (p.split_tiles > 0 && !Cfg<CG, BN, STAGES>::SPLIT_OK) return cudaErrorInvalidValue;
-    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tp, p);
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tp, tc, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -944,12 +1065,12 @@ int variant_exists(int layout, int cta_group, int tile_n, int stages)
 
 template <bool AT, bool BT, bool BF16>
 static cudaError_t launch_layout(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp,
-                                 const KernelParams &p, int cta_group, int tile_n, int stages, int grid,
-                                 cudaStream_t stream)
+                                 const CUtensorMap &tc, const KernelParams &p, int cta_group, int tile_n, int stages,
+                                 int grid, cudaStream_t stream)
 {
 #define TCT_CASE(CG_, BN_, ST_)                             \
     if (cta_group == CG_ && tile_n == BN_ && stages == ST_) \
-        return launch_variant<CG_, BN_, ST_, AT, BT, BF16>(ta, tb, tp, p, grid, stream);
+        return launch_variant<CG_, BN_, ST_, AT, BT, BF16>(ta, tb, tp, tc, p, grid, stream);
     if constexpr (!AT && !BT && !BF16) {
         TCT_VARIANTS(TCT_CASE)
     } else {
@@ -959,18 +1080,19 @@ static cudaError_t launch_layout(const CUtensorMap &ta, const CUtensorMap &tb, c
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const KernelParams &p,
-                        int layout, int cta_group, int tile_n, int stages, int grid, cudaStream_t stream)
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const CUtensorMap &tc,
+                        const KernelParams &p, int layout, int cta_group, int tile_n, int stages, int grid,
+                        cudaStream_t stream)
 {
     switch (layout) {
-    case 0: return launch_layout<false, false, false>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
-    case 1: return launch_layout<true, false, false>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
-    case 2: return launch_layout<false, true, false>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
-    case 3: return launch_layout<true, true, false>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
-    case 4: return launch_layout<false, false, true>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
-    case 5: return launch_layout<true, false, true>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
-    case 6: return launch_layout<false, true, true>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
-    case 7: return launch_layout<true, true, true>(ta, tb, tp, p, cta_group, tile_n, stages, grid, stream);
+    case 0: return launch_layout<false, false, false>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 1: return launch_layout<true, false, false>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 2: return launch_layout<false, true, false>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 3: return launch_layout<true, true, false>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 4: return launch_layout<false, false, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 5: return launch_layout<true, false, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 6: return launch_layout<false, true, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 7: return launch_layout<true, true, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

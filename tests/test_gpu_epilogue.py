@@ -105,13 +105,76 @@ def test_epilogue_integer_bit_exact(ct, opts):
     exact, so the stored value is the exact result rounded once to C's type -- the same bits
     as the oracle, split tiles included (their owner applies the epilogue once)."""
     rng = np.random.default_rng(72)
-    M, N, K = 700, 900, 300
+    M, N, K = 700, 904, 300  # N % 8 == 0: C of every type goes out by TMA stores
     A, B = inputs.pair_ex(rng, M, N, K, dtype="f16", integer=True)
     Cin = _typed_random(rng, (M, N), ct, integer=True)
     bias = _typed_random(rng, (N,), "f16", integer=True)
     got = run_gpu(A, B, "f16", False, False, M, N, K, ct, 3.0, -2.0, Cin, bias, "f16", **opts)
     want = run_ref(A, B, "f16", False, False, ct, 3.0, -2.0, Cin, bias, "f16")
     assert np.array_equal(got, want)
+
+
+def _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt, offset, ldc, **opts):
+    """gemm_ex with C stored at `offset` elements into its buffer with row pitch ldc; returns
+    C's M x N block and the buffer's other elements, as raw bits."""
+    esz = 4 if ct == "f32" else 2
+    buf = torch.full((offset + M * ldc + 64,), -1, dtype=torch.int32 if ct == "f32" else torch.int16, device="cuda")
+    body = buf[offset:offset + M * ldc].view(M, ldc)
+    src = torch.from_numpy(np.ascontiguousarray(Cin).view(np.int32 if ct == "f32" else np.int16)).cuda()
+    body[:, :N] = src
+    dA, dB = _dev(A, "f16"), _dev(B, "f16")
+    dbias = _dev(bias, bt) if bias is not None else None
+    st = tct.gemm_ex(tct.GEMM_DTYPE_F16, 0, 0, dA.data_ptr(), dB.data_ptr(), buf.data_ptr() + esz * offset,
+                     TYPES[ct][1], M, N, K, K, N, ldc, alpha=alpha, beta=beta,
+                     bias=dbias.data_ptr() if dbias is not None else 0, bias_type=TYPES[bt][1],
+                     stream=torch.cuda.current_stream().cuda_stream, **opts)
+    assert st == tct.GEMM_OK
+    torch.cuda.synchronize()
+    host = buf.cpu().numpy()
+    rest = np.concatenate([host[:offset], host[offset:offset + M * ldc].reshape(M, ldc)[:, N:].ravel(),
+                           host[offset + M * ldc:]])
+    return host[offset:offset + M * ldc].reshape(M, ldc)[:, :N].copy(), rest
+
+
+@pytest.mark.parametrize("ct", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("alpha,beta,bt", [(1.0, 0.0, None), (1.0, 1.0, None), (0.5, 0.0, "bf16"),
+                                           (-1.5, 0.75, "f32"), (2.0, -1.0, "f16")])
+@pytest.mark.parametrize("opts", [{}, dict(stream_k=2)])
+def test_tma_and_lane_store_paths_agree(ct, alpha, beta, bt, opts):
+    """The same problem with C where TMA can write it (16-byte aligned base and pitch, rows of
+    whole 16-byte units: the tile goes out through swizzled staging and TMA stores, C read by
+    TMA when beta != 0) and one element off that alignment (per-lane stores): the same bits,
+    since both paths apply the same operations; nothing outside the M x N block changes."""
+    rng = np.random.default_rng(75)
+    M, N, K = 333, 520, 200
+    A, B = inputs.pair_ex(rng, M, N, K, dtype="f16")
+    Cin = _typed_random(rng, (M, N), ct)
+    bias = _typed_random(rng, (N,), bt) if bt else None
+    ldc = N + 8
+    tma, rest_t = _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt or "f32", 0, ldc, **opts)
+    lane, rest_l = _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt or "f32", 1, ldc, **opts)
+    assert np.all(rest_t == -1) and np.all(rest_l == -1)
+    assert np.array_equal(tma, lane)
+    want = run_ref(A, B, "f16", False, False, ct, alpha, beta, Cin, bias, bt or "f32")
+    S = np.abs(oracle.gemm_ex_f32(A, B))
+    got = tma if ct == "f32" else tma.view(np.uint16)
+    assert close(got.view(np.float32) if ct == "f32" else got, want, ct, K, alpha, S)
+
+
+@pytest.mark.parametrize("ct,N", [("f16", 1500), ("bf16", 1500), ("f16", 1504), ("f32", 1502)])
+def test_padding_untouched_when_rows_end_inside_16_bytes(ct, N):
+    """Aligned base and pitch: rows of whole 16-byte units go through TMA stores, others
+    through per-lane stores; the columns between N and ldc keep their bits either way."""
+    rng = np.random.default_rng(76)
+    M, K = 300, 96
+    A, B = inputs.pair_ex(rng, M, N, K, dtype="f16", integer=True)
+    Cin = _typed_random(rng, (M, N), ct, integer=True)
+    bias = _typed_random(rng, (N,), "f16", integer=True)
+    ldc = N + (8 - N % 8) + 8
+    got, rest = _gemm_ex_at(A, B, M, N, K, ct, 2.0, -1.0, Cin, bias, "f16", 0, ldc)
+    assert np.all(rest == -1)
+    want = run_ref(A, B, "f16", False, False, ct, 2.0, -1.0, Cin, bias, "f16")
+    assert np.array_equal(got.view(np.uint32 if ct == "f32" else np.uint16), np.asarray(want).view(np.uint32 if ct == "f32" else np.uint16))
 
 
 def test_beta_zero_never_reads_c_and_k_zero_is_the_empty_sum():
