@@ -982,16 +982,27 @@ extern "C" gemm_status gemm_f16_f32_host(const void *A, const void *B, float *C,
             return GEMM_ERR_CUDA;
         return GEMM_OK;
     };
+    auto row_blocks = [&](int t) {  // row t against the earlier column blocks
+        for (int j = 0; j < std::min(t, Q); ++j)
+            if (t < P && (st = block(t, j)) != GEMM_OK) return false;
+        return true;
+    };
+    auto col_blocks = [&](int t) {  // column t against the earlier row blocks
+        for (int i = 0; i < std::min(t, P); ++i)
+            if (t < Q && (st = block(i, t)) != GEMM_OK) return false;
+        return true;
+    };
     for (int t = 0; t < std::max(P, Q); ++t) {
-        // A_t then B_t on even steps, B_t then A_t on odd ones; then every block they complete
+        // A_t then B_t on even steps, B_t then A_t on odd ones; the blocks go on the caller's
+        // stream in the order their inputs arrive (a block whose inputs are in never queues
+        // behind one still waiting for its row or column), then the diagonal block.
         const bool a_first = (t % 2) == 0;
         if (a_first && t < P && !send_a(t)) return host_finish(hp, s, ws, GEMM_ERR_CUDA);
-        if (t < Q && !send_b(t)) return host_finish(hp, s, ws, GEMM_ERR_CUDA);
+        if (!a_first && t < Q && !send_b(t)) return host_finish(hp, s, ws, GEMM_ERR_CUDA);
+        if (!(a_first ? row_blocks(t) : col_blocks(t))) return host_finish(hp, s, ws, st);
+        if (a_first && t < Q && !send_b(t)) return host_finish(hp, s, ws, GEMM_ERR_CUDA);
         if (!a_first && t < P && !send_a(t)) return host_finish(hp, s, ws, GEMM_ERR_CUDA);
-        for (int j = 0; j < std::min(t, Q); ++j)  // row t against the earlier column blocks
-            if (t < P && (st = block(t, j)) != GEMM_OK) return host_finish(hp, s, ws, st);
-        for (int i = 0; i < std::min(t, P); ++i)  // column t against the earlier row blocks
-            if (t < Q && (st = block(i, t)) != GEMM_OK) return host_finish(hp, s, ws, st);
+        if (!(a_first ? col_blocks(t) : row_blocks(t))) return host_finish(hp, s, ws, st);
         if (t < P && t < Q && (st = block(t, t)) != GEMM_OK) return host_finish(hp, s, ws, st);
     }
     return host_finish(hp, s, ws, GEMM_OK);
