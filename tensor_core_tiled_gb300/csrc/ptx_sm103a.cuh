@@ -47,12 +47,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Suspend-time hint of a try_wait (ns): a waiting thread sleeps in hardware until the phase
+// completes or this much time has passed, instead of re-polling.  Measured on GB300 against
+// polling without a hint: 0.7-0.8% less time per GEMM at 8192^3 under the power cap,
+// 1.5-2.4% at 4096^3, 6144^3 and 16384 x 16384 x 4096; the softmax unchanged.
+#define TCT_WAIT_HINT_NS "1000000"
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, " TCT_WAIT_HINT_NS ";\n\t"
         "selp.b32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -278,7 +284,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, " TCT_WAIT_HINT_NS ";\n\t"
         "selp.b32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
