@@ -15,7 +15,9 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All
  *     work is enqueued on it; no call synchronises the host.
  *   - C is overwritten (gemm_ex adds the beta * C term).  M == 0 or N == 0 is a no-op.
- *     K == 0 writes zeros (the empty sum) into the M x N block of C.
+ *     K == 0 writes zeros (the empty sum) into the M x N block of C.  Only the M x N block
+ *     is written: the elements between N and ldc, and memory outside the block, keep
+ *     their bits.
  *   - Errors in the arguments are reported immediately through the return value and
  *     nothing is enqueued.  Device-side errors (a pipeline wait that exceeded its time
  *     limit) are recorded in a per-device error word read by gemm_f16_f32_get_error().
