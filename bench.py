@@ -1,7 +1,7 @@
 """Benchmark: FP16 -> FP32 GEMM throughput on GB300 through the library's C ABI.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
-                  [--workload {gemm,softmax}] [--configs]
+                  [--workload {gemm,softmax}] [--configs] [--sustained SECONDS]
 
 A step is one C = A.B call on the 8192 x 8192 x 8192 workload (A, B drawn N(0,1) from
 seed 4, rounded to FP16).  The inputs (256 MiB) are larger than L2, so no flush is needed
@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--workload", choices=["gemm", "softmax"], default="gemm")
     ap.add_argument("--configs", action="store_true",
                     help="instead of the benchmark line, time every workload shape (one JSON line each)")
+    ap.add_argument("--sustained", type=float, default=0.0, metavar="SECONDS",
+                    help="instead of the benchmark line, run 4096^3 and 8192^3 back to back for SECONDS each "
+                         "and report TFLOP/s with the SM clocks and power seen (one JSON line each)")
     return ap.parse_args()
 
 
@@ -850,6 +853,63 @@ def run_softmax(args):
     return 0
 
 
+def run_sustained(args):
+    """4096^3 and 8192^3 launched back to back for args.sustained seconds each (after a
+    second of warm-up): whole-loop TFLOP/s by CUDA events, with the median SM clock, the
+    largest power draw and the throttle reasons nvidia-smi reported during the loop."""
+    import torch
+
+    import tensor_core_tiled_gb300 as tct
+    from tensor_core_tiled_gb300 import build as lib_build
+
+    lib_build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peak_burst, peak_sus, _ = peaks()
+    sampler = ClockSampler(0)
+    sampler.start()
+    try:
+        for n, seed in ((4096, 2), (8192, SEED)):
+            g = torch.Generator(device=dev).manual_seed(seed)
+            A = torch.randn(n, n, device=dev, generator=g).half()
+            B = torch.randn(n, n, device=dev, generator=g).half()
+            C = torch.empty(n, n, device=dev)
+            t_end = time.time() + 1.0
+            while time.time() < t_end:
+                for _ in range(20):
+                    tct.matmul(A, B, C)
+                torch.cuda.synchronize()
+            # launches per batch sized to about 0.1 s, batches until the time is up
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(10):
+                tct.matmul(A, B, C)
+            e1.record()
+            torch.cuda.synchronize()
+            per = max(1, int(0.1 / (e0.elapsed_time(e1) / 10 / 1e3)))
+            launches = 0
+            t0 = time.time()
+            e0.record()
+            while time.time() - t0 < args.sustained:
+                for _ in range(per):
+                    tct.matmul(A, B, C)
+                launches += per
+                torch.cuda.synchronize()
+            e1.record()
+            torch.cuda.synchronize()
+            t1 = time.time()
+            ms = e0.elapsed_time(e1) / launches
+            tflops = 2 * n ** 3 / ms / 1e9
+            print(json.dumps({"workload": f"gemm_f16_f32 {n}^3 back to back", "seconds": round(t1 - t0, 2),
+                              "launches": launches, "ms_per_launch": ms, "tflops": tflops,
+                              "frac_of_sustained": tflops / peak_sus if peak_sus else None,
+                              "frac_of_burst": tflops / peak_burst, "clocks": sampler.summary(t0, t1),
+                              "device_status": tct.gemm_f16_f32_get_error()}), flush=True)
+            del A, B, C
+    finally:
+        sampler.stop()
+
+
 def main():
     args = parse()
     if args.workload == "softmax":
@@ -860,6 +920,8 @@ def main():
         return run_reference(args)
     if args.configs:
         return run_configs(args)
+    if args.sustained > 0:
+        return run_sustained(args)
     return run_ours(args)
 
 
