@@ -173,6 +173,16 @@ def test_planner_on_gb300_shapes(tct_lib):
     p = tct.gemm_f16_f32_plan(128, 16384, 16384, num_sms=sms)
     busy = p["cta_group"] * min(p["units"], p["tiles"] * (2 if p["stream_k_tiles"] else 1))
     assert busy >= 128
+    # rows of C that end inside a 16-byte unit cannot be written by TMA: their split tiles
+    # would combine through workspace (a helper takes one part, at a higher fixed cost), so
+    # the same tile grid that splits with N % 4 == 0 keeps whole waves with N % 4 != 0
+    p = tct.gemm_f16_f32_plan(6144, 6140, 6144, num_sms=sms)
+    assert (p["stream_k_tiles"], p["split_parts_per_unit"]) == (44, 2)
+    for n in (6142, 6143):
+        p = tct.gemm_f16_f32_plan(6144, n, 6144, num_sms=sms)
+        assert p["tiles"] == 576 and p["stream_k_tiles"] == 0
+    assert tct.gemm_f16_f32_plan(4096, 4092, 4096, num_sms=sms)["stream_k_tiles"] == 28
+    assert tct.gemm_f16_f32_plan(4096, 4094, 4096, num_sms=sms)["stream_k_tiles"] == 0
     # ragged leading dimensions are repacked before TMA
     p = tct.gemm_f16_f32_plan(17, 4097, 31, num_sms=sms)
     assert p["pack_a"] == 1 and p["pack_b"] == 1
