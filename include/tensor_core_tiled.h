@@ -91,8 +91,10 @@ TCT_API gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t
  *               tiles are never published (the owner neither zeroes nor flags its tile, or
  *               the helper never flags its part), so the waits for them run until timeout_ms,
  *               record GEMM_ERR_DEVICE_TIMEOUT (read by gemm_f16_f32_get_error) and return
- *               without storing those tiles.  Nothing faults, traps or hangs; later calls are
- *               unaffected.
+ *               without storing those tiles.  Bit 1 (gemm_ex with beta != 0 on a C that TMA
+ *               writes): the epilogue never loads C's blocks, so its waits for them run out
+ *               the same way and no tile is stored.  Nothing faults, traps or hangs; later
+ *               calls are unaffected.  Values above 3 are rejected.
  */
 typedef struct gemm_options {
     int32_t group_m;

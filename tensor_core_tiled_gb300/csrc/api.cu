@@ -154,7 +154,7 @@ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 gemm_status check_options(const gemm_options *opt)
 {
     if (!opt) return GEMM_OK;
-    if (opt->fault_inject < 0 || opt->fault_inject > 1) return GEMM_ERR_INVALID_ARG;
+    if (opt->fault_inject < 0 || opt->fault_inject > 3) return GEMM_ERR_INVALID_ARG;
     if (opt->stream_k < 0 || opt->stream_k > 2) return GEMM_ERR_INVALID_ARG;
     if (opt->group_m < 0 || opt->group_m > 256) return GEMM_ERR_INVALID_ARG;
     if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return GEMM_ERR_INVALID_ARG;

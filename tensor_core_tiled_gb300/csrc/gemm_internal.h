@@ -41,7 +41,8 @@ struct KernelParams {
     int32_t split_kb;  // first k-block of a split tile's second part (the owner takes [0, split_kb))
     float *workspace;
     unsigned int *flags;
-    int32_t fault_inject;  // bit 0: never publish a split tile (its part, or its zeroed C rows)
+    int32_t fault_inject;  // bit 0: never publish a split tile (its part, or its zeroed C rows);
+                           // bit 1: never issue the TMA loads of C (beta != 0)
     // How split tiles are combined.  0: the second half goes through workspace and the owner
     // adds it (any epilogue).  1 (plain FP32 epilogue, C TMA-addressable): the owner zeroes
     // its rows of the tile in C at kernel start and raises flag[part * cta_group + rank]; both

@@ -359,14 +359,15 @@ __device__ __forceinline__ uint32_t pack_16bit(float a, float b, int type)
 // hardware clips boxes that reach past C.  With kOwnBlocks, `stage` holds one 4 KB block
 // (1024-byte aligned) per block of the accumulator, all C loads are issued at once and the
 // copies go out back to back; otherwise it is one block, reused once the previous copy has
-// read it.  Returns false if a C load did not arrive in time (after recording the timeout);
+// read it.  `skip_c_load` (fault injection) never issues the C loads, so their waits run
+// out.  Returns false if a C load did not arrive in time (after recording the timeout);
 // else once the copies have read shared memory, and with kOwnBlocks once they have completed.
 // `release` is called by lane 0 once every column has been read from TMEM.
 template <int BN, bool kReduce, bool kOwnBlocks, bool kWide, typename Release>
 __device__ __forceinline__ bool bulk_accumulator(uint32_t t_row, const void *tmap_c, int64_t row0, int64_t col0,
                                                  const TileDst &d, const float *sbias, float *stage, int lane,
                                                  uint32_t cbar, uint32_t &cphase, uint64_t limit,
-                                                 volatile int *abort_flag, Release release)
+                                                 volatile int *abort_flag, bool skip_c_load, Release release)
 {
     static_assert(!(kReduce && kWide), "reduce-add of FP32 only");
     constexpr int kCols = kWide ? 64 : 32;  // columns per staged block (128-byte rows)
@@ -384,7 +385,7 @@ __device__ __forceinline__ bool bulk_accumulator(uint32_t t_row, const void *tma
         int n = 0;
         for (int blk = 0; blk < kBlocks; ++blk) n += block_in(blk) ? 1 : 0;
         if (n > 0) {
-            if (lane == 0) {
+            if (lane == 0 && !skip_c_load) {
                 mbar_arrive_expect_tx(cbar, n * 4096u);
                 for (int blk = 0; blk < kBlocks; ++blk)
                     if (block_in(blk)) load_c(blk, stage + blk * 32 * 32);
@@ -405,7 +406,7 @@ __device__ __forceinline__ bool bulk_accumulator(uint32_t t_row, const void *tma
                 __syncwarp();
             }
             if (read_c && block_in(blk)) {
-                if (lane == 0) {
+                if (lane == 0 && !skip_c_load) {
                     mbar_arrive_expect_tx(cbar, 4096u);
                     load_c(blk, block);
                 }
@@ -801,6 +802,7 @@ __global__ void __launch_bounds__(192, 1)
             WorkItem next;
             const bool own_blocks = Cf::SPLIT_OK && !work_item(p, unit, it + 1, next);
             const uint32_t cb = cload_bar(warp - 2);
+            const bool skip_c = (p.fault_inject & 2) != 0;
             float *blocks = reinterpret_cast<float *>(sA) + (warp - 2) * 32 * BN;
             if (p.split_mode == 1 && w.mode != WORK_STORE) {
                 ok = wait_flag(p.flags + w.part * CG + rank, limit, abort_flag);
@@ -809,10 +811,10 @@ __global__ void __launch_bounds__(192, 1)
                 fence_proxy_async_all();  // the owner's zeros (generic writes) before the reduce
                 if (own_blocks)
                     ok = bulk_accumulator<BN, true, true, false>(t_row0, &tmC, row_base, col_base, d, sbias, blocks, lane, cb,
-                                                                 cphase, limit, abort_flag, release);
+                                                                 cphase, limit, abort_flag, skip_c, release);
                 else
                     ok = bulk_accumulator<BN, true, false, false>(t_row0, &tmC, row_base, col_base, d, sbias, stage, lane, cb,
-                                                                  cphase, limit, abort_flag, release);
+                                                                  cphase, limit, abort_flag, skip_c, release);
                 if (!ok) break;
                 continue;
             }
@@ -820,17 +822,17 @@ __global__ void __launch_bounds__(192, 1)
                 if (p.c_type == 2) {
                     if (own_blocks)
                         ok = bulk_accumulator<BN, false, true, false>(t_row0, &tmC, row_base, col_base, d, sbias, blocks, lane,
-                                                                      cb, cphase, limit, abort_flag, release);
+                                                                      cb, cphase, limit, abort_flag, skip_c, release);
                     else
                         ok = bulk_accumulator<BN, false, false, false>(t_row0, &tmC, row_base, col_base, d, sbias, stage, lane,
-                                                                       cb, cphase, limit, abort_flag, release);
+                                                                       cb, cphase, limit, abort_flag, skip_c, release);
                 } else {
                     if (own_blocks)
                         ok = bulk_accumulator<BN, false, true, true>(t_row0, &tmC, row_base, col_base, d, sbias, blocks, lane,
-                                                                     cb, cphase, limit, abort_flag, release);
+                                                                     cb, cphase, limit, abort_flag, skip_c, release);
                     else
                         ok = bulk_accumulator<BN, false, false, true>(t_row0, &tmC, row_base, col_base, d, sbias, stage, lane,
-                                                                      cb, cphase, limit, abort_flag, release);
+                                                                      cb, cphase, limit, abort_flag, skip_c, release);
                 }
                 if (!ok) break;
                 continue;

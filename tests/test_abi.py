@@ -78,7 +78,7 @@ def test_invalid_arguments_rejected_before_any_device_work(tct_lib):
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, group_m=-1) == tct.GEMM_ERR_INVALID_ARG
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, cta_group=3) == tct.GEMM_ERR_INVALID_ARG
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, stream_k=3) == tct.GEMM_ERR_INVALID_ARG
-    assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, fault_inject=2) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, fault_inject=4) == tct.GEMM_ERR_INVALID_ARG
     # generalised entry: bad type or op, and leading dimensions checked against the storage
     assert tct.gemm_f32acc(2, 0, 0, p, p, p, 4, 4, 4, 4, 4, 4, 0) == tct.GEMM_ERR_INVALID_ARG
     assert tct.gemm_f32acc(0, 2, 0, p, p, p, 4, 4, 4, 4, 4, 4, 0) == tct.GEMM_ERR_INVALID_ARG

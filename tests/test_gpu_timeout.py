@@ -6,8 +6,9 @@ own copies and MMAs, frees tensor memory) and returns.  The test injects the fai
 the host: with fault_inject bit 0 a split tile is never published -- with the plain FP32
 epilogue its owner never zeroes and flags its rows of C, so both halves' waits to add into
 C run out; with an epilogue the second half's unit never publishes its part, so the
-owner's wait runs out.  Either way the wait is on a flag nothing sets.  The host reads the
-status, and the same context then computes a correct product.
+owner's wait runs out.  Either way the wait is on a flag nothing sets.  With bit 1 and
+beta != 0 the epilogue's TMA loads of C are never issued, so its waits for C's blocks run
+out.  The host reads the status, and the same context then computes a correct product.
 """
 import time
 
@@ -67,3 +68,32 @@ def test_unpublished_part_times_out_and_context_survives(opts, through_workspace
     C2 = tct.matmul(dA, dB, stream_k=2, **opts)
     assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
     assert within_tol(C2.cpu().numpy(), oracle.gemm_f32(A, B), K)
+
+
+@pytest.mark.parametrize("c_dtype", [torch.float32, torch.bfloat16])
+def test_missing_c_load_times_out_and_context_survives(c_dtype):
+    """beta != 0 with a C that TMA writes: the epilogue TMA-loads each block of C before it
+    adds beta * C; with fault_inject bit 1 those loads are never issued, every epilogue's
+    first wait runs out, nothing is stored, and the next call is correct."""
+    M, N, K = 1000, 1024, 256
+    rng = np.random.default_rng(52)
+    A, B = inputs.normal_pair(rng, M, N, K)
+    dA, dB = _dev16(A), _dev16(B)
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    C0 = torch.randn(M, N, device="cuda").to(c_dtype)
+    C = C0.clone()
+    t0 = time.time()
+    tct.gemm(dA, dB, C, beta=1.0, timeout_ms=50, fault_inject=2, stream_k=1)  # whole tiles only
+    status = tct.gemm_f16_f32_get_error()
+    assert status == tct.GEMM_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 5.0
+    assert torch.equal(C.view(torch.int16 if c_dtype != torch.float32 else torch.int32),
+                       C0.view(torch.int16 if c_dtype != torch.float32 else torch.int32))
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    tct.gemm(dA, dB, C, beta=1.0)
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    want = oracle.gemm_f32(A, B).astype(np.float64) + C0.double().cpu().numpy()
+    got = C.double().cpu().numpy()
+    ulp = 0.0 if c_dtype == torch.float32 else 2.0 ** -7
+    tol = 1e-3 * np.sqrt(K) * np.maximum(1.0, np.abs(want)) + 2 * ulp * np.abs(want)
+    assert np.all(np.abs(got - want) <= tol)
