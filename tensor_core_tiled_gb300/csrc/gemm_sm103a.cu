@@ -569,6 +569,9 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t limit = p.timeout_ns;
+    // Everything above touched only shared memory, tensor memory and the parameters, so it
+    // may overlap the end of the previous grid on the stream; global memory waits for it.
+    griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -632,6 +635,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
+            griddep_launch_dependents();  // every load issued: the next grid may start launching
             if (ok) {
                 // Tail: wait until the MMAs have released every stage, so that no arrival is
                 // still on its way to this CTA's shared memory when it exits.
@@ -993,8 +997,12 @@ static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<CG, BN, STAGES>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = launch_config<CG, BN, STAGES>(grid, stream, attr);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config<CG, BN, STAGES>(grid, stream, attr);
+    // programmatic dependent launch: the prologue may overlap the previous kernel's end
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     if (p.split_tiles > 0 && !Cfg<CG, BN, STAGES>::SPLIT_OK) return cudaErrorInvalidValue;
     e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tp, tc, p);
     if (e != cudaSuccess) return e;

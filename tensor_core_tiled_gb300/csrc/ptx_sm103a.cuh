@@ -80,6 +80,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// Programmatic dependent launch: wait until the grid this launch depends on has completed
+// and its memory is visible (returns at once when there is none), and let the grids that
+// depend on this one begin launching (they still wait for this grid's completion before
+// touching its results).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)
