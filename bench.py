@@ -19,7 +19,6 @@ write MN), with the page's own 4096 x 1024 case (L2 flushed before each launch) 
 """
 import argparse
 import hashlib
-import re
 import json
 import os
 import statistics
@@ -106,16 +105,39 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_text(text):
+    """C/C++ source with its comments removed and its whitespace collapsed to single spaces
+    (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_hash(sources=KERNEL_SOURCES):
     """Hash of the device sources' code: comments and layout are left out, so that an edit
     of a comment does not retire a profile taken on the same code."""
     h = hashlib.sha256()
     for name in sources:
         with open(os.path.join(ROOT, "tensor_core_tiled_gb300", "csrc", name), encoding="utf-8") as f:
-            text = f.read()
-        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-        text = re.sub(r"//[^\n]*", " ", text)
-        h.update(" ".join(text.split()).encode())
+            h.update(code_text(f.read()).encode())
     return h.hexdigest()[:16]
 
 
