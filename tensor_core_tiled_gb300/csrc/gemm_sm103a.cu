@@ -26,10 +26,15 @@
 //   * A persistent grid walks the tiles in GROUP_M launch order ("06_triton_style.py",
 //     matmul_kernel / demo 2) for L2 reuse.
 //   * Ragged shapes ("06_triton_style.py", matmul_kernel masks): TMA fills out-of-range
-//     operand elements with zeros (the masked load with other = 0) and the epilogue
-//     predicates every store on row < M and column < N (the masked store).
-//   * Every pipeline wait is bounded in wall time; on expiry the CTA records an error
-//     code in a device word, drains its own copies and MMAs, frees TMEM and returns.
+//     operand elements with zeros (the masked load with other = 0); the epilogue writes C
+//     with TMA stores from swizzled staging blocks where the hardware clips rows >= M and
+//     columns >= N (the masked store), or, where TMA cannot write C, with per-lane stores
+//     predicated on row < M and column < N.
+//   * Every pipeline wait sleeps in hardware (mbarrier try_wait with a suspend-time hint)
+//     and is bounded in wall time; on expiry the CTA records an error code in a device
+//     word, drains its own copies and MMAs, frees TMEM and returns.
+//   * Launched as a programmatic dependent launch: the set-up may overlap the previous
+//     kernel on the stream; global memory is touched only after waiting for it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
