@@ -16,6 +16,8 @@
 //     every CTA reduces its slice to (max, sum), sends the pair to every CTA of the cluster
 //     through distributed shared memory (st.async, counted on the receiver's mbarrier), and
 //     rescales its slice by exp(max_slice - max_row) / sum_row.
+// The team kernels launch as programmatic dependent launches: their barrier set-up may
+// overlap the previous kernel on the stream, and X and Y are touched only after waiting for it.
 // Other layouts (and rows beyond 16 slices of 96 KB) take the plain kernels below: a warp per
 // row held in registers, a CTA per row staged in shared memory, or two passes over the row.
 // exp(-inf) = 0; a row holding a NaN, whose maximum is +inf, or that is all -inf has no
