@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "gemm_internal.h"
 #include "ptx_sm103a.cuh"
@@ -813,36 +814,27 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t cb = cload_bar(warp - 2);
             const bool skip_c = (p.fault_inject & 2) != 0;
             float *blocks = reinterpret_cast<float *>(sA) + (warp - 2) * 32 * BN;
+            // One accumulator out by TMA: reduce-add (split half, FP32) or store, 16-bit (wide) or
+            // FP32 blocks; staged in its own blocks when it is the unit's last.
+            auto bulk = [&](auto reduce, auto wide) {
+                constexpr bool kReduce = decltype(reduce)::value, kWide = decltype(wide)::value;
+                return own_blocks ? bulk_accumulator<BN, kReduce, true, kWide>(t_row0, &tmC, row_base, col_base, d, sbias,
+                                                                              blocks, lane, cb, cphase, limit, abort_flag,
+                                                                              skip_c, release)
+                                  : bulk_accumulator<BN, kReduce, false, kWide>(t_row0, &tmC, row_base, col_base, d, sbias,
+                                                                               stage, lane, cb, cphase, limit, abort_flag,
+                                                                               skip_c, release);
+            };
             if (p.split_mode == 1 && w.mode != WORK_STORE) {
                 ok = wait_flag(p.flags + w.part * CG + rank, limit, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 fence_proxy_async_all();  // the owner's zeros (generic writes) before the reduce
-                if (own_blocks)
-                    ok = bulk_accumulator<BN, true, true, false>(t_row0, &tmC, row_base, col_base, d, sbias, blocks, lane, cb,
-                                                                 cphase, limit, abort_flag, skip_c, release);
-                else
-                    ok = bulk_accumulator<BN, true, false, false>(t_row0, &tmC, row_base, col_base, d, sbias, stage, lane, cb,
-                                                                  cphase, limit, abort_flag, skip_c, release);
-                if (!ok) break;
+                if (!bulk(std::true_type{}, std::false_type{})) break;
                 continue;
             }
             if (p.c_tma && w.mode == WORK_STORE) {
-                if (p.c_type == 2) {
-                    if (own_blocks)
-                        ok = bulk_accumulator<BN, false, true, false>(t_row0, &tmC, row_base, col_base, d, sbias, blocks, lane,
-                                                                      cb, cphase, limit, abort_flag, skip_c, release);
-                    else
-                        ok = bulk_accumulator<BN, false, false, false>(t_row0, &tmC, row_base, col_base, d, sbias, stage, lane,
-                                                                       cb, cphase, limit, abort_flag, skip_c, release);
-                } else {
-                    if (own_blocks)
-                        ok = bulk_accumulator<BN, false, true, true>(t_row0, &tmC, row_base, col_base, d, sbias, blocks, lane,
-                                                                     cb, cphase, limit, abort_flag, skip_c, release);
-                    else
-                        ok = bulk_accumulator<BN, false, false, true>(t_row0, &tmC, row_base, col_base, d, sbias, stage, lane,
-                                                                      cb, cphase, limit, abort_flag, skip_c, release);
-                }
+                ok = p.c_type == 2 ? bulk(std::false_type{}, std::false_type{}) : bulk(std::false_type{}, std::true_type{});
                 if (!ok) break;
                 continue;
             }
