@@ -2,12 +2,22 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
                   [--workload {gemm,softmax}] [--configs] [--sustained SECONDS]
+                  [--sustained-leg SECONDS]
+  python bench.py --case M N K [--launches L] [--warmup W] [--cta-group G] [--tile-n T]
+                  [--stages S] [--group-m G] [--max-ctas C] [--stream-k 0|1|2] [--flush-l2]
 
 A step is one C = A.B call on the 8192 x 8192 x 8192 workload (A, B drawn N(0,1) from
 seed 4, rounded to FP16).  The inputs (256 MiB) are larger than L2, so no flush is needed
 between steps.  Prints one JSON line (rank 0).  Under torchrun with N > 1 every rank runs
 its own replica on its own GPU (the problem does not need a collective); the time is the
 maximum over ranks and the value the aggregate throughput.
+
+After the timed steps the line adds: the end-to-end figure through the host-buffer call,
+4096^3 with L2 flushed before each launch (`secondary`), 8192^3 with L2 flushed (`cold_l2`),
+and 4096^3 and 8192^3 back to back for --sustained-leg seconds with the SM clock sampled
+inside each loop (`sustained`).  The roofline's `frac` divides by the measured cuBLAS bf16
+peak; `frac_per_clock` divides the sustained 8192^3 rate by SMs x 8192 FLOP/clk x the median
+SM clock of that loop, the device's dense FP16 rate at the clock it actually ran.
 
 --impl reference times the CPU oracle (the plain FP64-accumulating definition) on the
 host cores over a bounded sample of the same workload.
@@ -38,6 +48,10 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAK_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
 SUSTAINED_SECONDS = 0.25
+# Dense FP16/BF16 tensor rate of one SM per clock (kind::f16 MMAs with FP32 accumulation):
+# the per-clock denominator, peak = SMs x this x SM clock.
+TENSOR_FLOP_PER_CLK_SM = 8192
+MAX_SM_MHZ = 2070.0
 # device code of the measured kernels (a committed ncu figure holds while these are unchanged
 # and the plan it was taken with is the plan the bench runs)
 KERNEL_SOURCES = ("gemm_sm103a.cu", "ptx_sm103a.cuh", "tile_sched.h", "gemm_internal.h")
@@ -63,6 +77,21 @@ def parse():
     ap.add_argument("--sustained", type=float, default=0.0, metavar="SECONDS",
                     help="instead of the benchmark line, run 4096^3 and 8192^3 back to back for SECONDS each "
                          "and report TFLOP/s with the SM clocks and power seen (one JSON line each)")
+    ap.add_argument("--sustained-leg", type=float, default=4.0, metavar="SECONDS",
+                    help="length of the back-to-back 4096^3 and 8192^3 loops that follow the timed steps in the "
+                         "benchmark line (clock-sampled; they give the per-clock fraction); 0 leaves them out")
+    # one shape, for profiling and sweeps
+    ap.add_argument("--case", type=int, nargs=3, metavar=("M", "N", "K"),
+                    help="instead of the benchmark line, time C = A.B on one shape (inputs drawn on the device) "
+                         "and print the per-launch device times")
+    ap.add_argument("--launches", type=int, default=3, help="--case: timed launches")
+    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--group-m", type=int, default=0)
+    ap.add_argument("--max-ctas", type=int, default=0)
+    ap.add_argument("--cta-group", type=int, default=0)
+    ap.add_argument("--stream-k", type=int, default=0, help="--case: 1 = whole tiles only, 2 = force split tiles")
+    ap.add_argument("--flush-l2", action="store_true", help="--case: write 512 MiB before each launch")
     return ap.parse_args()
 
 
@@ -272,6 +301,42 @@ def cpu_baseline(A, B, target_seconds):
     return _baseline_record(A, B, rows, secs, flops)
 
 
+def back_to_back(launch, seconds, sampler, warm_seconds=1.0):
+    """Launches `launch` back to back for `seconds` (after `warm_seconds` of warm-up), in
+    batches of about 0.1 s, timed by one CUDA event pair around the whole loop; the clocks
+    are the sampler's summary over the loop.  Returns (ms per launch, launches, clocks)."""
+    import torch
+    t_end = time.time() + warm_seconds
+    while time.time() < t_end:
+        for _ in range(10):
+            launch()
+        torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        launch()
+    e1.record()
+    torch.cuda.synchronize()
+    per = max(1, int(0.1 / max(e0.elapsed_time(e1) / 10 / 1e3, 1e-9)))
+    launches = 0
+    t0 = time.time()
+    e0.record()
+    while time.time() - t0 < seconds:
+        for _ in range(per):
+            launch()
+        launches += per
+        torch.cuda.synchronize()
+    e1.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    return e0.elapsed_time(e1) / launches, launches, sampler.summary(t0, t1)
+
+
+def per_clock_peak_tflops(sms, mhz):
+    """Dense FP16 tensor peak of the device at an SM clock of `mhz`, in TFLOP/s."""
+    return sms * TENSOR_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -435,9 +500,46 @@ def run_ours(args):
     sec_tflops = 2.0 * m2 * n2 * k2 / (sec_ms * 1e-3) / 1e12
     assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
 
+    # ---- 8192^3 with L2 flushed (512 MiB written) before each launch: the cold-cache form
+    cold = []
+    cold_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(max(5, min(args.steps, 20)))]
+    for a, b in cold_pairs:
+        flush.fill_(1.0)
+        a.record(stream)
+        launch()
+        b.record(stream)
+    torch.cuda.synchronize()
+    cold = [a.elapsed_time(b) for a, b in cold_pairs]
+    cold_ms = statistics.mean(cold)
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+
+    # ---- back-to-back loops of 4096^3 and 8192^3 under the power cap, clocks sampled inside
+    # the loop: the sustained figures and, from time x median clock, the per-clock fraction
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sustained = {}
+    if args.sustained_leg > 0:
+        sampler2 = ClockSampler(local)
+        sampler2.start()
+        try:
+            for name, fn, f in (("4096^3", launch2, 2.0 * m2 * n2 * k2), ("8192^3", launch, flops)):
+                ms_l, n_l, clk = back_to_back(fn, args.sustained_leg, sampler2)
+                tf = f / (ms_l * 1e-3) / 1e12
+                mhz = clk.get("sm_mhz")
+                sustained[name] = {
+                    "seconds": args.sustained_leg, "launches": n_l, "ms_per_launch": ms_l, "tflops": tf,
+                    "sm_mhz_median": mhz, "clocks": clk,
+                    "cycles_per_launch": ms_l * 1e-3 * mhz * 1e6 if mhz else None,
+                    "frac_per_clock": tf / per_clock_peak_tflops(sms, mhz) if mhz else None}
+        finally:
+            sampler2.stop()
+        assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+
     peak_burst, peak_sustained, peak_src = peaks()
     mean_launch = statistics.mean(launch_ms)
     achieved = flops / (mean_launch * 1e-3) / 1e12
+    clock_peak_max = per_clock_peak_tflops(sms, MAX_SM_MHZ)
+    s8 = sustained.get("8192^3", {})
     # A timed region of back-to-back launches longer than SUSTAINED_SECONDS runs under the
     # power cap: compare it with the sustained library figure, a short one with the burst one.
     region_s = total_ms * 1e-3
@@ -467,7 +569,14 @@ def run_ours(args):
                          "peak_burst": peak_burst, "frac_of_burst": achieved / peak_burst,
                          "peak_sustained": peak_sustained,
                          "frac_of_sustained": (achieved / peak_sustained) if peak_sustained else None,
-                         "kernel_ms_mean": mean_launch, "kernel_ms_min": min(launch_ms)},
+                         "kernel_ms_mean": mean_launch, "kernel_ms_min": min(launch_ms),
+                         # the per-clock denominator: SMs x 8192 FLOP/clk x SM clock
+                         "per_clock_peak_at_max_clock": clock_peak_max,
+                         "frac_of_per_clock_peak_at_max_clock": achieved / clock_peak_max,
+                         "frac_per_clock": s8.get("frac_per_clock"),
+                         "frac_per_clock_source": (f"8192^3 back to back for {args.sustained_leg:g} s: "
+                                                   f"TFLOP/s / ({sms} SMs x {TENSOR_FLOP_PER_CLK_SM} FLOP/clk x "
+                                                   f"median SM clock sampled inside the loop)") if s8 else None},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(dA.numel() * 2 + dB.numel() * 2),
                     "d2h_bytes_per_step": int(dC.numel() * 4), "steps": e2e_steps, "ms_per_step": e2e_ms,
                     "api": "gemm_f16_f32_host (pinned host buffers; 4x4 blocks pipelined over H2D, GEMM, D2H)"},
@@ -476,7 +585,12 @@ def run_ours(args):
             "secondary": {"workload": f"gemm_f16_f32 {m2}x{n2}x{k2}, seed 2, L2 flushed before each launch",
                           "value": sec_tflops, "unit": UNIT, "frac_of_burst": sec_tflops / peak_burst,
                           "ms_mean": sec_ms, "launches": n_sec,
-                          "tile": [plan2["tile_m"], plan2["tile_n"], plan2["tile_k"]], "waves": plan2["waves"]},
+                          "tile": [plan2["tile_m"], plan2["tile_n"], plan2["tile_k"]], "waves": plan2["waves"],
+                          "frac_of_per_clock_peak_at_max_clock": sec_tflops / clock_peak_max},
+            "cold_l2": {"workload": f"gemm_f16_f32 {M}x{N}x{K}, seed {SEED}, L2 flushed (512 MiB written) "
+                                    f"before each launch", "value": flops / (cold_ms * 1e-3) / 1e12, "unit": UNIT,
+                        "ms_mean": cold_ms, "launches": len(cold)},
+            "sustained": sustained,
             "kernel_hash": kernel_hash(),
         }
     if dist:
@@ -889,6 +1003,7 @@ def run_sustained(args):
     lib_build.build()
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     peak_burst, peak_sus, _ = peaks()
     sampler = ClockSampler(0)
     sampler.start()
@@ -898,40 +1013,64 @@ def run_sustained(args):
             A = torch.randn(n, n, device=dev, generator=g).half()
             B = torch.randn(n, n, device=dev, generator=g).half()
             C = torch.empty(n, n, device=dev)
-            t_end = time.time() + 1.0
-            while time.time() < t_end:
-                for _ in range(20):
-                    tct.matmul(A, B, C)
-                torch.cuda.synchronize()
-            # launches per batch sized to about 0.1 s, batches until the time is up
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(10):
-                tct.matmul(A, B, C)
-            e1.record()
-            torch.cuda.synchronize()
-            per = max(1, int(0.1 / (e0.elapsed_time(e1) / 10 / 1e3)))
-            launches = 0
-            t0 = time.time()
-            e0.record()
-            while time.time() - t0 < args.sustained:
-                for _ in range(per):
-                    tct.matmul(A, B, C)
-                launches += per
-                torch.cuda.synchronize()
-            e1.record()
-            torch.cuda.synchronize()
-            t1 = time.time()
-            ms = e0.elapsed_time(e1) / launches
+            ms, launches, clk = back_to_back(lambda: tct.matmul(A, B, C), args.sustained, sampler)
             tflops = 2 * n ** 3 / ms / 1e9
-            print(json.dumps({"workload": f"gemm_f16_f32 {n}^3 back to back", "seconds": round(t1 - t0, 2),
+            mhz = clk.get("sm_mhz")
+            print(json.dumps({"workload": f"gemm_f16_f32 {n}^3 back to back", "seconds": args.sustained,
                               "launches": launches, "ms_per_launch": ms, "tflops": tflops,
                               "frac_of_sustained": tflops / peak_sus if peak_sus else None,
-                              "frac_of_burst": tflops / peak_burst, "clocks": sampler.summary(t0, t1),
-                              "device_status": tct.gemm_f16_f32_get_error()}), flush=True)
+                              "frac_of_burst": tflops / peak_burst,
+                              "frac_per_clock": tflops / per_clock_peak_tflops(sms, mhz) if mhz else None,
+                              "clocks": clk, "device_status": tct.gemm_f16_f32_get_error()}), flush=True)
             del A, B, C
     finally:
         sampler.stop()
+
+
+def run_case(args):
+    """One shape, a few launches: per-launch device times (CUDA events), the launch plan and
+    the device status, as one JSON line.  Inputs are N(0,1) FP16 drawn on the device, so the
+    command starts quickly; meant for profiling one kernel on a chosen shape and for sweeps."""
+    import torch
+
+    import tensor_core_tiled_gb300 as tct
+    from tensor_core_tiled_gb300 import build as lib_build
+
+    lib_build.build()
+    torch.cuda.set_device(0)
+    M, N, K = args.case
+    g = torch.Generator(device="cuda").manual_seed(0)
+    A = torch.randn(M, K, device="cuda", generator=g).half()
+    B = torch.randn(K, N, device="cuda", generator=g).half()
+    C = torch.empty(M, N, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device="cuda") if args.flush_l2 else None
+    opts = dict(tile_n=args.tile_n, stages=args.stages, group_m=args.group_m, max_ctas=args.max_ctas,
+                cta_group=args.cta_group, stream_k=args.stream_k)
+    opts = {k: v for k, v in opts.items() if v}
+    for _ in range(args.warmup):
+        tct.matmul(A, B, C, **opts)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.launches):
+        if flush is not None:
+            flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        tct.matmul(A, B, C, **opts)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    st = tct.gemm_f16_f32_get_error()
+    flops = 2.0 * M * N * K
+    best = min(times)
+    plan = tct.gemm_f16_f32_plan(M, N, K, **opts)
+    print(json.dumps({"shape": [M, N, K], "opts": opts, "ms": times, "best_ms": best,
+                      "median_ms": statistics.median(times), "tflops_best": flops / best / 1e9,
+                      "tflops_median": flops / statistics.median(times) / 1e9, "plan": plan,
+                      "device_status": st}), flush=True)
+    if st != tct.GEMM_OK:
+        raise SystemExit(f"device status {st}")
+    return 0
 
 
 def main():
@@ -942,6 +1081,8 @@ def main():
         return run_softmax_configs(args) if args.configs else run_softmax(args)
     if args.impl == "reference":
         return run_reference(args)
+    if args.case:
+        return run_case(args)
     if args.configs:
         return run_configs(args)
     if args.sustained > 0:

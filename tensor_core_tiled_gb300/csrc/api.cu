@@ -781,10 +781,15 @@ extern "C" gemm_status gemm_f16_f32_noalloc(const void *A, const void *B, float 
     // Scratch needed for the repacked operands, checked against the fixed array first.
     const bool pack_a = K > 0 && !tma_ok(A, lda);
     const bool pack_b = K > 0 && !tma_ok(B, ldb);
+    // Each size is compared with the limit before it is formed, so that no product or sum
+    // can wrap around for the largest dimensions check_args accepts.
+    constexpr int64_t kLimit = static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_BYTES);
     const int64_t lda_p = round_up(K, 8), ldb_p = round_up(N, 8);
+    if (pack_a && M > kLimit / (2 * lda_p)) return GEMM_ERR_INVALID_ARG;
+    if (pack_b && K > kLimit / (2 * ldb_p)) return GEMM_ERR_INVALID_ARG;
     const int64_t a_bytes = pack_a ? round_up(M * lda_p * 2, 256) : 0;
     const int64_t b_bytes = pack_b ? round_up(K * ldb_p * 2, 256) : 0;
-    if (a_bytes + b_bytes > static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_BYTES)) return GEMM_ERR_INVALID_ARG;
+    if (a_bytes > kLimit || b_bytes > kLimit - a_bytes) return GEMM_ERR_INVALID_ARG;
 
     DeviceInfo dev;
     st = device_info(&dev);

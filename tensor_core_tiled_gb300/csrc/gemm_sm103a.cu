@@ -907,49 +907,75 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------- helper kernels
 
 // Row copy into buffers whose rows start on 16-byte boundaries (TMA's stride rule), for up
-// to two operands in one launch: blockIdx.y < rows0 copies row blockIdx.y of operand 0, the
-// rest copy rows of operand 1.  Each thread moves 8 consecutive elements (16 bytes) of one
-// row.  A source row may start on any 2-byte boundary, so the 16 bytes generally straddle
-// two aligned 16-byte blocks: both are loaded whole and the bytes realigned with funnel
-// shifts.  Each of the two blocks holds at least one byte of the 8 elements, so no load
-// reaches outside the 16-byte blocks the row occupies.  A row's last, partial group of
-// elements is copied element by element.
+// to two operands in one launch: blocks [0, j0.blocks) copy rows of operand 0, the rest rows
+// of operand 1.  A row is copied by a group of g lanes of one warp (g a power of two, the
+// smallest that covers the row's 16-byte units, at most 32), so a warp copies 32 / g short
+// rows at once and a block of kPackWarps warps copies 8 * 32 / g rows; nothing idles on
+// rows much narrower than a block.  Each lane moves 8 consecutive elements (16 bytes) at a
+// time, up to kPackUnroll units loaded before any is stored.  A source row may start on any
+// 2-byte boundary, so 16 bytes generally straddle two aligned 16-byte blocks: both are
+// loaded whole and the bytes realigned with funnel shifts.  Each of the two blocks holds at
+// least one byte of the 8 elements, so no load reaches outside the 16-byte blocks the row
+// occupies.  A row's last, partial group of elements is copied element by element.
+constexpr int kPackWarps = 8;
+constexpr int kPackUnroll = 4;
+
 struct PackJob {
     const uint16_t *src;
     int64_t ld_src;
     uint16_t *dst;
     int64_t ld_dst;
     int64_t rows, cols;
+    int32_t lanes_per_row;  // g
+    int64_t blocks;
 };
 
-__global__ void pack_rows_f16(const PackJob j0, const PackJob j1)
+// Elements [8u, 8u + 8) of a source row starting at `s` (2-byte aligned), realigned.
+__device__ __forceinline__ uint4 load_unit_realigned(const uint16_t *__restrict__ s, int64_t u)
 {
-    const bool first = blockIdx.y < j0.rows;
-    const PackJob &j = first ? j0 : j1;
-    const int64_t r = first ? blockIdx.y : blockIdx.y - j0.rows;
-    const int64_t c8 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
-    if (c8 >= j.cols) return;
-    const uint16_t *s = j.src + r * j.ld_src + c8;
-    uint16_t *d = j.dst + r * j.ld_dst + c8;
-    if (c8 + 8 <= j.cols) {
-        const uintptr_t addr = reinterpret_cast<uintptr_t>(s);
-        const uint32_t off = static_cast<uint32_t>(addr & 15u);  // 0, 2, ..., 14
-        const uint4 *blk = reinterpret_cast<const uint4 *>(addr - off);
-        const uint4 lo = __ldg(blk);
-        const uint4 hi = off ? __ldg(blk + 1) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        const uint32_t q = off >> 2, sh = (off & 3u) * 8u;
-        uint32_t o[4];
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(s + 8 * u);
+    const uint32_t off = static_cast<uint32_t>(addr & 15u);  // 0, 2, ..., 14
+    const uint4 *blk = reinterpret_cast<const uint4 *>(addr - off);
+    const uint4 lo = __ldg(blk);
+    const uint4 hi = off ? __ldg(blk + 1) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t q = off >> 2, sh = (off & 3u) * 8u;
+    uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t a = q == 0 ? w[i] : q == 1 ? w[i + 1] : q == 2 ? w[i + 2] : w[i + 3];
-            const uint32_t b = q == 0 ? w[i + 1] : q == 1 ? w[i + 2] : q == 2 ? w[i + 3] : w[i + 4];
-            o[i] = __funnelshift_r(a, b, sh);
-        }
-        *reinterpret_cast<uint4 *>(d) = make_uint4(o[0], o[1], o[2], o[3]);
-    } else {
-        for (int64_t i = 0; i < j.cols - c8; ++i) d[i] = s[i];
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = q == 0 ? w[i] : q == 1 ? w[i + 1] : q == 2 ? w[i + 2] : w[i + 3];
+        const uint32_t b = q == 0 ? w[i + 1] : q == 1 ? w[i + 2] : q == 2 ? w[i + 3] : w[i + 4];
+        o[i] = __funnelshift_r(a, b, sh);
     }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(kPackWarps * 32) pack_rows_f16(const PackJob j0, const PackJob j1)
+{
+    // The next kernel (the GEMM) may start its set-up; it reads these rows only after its
+    // dependency wait, i.e. after this grid has completed.
+    griddep_launch_dependents();
+    const bool first = blockIdx.x < j0.blocks;
+    const PackJob &j = first ? j0 : j1;
+    const int64_t blk = first ? blockIdx.x : blockIdx.x - j0.blocks;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = j.lanes_per_row;
+    const int64_t r = (blk * kPackWarps + warp) * (32 / g) + lane / g;
+    if (r >= j.rows) return;
+    const int sub = lane & (g - 1);
+    const uint16_t *__restrict__ s = j.src + r * j.ld_src;
+    uint16_t *__restrict__ d = j.dst + r * j.ld_dst;
+    const int64_t units = j.cols / 8;
+    for (int64_t u0 = sub; u0 < units; u0 += kPackUnroll * g) {
+        uint4 v[kPackUnroll];
+#pragma unroll
+        for (int t = 0; t < kPackUnroll; ++t)
+            if (u0 + t * g < units) v[t] = load_unit_realigned(s, u0 + t * g);
+#pragma unroll
+        for (int t = 0; t < kPackUnroll; ++t)
+            if (u0 + t * g < units) *reinterpret_cast<uint4 *>(d + 8 * (u0 + t * g)) = v[t];
+    }
+    for (int64_t i = units * 8 + sub; i < j.cols; i += g) d[i] = s[i];
 }
 
 // K == 0: the empty sum, through the epilogue (C = beta * C + bias[col], or zeros).
@@ -1104,41 +1130,34 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUte
     }
 }
 
+// Lanes per row for a row of `cols` elements: the smallest power of two that covers its
+// 16-byte units, at most a warp.
+static int pack_lanes_per_row(int64_t cols)
+{
+    const int64_t units = (cols + 7) / 8;
+    int g = 1;
+    while (g < 32 && g < units) g *= 2;
+    return g;
+}
+
 cudaError_t launch_pack2(const void *src0, int64_t ld_src0, void *dst0, int64_t ld_dst0, int64_t rows0, int64_t cols0,
                          const void *src1, int64_t ld_src1, void *dst1, int64_t ld_dst1, int64_t rows1, int64_t cols1,
                          cudaStream_t stream)
 {
-    const PackJob j0{static_cast<const uint16_t *>(src0), ld_src0, static_cast<uint16_t *>(dst0), ld_dst0,
-                     src0 ? rows0 : 0, cols0};
-    const PackJob j1{static_cast<const uint16_t *>(src1), ld_src1, static_cast<uint16_t *>(dst1), ld_dst1,
-                     src1 ? rows1 : 0, cols1};
-    const int64_t rows = j0.rows + j1.rows;
-    if (rows <= 0) return cudaSuccess;
-    if (rows > 2147483647ll) return cudaErrorInvalidValue;
-    const int64_t cols = (j0.rows ? cols0 : 0) > (j1.rows ? cols1 : 0) ? cols0 : cols1;
-    const unsigned gx = static_cast<unsigned>(((cols + 7) / 8 + 127) / 128);
-    if (rows <= 65535) {
-        pack_rows_f16<<<dim3(gx, static_cast<unsigned>(rows), 1), 128, 0, stream>>>(j0, j1);
-        return cudaGetLastError();
-    }
-    // gridDim.y is limited to 65535: launch in slices of rows
-    for (int64_t r0 = 0; r0 < rows; r0 += 65535) {
-        const int64_t n = rows - r0 < 65535 ? rows - r0 : 65535;
-        PackJob a = j0, b = j1;
-        // express the slice as rows [r0, r0 + n) of the concatenation
-        const int64_t a_lo = r0 < j0.rows ? r0 : j0.rows, a_hi = (r0 + n) < j0.rows ? r0 + n : j0.rows;
-        a.src = j0.src ? j0.src + a_lo * j0.ld_src : nullptr;
-        a.dst = j0.dst ? j0.dst + a_lo * j0.ld_dst : nullptr;
-        a.rows = a_hi - a_lo;
-        const int64_t b_lo = r0 > j0.rows ? r0 - j0.rows : 0, b_hi = r0 + n > j0.rows ? r0 + n - j0.rows : 0;
-        b.src = j1.src ? j1.src + b_lo * j1.ld_src : nullptr;
-        b.dst = j1.dst ? j1.dst + b_lo * j1.ld_dst : nullptr;
-        b.rows = b_hi - b_lo;
-        pack_rows_f16<<<dim3(gx, static_cast<unsigned>(n), 1), 128, 0, stream>>>(a, b);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    auto job = [](const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows, int64_t cols) {
+        PackJob j{static_cast<const uint16_t *>(src), ld_src, static_cast<uint16_t *>(dst), ld_dst,
+                  src ? rows : 0, cols, pack_lanes_per_row(cols), 0};
+        const int64_t rows_per_block = static_cast<int64_t>(kPackWarps) * (32 / j.lanes_per_row);
+        j.blocks = (j.rows + rows_per_block - 1) / rows_per_block;
+        return j;
+    };
+    const PackJob j0 = job(src0, ld_src0, dst0, ld_dst0, rows0, cols0);
+    const PackJob j1 = job(src1, ld_src1, dst1, ld_dst1, rows1, cols1);
+    const int64_t blocks = j0.blocks + j1.blocks;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 2147483647ll) return cudaErrorInvalidValue;
+    pack_rows_f16<<<static_cast<unsigned>(blocks), kPackWarps * 32, 0, stream>>>(j0, j1);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_fill_epilogue(const KernelParams &p, int num_sms, cudaStream_t stream)

@@ -221,14 +221,21 @@ def test_unaligned_c_and_padded_ldc():
 
 
 def test_torch_helper():
+    """The torch-facing helper (tct.gemm) gives the oracle's epilogue result."""
     rng = np.random.default_rng(75)
     M, N, K = 256, 384, 128
     A, B = inputs.pair_ex(rng, M, N, K, dtype="f16")
     dA, dB = _dev(A, "f16"), _dev(B, "f16")
-    bias = torch.randn(N, device="cuda")
-    C0 = torch.randn(M, N, device="cuda")
-    out = tct.gemm(dA, dB, C0.clone(), alpha=2.0, beta=0.5, bias=bias)
-    ref = 2.0 * (dA.double() @ dB.double()) + 0.5 * C0.double() + bias.double()
-    assert torch.allclose(out.double(), ref, atol=1e-2, rtol=1e-3)
+    bias = rng.standard_normal(N).astype(np.float32)
+    C0 = rng.standard_normal((M, N)).astype(np.float32)
+    out = tct.gemm(dA, dB, _dev(C0, "f32"), alpha=2.0, beta=0.5, bias=_dev(bias, "f32"))
+    torch.cuda.synchronize()
+    want = run_ref(A, B, "f16", False, False, "f32", 2.0, 0.5, C0, bias, "f32")
+    S = np.abs(oracle.gemm_ex_f32(A, B, dtype=oracle.F16))
+    assert close(out.cpu().numpy(), want, "f32", K, 2.0, S)
+    # A given as a transposed view, BF16 output: the stored layout is read in place
     out16 = tct.gemm(dA.t().contiguous().t(), dB, out_dtype=torch.bfloat16)
     assert out16.dtype == torch.bfloat16
+    got16 = out16.cpu().view(torch.int16).numpy().view(np.uint16)
+    want16 = run_ref(A, B, "f16", False, False, "bf16", 1.0, 0.0, None, None, "f32")
+    assert close(got16, want16, "bf16", K, 1.0, S)
