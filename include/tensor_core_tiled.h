@@ -86,10 +86,21 @@ TCT_API gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t
  *               both parts are added into it by TMA reduce-add; otherwise the second part goes
  *               through a stream-ordered workspace and the owner adds it.  Every tile has two
  *               contributions, so the sum does not depend on their order and results are
- *               reproducible.  0 = let the planner decide.
+ *               reproducible.
+ *               3 = stream-K (plain FP32 epilogue and a C that TMA writes, as above; else
+ *               GEMM_ERR_INVALID_ARG at launch): after whole waves of tiles, the k-blocks of
+ *               the remaining tiles are cut into contiguous ranges of balanced length, one per
+ *               unit, so that every unit finishes together even when there are fewer tiles
+ *               than units ("02_gpu_execution_model.py", part 5: a partial wave leaves SMs
+ *               idle).  A tile's k-loop may then be spread over several consecutive units;
+ *               its pieces reach C in a fixed order, the last piece stored first and each
+ *               earlier piece added by TMA reduce-add once the next one is in C, so results
+ *               are reproducible bit for bit.  No workspace is used.
+ *               0 = let the planner decide among whole tiles, 2 and 3.
  *   fault_inject: test hook for the device-side timeout path; 0 in normal use.  Bit 0: split
- *               tiles are never published (the owner neither zeroes nor flags its tile, or
- *               the helper never flags its part), so the waits for them run until timeout_ms,
+ *               tiles are never published (the owner neither zeroes nor flags its tile, the
+ *               helper never flags its part, or a stream-K piece that starts inside a tile
+ *               never flags it), so the waits for them run until timeout_ms,
  *               record GEMM_ERR_DEVICE_TIMEOUT (read by gemm_f16_f32_get_error) and return
  *               without storing those tiles.  Bit 1 (gemm_ex with beta != 0 on a C that TMA
  *               writes): the epilogue never loads C's blocks, so its waits for them run out
@@ -181,10 +192,15 @@ typedef struct gemm_plan {
     int32_t pack_a, pack_b;         /* 1 if the operand would be repacked first       */
     int32_t cta_group;              /* CTAs sharing one tile (1 or 2)                 */
     int32_t units;                  /* persistent work units (CTAs or CTA pairs)      */
-    int32_t stream_k_tiles;         /* tiles whose k-loop is split in two parts       */
+    int32_t stream_k_tiles;         /* tiles whose k-loop may be split across units   */
     double effective_waves;         /* tile-times per unit: whole waves + split share */
-    int32_t split_kb;               /* k-block where a split tile's second part starts */
-    int32_t split_parts_per_unit;   /* second parts a helper unit takes in turn (>= 1) */
+    int32_t split_kb;               /* form 1: k-block where a split tile's second part
+                                       starts; form 2: the shortest unit range (k-blocks) */
+    int32_t split_parts_per_unit;   /* form 1: second parts a helper unit takes in turn;
+                                       form 2: most pieces one tile is cut into */
+    int32_t split_form;             /* 0 whole tiles, 1 two-part split tail (stream_k 2),
+                                       2 stream-K ranges (stream_k 3)                    */
+    int32_t sk_units;               /* form 2: units sharing the stream-K k-blocks     */
 } gemm_plan;
 
 TCT_API gemm_status gemm_f16_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -204,7 +220,8 @@ TCT_API gemm_status gemm_tile_coord(int64_t t, int64_t num_m, int64_t num_n, int
  * [kb0, kb1) of linear tile `tile`.  mode 0: store the tile to C.  A tile of the last,
  * partial wave may be split into two k-parts: mode 1 is its owner (k-blocks [0, split_kb)),
  * mode 2 the helper computing the rest; `part` numbers the split tile (its flag, and its
- * workspace slot when the parts are combined through workspace).
+ * workspace slot when the parts are combined through workspace).  mode 3: a stream-K piece
+ * of a tile (split_form 2), `part` = the unit, whose flag it raises when kb0 > 0.
  */
 typedef struct gemm_work {
     int32_t tile, kb0, kb1;

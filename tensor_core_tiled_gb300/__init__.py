@@ -60,7 +60,8 @@ class GemmPlan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int32), ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32),
                 ("cta_group", ctypes.c_int32), ("units", ctypes.c_int32), ("stream_k_tiles", ctypes.c_int32),
                 ("effective_waves", ctypes.c_double), ("split_kb", ctypes.c_int32),
-                ("split_parts_per_unit", ctypes.c_int32)]
+                ("split_parts_per_unit", ctypes.c_int32), ("split_form", ctypes.c_int32),
+                ("sk_units", ctypes.c_int32)]
 
 
 class GemmEpilogue(ctypes.Structure):
@@ -73,7 +74,7 @@ class GemmWork(ctypes.Structure):
                 ("part", ctypes.c_int32)]
 
 
-WORK_STORE, WORK_FIXUP, WORK_PARTIAL = 0, 1, 2
+WORK_STORE, WORK_FIXUP, WORK_PARTIAL, WORK_CHAIN = 0, 1, 2, 3
 
 _lib = None
 

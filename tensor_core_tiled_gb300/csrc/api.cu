@@ -43,8 +43,16 @@ constexpr double kL2BytesPerSec = 20e12;
 // store are serial after the halves finish, about two tile epilogues plus a flag handoff.
 constexpr double kFixupSec = 12e-6;       // split tile combined through workspace (measured)
 constexpr double kFixupReduceSec = 3e-6;  // split tile combined by TMA reduce-add into C
-// A tile is only split in two when each half has at least this many k-blocks.
+// A tile is only split in two when each half has at least this many k-blocks; a stream-K
+// range is at least this long too.
 constexpr int64_t kMinSplitIters = 4;
+// Exposed cost of one link of a stream-K chain: a piece that ends inside its tile waits for
+// the next piece to be in C, then adds its own rows (128 x tile_n FP32 per CTA) by TMA
+// reduce-add.  Per link: a fixed hand-off plus the reduce at about 64 bytes per SM clock.
+constexpr double kLinkFixedSec = 0.5e-6;
+constexpr double kLinkBytesPerSecPerSm = 64.0 * 1.9e9;
+// Pieces one tile may be cut into (bounds the chain's length); the planner tries each cap.
+constexpr int64_t kStreamKPieceCaps[] = {2, 3, 4, 6};
 
 constexpr Candidate kCandidates[] = {
     {2, 256, 6, 1.00},
@@ -155,7 +163,7 @@ gemm_status check_options(const gemm_options *opt)
 {
     if (!opt) return GEMM_OK;
     if (opt->fault_inject < 0 || opt->fault_inject > 3) return GEMM_ERR_INVALID_ARG;
-    if (opt->stream_k < 0 || opt->stream_k > 2) return GEMM_ERR_INVALID_ARG;
+    if (opt->stream_k < 0 || opt->stream_k > 3) return GEMM_ERR_INVALID_ARG;
     if (opt->group_m < 0 || opt->group_m > 256) return GEMM_ERR_INVALID_ARG;
     if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return GEMM_ERR_INVALID_ARG;
     if (opt->cta_group < 0 || opt->cta_group > 2) return GEMM_ERR_INVALID_ARG;
@@ -209,8 +217,11 @@ double wave_util(int64_t M, int64_t N, int64_t tm, int64_t tn, int64_t slots, in
 struct Split {
     int64_t units, tiles, waves, dp_tiles, split_tiles;
     int64_t split_kb, parts;  // owner's k-blocks of a split tile; second parts per helper
+                              // (stream-K: shortest range; most pieces of one tile)
     double time, eff_waves;
     double compute;  // the compute part of `time` (tile time x effective waves)
+    int form;        // 0 whole tiles, 1 two-part split tail, 2 stream-K
+    int64_t sk_units;
 };
 
 // Work split and modelled time of one variant.  Whole waves of tiles go data-parallel; the
@@ -272,7 +283,55 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
             sp.time = t_sp;
             sp.eff_waves = ew;
             sp.compute = ew * tile_sec;
+            sp.form = 1;
         }
+    }
+    // Stream-K ("02_gpu_execution_model.py" part 5: rather than leave a partial wave's SMs
+    // idle, cut the remaining work finer): after dpw whole waves, the k-blocks of the other
+    // tiles are shared out in contiguous, balanced ranges over sku units.  The tiles whose
+    // k-blocks are shared are the partial wave, or the partial wave and one whole wave
+    // before it (longer ranges, fewer pieces per tile).  Each unit's time is dpw tiles plus
+    // its range; a tile cut into c pieces adds c - 1 links to the critical path.  Only with
+    // the reduce-add combination (plain FP32 epilogue, C TMA-writable).
+    if (reduce_split && (want_sk == 0 || want_sk == 3)) {
+        bool found = false;
+        Split best{};
+        const double link_sec = kLinkFixedSec + 4.0 * kTileM * tile_n / kLinkBytesPerSecPerSm;
+        for (int64_t d = 0; d <= 1; ++d) {
+            const int64_t dpw = full - d;
+            if (dpw < 0) continue;
+            const int64_t skt = tiles - dpw * units;
+            if (skt <= 0) continue;
+            const int64_t iters = skt * kb;
+            for (const int64_t cap : kStreamKPieceCaps) {
+                const int64_t qmin = std::max<int64_t>(want_sk == 3 ? 1 : kMinSplitIters, tct::ceil_div(kb, cap));
+                const int64_t sku = std::min<int64_t>(units, iters / qmin);
+                if (sku < 2 || (want_sk != 3 && sku <= skt)) continue;  // no finer than whole tiles
+                const int64_t q = iters / sku, qmax = tct::ceil_div(iters, sku);
+                const int64_t pieces = std::min<int64_t>(tct::ceil_div(kb - 1, q) + 1, sku);
+                const double ew = dpw + static_cast<double>(qmax) / kb;
+                const double busy_sk = static_cast<double>(sku) / units;
+                const double t_mem = (dpw > 0 ? bytes * dpw * units / tiles / kHbmBytesPerSec : 0.0) +
+                                     bytes * skt / tiles / (kHbmBytesPerSec * busy_sk);
+                const double t = std::max(ew * tile_sec, t_mem) + (pieces - 1) * link_sec;
+                if (!found || t < best.time) {
+                    found = true;
+                    best = sp;
+                    best.units = units;
+                    best.waves = tct::ceil_div(tiles, units);
+                    best.dp_tiles = dpw * units;
+                    best.split_tiles = skt;
+                    best.split_kb = q;
+                    best.parts = pieces;
+                    best.time = t;
+                    best.eff_waves = ew;
+                    best.compute = ew * tile_sec;
+                    best.form = 2;
+                    best.sk_units = sku;
+                }
+            }
+        }
+        if (found && (want_sk == 3 || best.time < sp.time)) sp = best;
     }
     return sp;
 }
@@ -303,6 +362,7 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
         const int st = want_st ? want_st : c.stages;
         const Split sp = model_split(M, N, K, c.cta_group, c.tile_n, st, c.rate, units, want_sk,
                                      reduce_split ? kFixupReduceSec : kFixupSec, reduce_split);
+        if (want_sk == 3 && sp.form != 2) continue;  // stream-K asked for: only plans that use it
         // Within 1% (e.g. every candidate bound by the same HBM time) the one with less compute
         // time wins: it has the most slack (measured: 1-CTA 128x128 tiles stream the skinny
         // 128 x 16384 x 16384 shape 5% faster than CTA-pair 256x256 tiles, half of whose rows
@@ -341,6 +401,9 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
     pl->effective_waves = best_sp.eff_waves;
     pl->split_kb = static_cast<int32_t>(best_sp.split_kb);
     pl->split_parts_per_unit = static_cast<int32_t>(best_sp.parts);
+    pl->split_form = best_sp.form;
+    pl->sk_units = static_cast<int32_t>(best_sp.sk_units);
+    if (want_sk == 3 && best_sp.form != 2) return GEMM_ERR_INVALID_ARG;  // stream-K asked for, not possible
     return GEMM_OK;
 }
 
@@ -381,7 +444,8 @@ tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t 
     p.workspace = nullptr;
     p.flags = nullptr;
     p.fault_inject = 0;
-    p.split_mode = 0;
+    p.split_mode = pl.split_form == 2 ? 2 : 0;
+    p.sk_units = pl.split_form == 2 ? pl.sk_units : 0;
     p.c_tma = 0;
     return p;
 }
@@ -390,13 +454,14 @@ tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t 
 // tile and CTA rank.
 int64_t split_parts_bytes(const gemm_plan &pl)
 {
-    if (pl.stream_k_tiles <= 0) return 0;
+    if (pl.stream_k_tiles <= 0 || pl.split_form == 2) return 0;
     return static_cast<int64_t>(pl.stream_k_tiles) * pl.tile_m * pl.tile_n * 4;
 }
 
 int64_t split_flags_bytes(const gemm_plan &pl)
 {
     if (pl.stream_k_tiles <= 0) return 0;
+    if (pl.split_form == 2) return round_up(static_cast<int64_t>(pl.sk_units) * pl.cta_group * 4, 256);
     return round_up(static_cast<int64_t>(pl.stream_k_tiles) * pl.cta_group * 4, 256);
 }
 
@@ -574,7 +639,9 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
         if (pl.stream_k_tiles > 0 && st == GEMM_OK) {
             uint8_t *w = static_cast<uint8_t *>(ws) + a_bytes + b_bytes;
             p.flags = reinterpret_cast<unsigned int *>(w + w_bytes);
-            if (reduce_ok) {
+            if (pl.split_form == 2) {
+                // stream-K pieces: split_mode 2 from the plan, flags only
+            } else if (reduce_ok) {
                 p.split_mode = 1;
             } else {
                 p.workspace = reinterpret_cast<float *>(w);

@@ -52,12 +52,25 @@ struct KernelParams {
     // 1 when the tensor map over C is valid (C's base and row pitch 16-byte aligned, N a
     // whole number of 16-byte units): whole tiles are then written by TMA stores.
     int32_t c_tma;
+    // split_mode 2 (stream-K; plain FP32 epilogue, C TMA-writable): after dp_tiles whole
+    // tiles, the k-blocks of the last split_tiles tiles -- split_tiles * num_kb iterations in
+    // tile order -- are cut into sk_units contiguous ranges of balanced length, one per unit
+    // (sk_units <= units, every range non-empty).  A unit walks its range in order, so only
+    // its first piece can start inside a tile and only its last can end inside one.  The
+    // pieces of one tile lie on consecutive units and are combined in C in a fixed order, the
+    // last piece first: a piece that reaches the tile's end is stored; a piece that ends
+    // inside the tile waits until the next unit's piece is in C (flag[(u + 1) * cta_group +
+    // rank]) and adds itself by TMA reduce-add; a piece that starts inside the tile raises
+    // flag[u * cta_group + rank] once its rows are in C.  C = ((p_last + ...) + p_1) + p_0,
+    // the same bits on every run.
+    int32_t sk_units;
 };
 
 enum WorkMode : int32_t {
     WORK_STORE = 0,    // store the accumulator to C
     WORK_FIXUP = 1,    // add the part in workspace slot `part`, then store to C
     WORK_PARTIAL = 2,  // store the accumulator to workspace slot `part`, raise its flag
+    WORK_CHAIN = 3,    // stream-K piece of a tile (split_mode 2); `part` is the unit
 };
 
 // One piece of work of a unit: k-blocks [kb0, kb1) of linear tile `tile`.
@@ -82,6 +95,25 @@ inline bool work_item(const KernelParams &p, int32_t u, int32_t idx, WorkItem &i
         it.kb0 = 0;
         it.kb1 = p.num_kb;
         it.mode = WORK_STORE;
+        return true;
+    }
+    if (p.split_mode == 2) {
+        // Stream-K: the idx - waves-th tile piece of this unit's range [a, b) of iterations.
+        if (u >= p.sk_units || p.split_tiles <= 0) return false;
+        const int64_t iters = static_cast<int64_t>(p.split_tiles) * p.num_kb;
+        const int64_t a = static_cast<int64_t>(u) * iters / p.sk_units;
+        const int64_t b = static_cast<int64_t>(u + 1) * iters / p.sk_units;
+        const int64_t t = a / p.num_kb + (idx - waves);
+        const int64_t t0 = t * p.num_kb;
+        const int64_t lo = a > t0 ? a : t0;
+        const int64_t hi = b < t0 + p.num_kb ? b : t0 + p.num_kb;
+        if (lo >= hi) return false;
+        it.tile = p.dp_tiles + static_cast<int32_t>(t);
+        it.kb0 = static_cast<int32_t>(lo - t0);
+        it.kb1 = static_cast<int32_t>(hi - t0);
+        const bool whole = it.kb0 == 0 && it.kb1 == p.num_kb;
+        it.mode = whole ? WORK_STORE : WORK_CHAIN;
+        it.part = whole ? -1 : u;
         return true;
     }
     // Split tail tile j = dp_tiles + j' (j' < split_tiles): unit j' owns k-blocks

@@ -825,6 +825,35 @@ __global__ void __launch_bounds__(192, 1)
                                                                                stage, lane, cb, cphase, limit, abort_flag,
                                                                                skip_c, release);
             };
+            if (w.mode == WORK_CHAIN) {
+                // Stream-K piece: the tile's pieces reach C last-first.  A piece that ends
+                // inside the tile waits for the next unit's piece, then adds itself; the piece
+                // that reaches the tile's end is the first and is stored.
+                const bool add = w.kb1 < p.num_kb;
+                if (add) {
+                    ok = wait_flag(p.flags + (unit + 1) * CG + rank, limit, abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    fence_proxy_async_all();  // the flag seen before the reduce reads C
+                }
+                ok = add ? bulk(std::true_type{}, std::false_type{}) : bulk(std::false_type{}, std::false_type{});
+                if (!ok) break;
+                if (w.kb0 > 0) {
+                    // A unit's only piece that starts inside a tile (its first): publish it to
+                    // the previous unit once all four warps' rows are in C.
+                    if (lane == 0) {
+                        bulk_wait_all();
+                        fence_proxy_async_all();
+                    }
+                    __syncwarp();
+                    __threadfence();
+                    if (lane == 0) mbar_arrive(part_bar);
+                    if (warp == 2 && lane == 0 && wait_or_abort<false>(part_bar, 0u, limit, abort_flag, SITE_EPI_PARTS) &&
+                        !(p.fault_inject & 1))
+                        flag_release_gpu(p.flags + unit * CG + rank, 1u);
+                }
+                continue;
+            }
             if (p.split_mode == 1 && w.mode != WORK_STORE) {
                 ok = wait_flag(p.flags + w.part * CG + rank, limit, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
@@ -1026,7 +1055,10 @@ static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, 
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.numAttrs = 2;
-    if (p.split_tiles > 0 && !Cfg<CG, BN, STAGES>::SPLIT_OK) return cudaErrorInvalidValue;
+    // split tiles combined through workspace or reduce-add need room for a part in the stage
+    // buffers; stream-K pieces (split_mode 2) need none
+    if (p.split_tiles > 0 && p.split_mode != 2 && !Cfg<CG, BN, STAGES>::SPLIT_OK) return cudaErrorInvalidValue;
+    if (p.split_mode == 2 && !p.c_tma) return cudaErrorInvalidValue;
     e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tp, tc, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -77,7 +77,7 @@ def test_invalid_arguments_rejected_before_any_device_work(tct_lib):
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, stages=9) == tct.GEMM_ERR_INVALID_ARG
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, group_m=-1) == tct.GEMM_ERR_INVALID_ARG
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, cta_group=3) == tct.GEMM_ERR_INVALID_ARG
-    assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, stream_k=3) == tct.GEMM_ERR_INVALID_ARG
+    assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, stream_k=4) == tct.GEMM_ERR_INVALID_ARG
     assert tct.gemm_f16_f32_ex(p, p, p, 4, 4, 4, 4, 4, 4, 0, fault_inject=4) == tct.GEMM_ERR_INVALID_ARG
     # generalised entry: bad type or op, and leading dimensions checked against the storage
     assert tct.gemm_f32acc(2, 0, 0, p, p, p, 4, 4, 4, 4, 4, 4, 0) == tct.GEMM_ERR_INVALID_ARG
@@ -254,3 +254,91 @@ def test_work_items_cover_every_k_block_once(tct_lib, shape, opts):
             assert wkb0 == p["split_kb"]
             per_helper[wu] = per_helper.get(wu, 0) + (wkb1 - wkb0)
         assert max(per_helper.values()) <= p["split_parts_per_unit"] * (kb - p["split_kb"]) <= p["split_kb"]
+
+
+STREAM_K_PLANS = [
+    ((1792, 1792, 1792), {"stream_k": 3}), ((2048, 2048, 2048), {"stream_k": 3}),
+    ((1793, 1793, 1793), {"stream_k": 3}), ((3072, 3072, 3072), {"stream_k": 3}),
+    ((4096, 4096, 4096), {"stream_k": 3}), ((8192, 8192, 8192), {"stream_k": 3}),
+    ((128, 16384, 16384), {"stream_k": 3}), ((128, 16384, 16384), {"stream_k": 3, "cta_group": 2}),
+    ((256, 256, 4096), {"stream_k": 3}), ((300, 200, 150), {"stream_k": 3}),
+    ((1, 1000, 64 * 40), {"stream_k": 3, "cta_group": 1, "tile_n": 128}),
+    ((6144, 6144, 6144), {"stream_k": 3}), ((1000, 1100, 700), {"stream_k": 3, "max_ctas": 30}),
+]
+
+
+@pytest.mark.parametrize("shape,opts", STREAM_K_PLANS)
+def test_stream_k_work_items(tct_lib, shape, opts):
+    """Stream-K plans: each (tile, k-block) pair belongs to exactly one item of one unit; the
+    whole waves come first; every unit's stream-K range is one contiguous, non-empty run of
+    iterations in tile order, the ranges differ in length by at most one and together cover
+    the stream-K tiles; only a unit's first piece starts inside a tile and only its last ends
+    inside one; a tile's pieces lie on consecutive units, in k order, and number at most the
+    plan's split_parts_per_unit."""
+    M, N, K = shape
+    sms = 152
+    p = tct.gemm_f16_f32_plan(M, N, K, num_sms=sms, **opts)
+    assert p["split_form"] == 2 and p["stream_k_tiles"] > 0 and 2 <= p["sk_units"] <= p["units"]
+    kb = -(-K // 64)
+    dp_tiles = p["tiles"] - p["stream_k_tiles"]
+    assert dp_tiles % p["units"] == 0
+    seen = {}
+    pieces = {}
+    lengths = []
+    for u in range(p["units"]):
+        idx = 0
+        sk_items = []
+        while True:
+            it = tct.gemm_f16_f32_work_item(M, N, K, sms, u, idx, **opts)
+            if it is None:
+                break
+            tile, kb0, kb1, mode = it["tile"], it["kb0"], it["kb1"], it["mode"]
+            assert 0 <= kb0 < kb1 <= kb
+            if idx < dp_tiles // p["units"]:
+                assert mode == tct.WORK_STORE and tile == u + idx * p["units"] and (kb0, kb1) == (0, kb)
+            else:
+                assert tile >= dp_tiles
+                sk_items.append((tile, kb0, kb1, mode, it["part"]))
+            for k in range(kb0, kb1):
+                assert (tile, k) not in seen
+                seen[(tile, k)] = u
+            idx += 1
+        if u >= p["sk_units"]:
+            assert not sk_items
+            continue
+        assert sk_items, f"unit {u} has an empty stream-K range"
+        flat = [(t - dp_tiles) * kb + k for (t, k0, k1, _, _) in sk_items for k in range(k0, k1)]
+        assert flat == list(range(flat[0], flat[0] + len(flat)))  # contiguous, in order
+        lengths.append((flat[0], len(flat)))
+        for j, (t, k0, k1, mode, part) in enumerate(sk_items):
+            whole = (k0, k1) == (0, kb)
+            assert mode == (tct.WORK_STORE if whole else tct.WORK_CHAIN)
+            assert part == (-1 if whole else u)
+            if k0 > 0:
+                assert j == 0
+            if k1 < kb:
+                assert j == len(sk_items) - 1
+            if not whole:
+                pieces.setdefault(t, []).append((u, k0, k1))
+    assert len(seen) == p["tiles"] * kb
+    starts = [a for a, _ in lengths]
+    assert starts == sorted(starts) and starts[0] == 0
+    assert max(n for _, n in lengths) - min(n for _, n in lengths) <= 1
+    assert sum(n for _, n in lengths) == p["stream_k_tiles"] * kb
+    assert min(n for _, n in lengths) == p["split_kb"]
+    for t, ps in pieces.items():
+        units = [u for u, _, _ in ps]
+        assert units == list(range(units[0], units[0] + len(units)))
+        assert ps[0][1] == 0 and ps[-1][2] == kb
+        assert all(ps[i][2] == ps[i + 1][1] for i in range(len(ps) - 1))
+        assert len(ps) <= p["split_parts_per_unit"]
+
+
+def test_stream_k_needs_the_reduce_add_path(tct_lib):
+    """Stream-K combines pieces by TMA reduce-add into C: it is only planned for the plain
+    FP32 epilogue on a C whose rows are whole 16-byte units; asked for otherwise, the plan
+    is rejected."""
+    sms = 152
+    assert tct.gemm_f16_f32_plan(2048, 2048, 2048, num_sms=sms, stream_k=3)["split_form"] == 2
+    with pytest.raises(tct.GemmError):
+        tct.gemm_f16_f32_plan(2048, 2046, 2048, num_sms=sms, stream_k=3)

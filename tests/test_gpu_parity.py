@@ -298,6 +298,67 @@ def test_stream_k_split(shape, opts):
     assert bit_exact(gpu_gemm(Ai, Bi, **opts), oracle.gemm_f32(Ai, Bi))
 
 
+STREAM_K_CHAIN_CASES = [
+    ((1792, 1792, 1792), {}),
+    ((2048, 2048, 2048), {}),
+    ((1000, 1100, 700), {}),
+    ((300, 200, 150), {}),
+    ((256, 256, 4096), {}),                      # one pair tile spread over many units
+    ((128, 4096, 8192), {"cta_group": 1, "tile_n": 128}),
+    ((128, 4096, 8192), {"cta_group": 2}),       # the pair's second 128 rows are empty
+    ((3000, 2052, 1500), {"cta_group": 1, "tile_n": 256}),
+    ((4096, 4096, 1024), {}),
+    ((777, 1500, 515), {"max_ctas": 40}),
+    ((129, 68, 64 * 33), {"cta_group": 1, "tile_n": 128}),
+]
+
+
+@pytest.mark.parametrize("shape,opts", STREAM_K_CHAIN_CASES)
+def test_stream_k_chain(shape, opts):
+    """Stream-K plans (balanced k-ranges per unit, a tile's pieces chained into C last-first
+    by TMA store and reduce-adds): the oracle's result over the whole matrix, bit for bit on
+    integer inputs, and the same bits on every run (the chain fixes the order of the sums)."""
+    M, N, K = shape
+    opts = dict(opts, stream_k=3)
+    plan = tct.gemm_f16_f32_plan(M, N, K, **opts)
+    assert plan["split_form"] == 2
+    rng = np.random.default_rng(47)
+    A, B = inputs.normal_pair(rng, M, N, K)
+    dA, dB = dev16(A), dev16(B)
+    C = tct.matmul(dA, dB, **opts)
+    torch.cuda.synchronize()
+    first = C.clone()
+    for _ in range(3):
+        tct.matmul(dA, dB, C, **opts)
+        torch.cuda.synchronize()
+        assert torch.equal(C.view(torch.int32), first.view(torch.int32))
+    assert within_tol(C.cpu().numpy(), oracle.gemm_f32(A, B), K)
+    Ai, Bi = inputs.integer_pair(rng, M, N, K)
+    assert bit_exact(gpu_gemm(Ai, Bi, **opts), oracle.gemm_f32(Ai, Bi))
+
+
+def test_stream_k_chain_padding_bits_untouched():
+    """The chain's TMA stores and reduce-adds write only the M x N block: -0.0 in the gap
+    columns (ldc > N) and around C keeps its bits."""
+    M, N, K, ldc = 1000, 1100, 700, 1108
+    rng = np.random.default_rng(53)
+    A, B = inputs.normal_pair(rng, M, N, K)
+    guard = 1024
+    c_buf = torch.full((guard + M * ldc + guard,), -0.0, dtype=torch.float32, device="cuda")
+    c_base = c_buf.data_ptr() + guard * 4
+    dA, dB = dev16(A), dev16(B)
+    st = tct.gemm_f16_f32_ex(dA.data_ptr(), dB.data_ptr(), c_base, M, N, K, K, N, ldc,
+                             torch.cuda.current_stream().cuda_stream, stream_k=3)
+    assert st == tct.GEMM_OK
+    torch.cuda.synchronize()
+    bits = c_buf.view(torch.int32).cpu().numpy()
+    neg0 = np.int32(-2 ** 31)
+    assert np.all(bits[:guard] == neg0) and np.all(bits[guard + M * ldc:] == neg0)
+    body = bits[guard:guard + M * ldc].reshape(M, ldc)
+    assert np.all(body[:, N:] == neg0)
+    assert within_tol(body[:, :N].view(np.float32), oracle.gemm_f32(A, B), K)
+
+
 def test_stream_k_and_whole_tiles_agree_on_integers():
     rng = np.random.default_rng(43)
     A, B = inputs.integer_pair(rng, 2048, 2304, 3000)

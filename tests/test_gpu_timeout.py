@@ -97,3 +97,48 @@ def test_missing_c_load_times_out_and_context_survives(c_dtype):
     ulp = 0.0 if c_dtype == torch.float32 else 2.0 ** -7
     tol = 1e-3 * np.sqrt(K) * np.maximum(1.0, np.abs(want)) + 2 * ulp * np.abs(want)
     assert np.all(np.abs(got - want) <= tol)
+
+
+def test_unpublished_stream_k_piece_times_out_and_context_survives():
+    """Stream-K with fault_inject bit 0: a piece that starts inside a tile never raises its
+    flag, so the unit before it, whose piece of that tile waits to add into C, runs out of
+    time.  The status is read on the host, the tiles computed whole are correct, and the next
+    call on the same context is correct everywhere."""
+    M, N, K = 4096, 4096, 1024
+    opts = dict(stream_k=3)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = tct.gemm_f16_f32_plan(M, N, K, num_sms=sms, **opts)
+    assert plan["split_form"] == 2 and 0 < plan["stream_k_tiles"] < plan["tiles"]
+    rng = np.random.default_rng(57)
+    A, B = inputs.normal_pair(rng, M, N, K)
+    dA, dB = _dev16(A), _dev16(B)
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    C = torch.full((M, N), float("nan"), device="cuda")
+    t0 = time.time()
+    tct.matmul(dA, dB, C, timeout_ms=50, fault_inject=1, **opts)
+    status = tct.gemm_f16_f32_get_error()
+    assert status == tct.GEMM_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 5.0
+    host = C.cpu().numpy()
+    R = oracle.gemm_f32(A, B)
+    tm, tn = plan["tile_m"], plan["tile_n"]
+    num_m, num_n = -(-M // tm), -(-N // tn)
+    whole = []
+    for u in range(plan["units"]):
+        idx = 0
+        while True:
+            it = tct.gemm_f16_f32_work_item(M, N, K, sms, u, idx, **opts)
+            if it is None:
+                break
+            if it["mode"] == tct.WORK_STORE:
+                whole.append(it["tile"])
+            idx += 1
+    assert whole
+    for t in whole:
+        r, c = tct.gemm_tile_coord(t, num_m, num_n, plan["group_m"])
+        blk = (slice(r * tm, min(M, (r + 1) * tm)), slice(c * tn, min(N, (c + 1) * tn)))
+        assert within_tol(host[blk], R[blk], K)
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    C2 = tct.matmul(dA, dB, **opts)
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    assert within_tol(C2.cpu().numpy(), R, K)
