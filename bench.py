@@ -535,6 +535,10 @@ def run_ours(args):
             sampler2.stop()
         assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
 
+    # ---- the tensor core's own rate per SM per clock, measured on this device (one CTA per
+    # SM issuing back-to-back 128x256x16 MMAs, timed by the SM clock counter)
+    probe_med, probe_lo, probe_hi = tct.gemm_tensor_rate_probe(1 << 16, sp)
+
     peak_burst, peak_sustained, peak_src = peaks()
     mean_launch = statistics.mean(launch_ms)
     achieved = flops / (mean_launch * 1e-3) / 1e12
@@ -574,6 +578,9 @@ def run_ours(args):
                          "per_clock_peak_at_max_clock": clock_peak_max,
                          "frac_of_per_clock_peak_at_max_clock": achieved / clock_peak_max,
                          "frac_per_clock": s8.get("frac_per_clock"),
+                         "tensor_flop_per_clk_sm_measured": {"median": probe_med, "min": probe_lo, "max": probe_hi,
+                                                             "how": "gemm_tensor_rate_probe: one CTA per SM, 65536 "
+                                                                    "back-to-back 128x256x16 kind::f16 MMAs, clock64"},
                          "frac_per_clock_source": (f"8192^3 back to back for {args.sustained_leg:g} s: "
                                                    f"TFLOP/s / ({sms} SMs x {TENSOR_FLOP_PER_CLK_SM} FLOP/clk x "
                                                    f"median SM clock sampled inside the loop)") if s8 else None},

@@ -316,6 +316,20 @@ TCT_API gemm_status softmax_rows_f32_host(const float *X, float *Y, int64_t M, i
                                           void *stream);
 
 /*
+ * Dense FP16 tensor rate of this device per SM and clock, measured (the per-clock factor of
+ * the GEMM's roofline, SMs x FLOP/clk/SM x SM clock, "04_tensor_cores.py" demo 3: the
+ * arithmetic a tensor core delivers per SM per clock).  One CTA per SM issues n_mma
+ * back-to-back tcgen05.mma.kind::f16 of 128 x 256 x 16 (FP32 accumulation in tensor memory,
+ * operands in shared memory) from one thread and times them with the SM clock counter;
+ * FLOP = n_mma x 2 x 128 x 256 x 16.  Writes the median over SMs to *flop_per_clk_sm and,
+ * when not NULL, the smallest and largest to *min_flop_per_clk_sm / *max_flop_per_clk_sm.
+ * Runs on `stream` and synchronises it.  n_mma in 1 .. 2^22, else GEMM_ERR_INVALID_ARG;
+ * GEMM_ERR_DEVICE_TIMEOUT if the MMAs did not complete within 2 s (bounded wait).
+ */
+TCT_API gemm_status gemm_tensor_rate_probe(int32_t n_mma, void *stream, double *flop_per_clk_sm,
+                                           double *min_flop_per_clk_sm, double *max_flop_per_clk_sm);
+
+/*
  * Reads and clears the device error word of the current device: GEMM_OK, or
  * GEMM_ERR_DEVICE_TIMEOUT if a kernel launched since the last read gave up on a pipeline
  * wait (its output is then incomplete).  Synchronises the current device first.

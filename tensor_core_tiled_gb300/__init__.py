@@ -36,6 +36,7 @@ EXPORTED = (
     "gemm_tile_coord",
     "gemm_wave_model",
     "gemm_f16_f32_get_error",
+    "gemm_tensor_rate_probe",
     "gemm_status_string",
     "gemm_version",
 )
@@ -119,6 +120,9 @@ def load():
                                     ctypes.POINTER(ctypes.c_double)]
     lib.gemm_f16_f32_get_error.restype = ctypes.c_int
     lib.gemm_f16_f32_get_error.argtypes = []
+    lib.gemm_tensor_rate_probe.restype = ctypes.c_int
+    lib.gemm_tensor_rate_probe.argtypes = [i32, vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_double)]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_status_string.argtypes = [ctypes.c_int]
     lib.gemm_version.restype = ctypes.c_char_p
@@ -223,6 +227,15 @@ def gemm_wave_model(M, N, tile_m, tile_n, slots):
 
 def gemm_f16_f32_get_error():
     return load().gemm_f16_f32_get_error()
+
+
+def gemm_tensor_rate_probe(n_mma=1 << 16, stream=0):
+    """Measured dense FP16 tensor FLOP per SM per clock: (median, min, max) over the SMs."""
+    med, lo, hi = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    st = load().gemm_tensor_rate_probe(n_mma, stream or None, ctypes.byref(med), ctypes.byref(lo), ctypes.byref(hi))
+    if st:
+        raise GemmError(st, "gemm_tensor_rate_probe")
+    return med.value, lo.value, hi.value
 
 
 def _current_stream_ptr(device):

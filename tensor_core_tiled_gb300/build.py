@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libtensor_core_tiled.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["gemm_sm103a.cu", "api.cu", "softmax_sm103a.cu"]
+SOURCES = ["gemm_sm103a.cu", "api.cu", "softmax_sm103a.cu", "probe_sm103a.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -47,10 +47,12 @@ constexpr double kFixupReduceSec = 3e-6;  // split tile combined by TMA reduce-a
 // range is at least this long too.
 constexpr int64_t kMinSplitIters = 4;
 // Exposed cost of one link of a stream-K chain: a piece that ends inside its tile waits for
-// the next piece to be in C, then adds its own rows (128 x tile_n FP32 per CTA) by TMA
-// reduce-add.  Per link: a fixed hand-off plus the reduce at about 64 bytes per SM clock.
-constexpr double kLinkFixedSec = 0.5e-6;
-constexpr double kLinkBytesPerSecPerSm = 64.0 * 1.9e9;
+// the next piece to be in C (its TMA writes complete, then its flag), then adds its own rows
+// (128 x tile_n FP32 per CTA) by TMA reduce-add.  Measured on GB300 against whole tiles on
+// the same shapes: about 3.5 us per link with 128-column tiles and 5.5 us with 256-column
+// tiles (a fixed 1.5 us plus the rows at about 33 GB/s per SM).
+constexpr double kLinkFixedSec = 1.5e-6;
+constexpr double kLinkBytesPerSecPerSm = 33e9;
 // Pieces one tile may be cut into (bounds the chain's length); the planner tries each cap.
 constexpr int64_t kStreamKPieceCaps[] = {2, 3, 4, 6};
 
@@ -214,6 +216,12 @@ double wave_util(int64_t M, int64_t N, int64_t tm, int64_t tn, int64_t slots, in
     return static_cast<double>(tiles) / static_cast<double>(waves * slots);
 }
 
+// Share of the HBM bandwidth that a fraction `busy` of the units streaming operands reaches.
+// Measured on GB300 with the skinny 128 x 16384 x 16384 product: 128 of 152 SMs streaming B
+// already draw as much as all 152 (a stream-K plan with every SM busy was not faster), so
+// the bandwidth is taken as saturated from 80% of the units on.
+double hbm_share(double busy) { return std::min(1.0, busy / 0.8); }
+
 struct Split {
     int64_t units, tiles, waves, dp_tiles, split_tiles;
     int64_t split_kb, parts;  // owner's k-blocks of a split tile; second parts per helper
@@ -247,7 +255,7 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
     const int64_t dp_units = std::min<int64_t>(units, tiles);
     const int64_t waves = tct::ceil_div(tiles, dp_units);
     const double busy = static_cast<double>(dp_units) / units;
-    const double t_dp = std::max(waves * tile_sec, bytes / (kHbmBytesPerSec * busy));
+    const double t_dp = std::max(waves * tile_sec, bytes / (kHbmBytesPerSec * hbm_share(busy)));
     sp.units = dp_units;
     sp.tiles = tiles;
     sp.waves = waves;
@@ -268,7 +276,7 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
         const double ew = full + t_tail;
         const double busy_split = static_cast<double>(rest + std::min(helpers, rest)) / units;
         const double t_tail_mem = (full > 0 ? bytes * full / tiles / kHbmBytesPerSec : 0.0) +
-                                  bytes * rest / tiles / (kHbmBytesPerSec * busy_split);
+                                  bytes * rest / tiles / (kHbmBytesPerSec * hbm_share(busy_split));
         // a helper combines each of its p parts (measured: 9 short parts per helper at 3072^3
         // cost more than the whole extra wave they replace)
         const double t_sp = std::max(ew * tile_sec, t_tail_mem) + fixup_sec * p +
@@ -312,7 +320,7 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
                 const double ew = dpw + static_cast<double>(qmax) / kb;
                 const double busy_sk = static_cast<double>(sku) / units;
                 const double t_mem = (dpw > 0 ? bytes * dpw * units / tiles / kHbmBytesPerSec : 0.0) +
-                                     bytes * skt / tiles / (kHbmBytesPerSec * busy_sk);
+                                     bytes * skt / tiles / (kHbmBytesPerSec * hbm_share(busy_sk));
                 const double t = std::max(ew * tile_sec, t_mem) + (pieces - 1) * link_sec;
                 if (!found || t < best.time) {
                     found = true;

@@ -278,6 +278,20 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst 
                 make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
                             __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
         __syncwarp();
+        if (!d.vec && !d.epi && !d.part && d.out_type == 2) {
+            // FP32 C whose rows are not 16-byte aligned (no vector stores): one row per
+            // store instruction, lane = column, so each instruction writes 128 contiguous bytes.
+            const int64_t gc = col_base + ch * 32 + lane;
+            const int swz = lane & 3;
+#pragma unroll 8
+            for (int rr = 0; rr < 32; ++rr) {
+                const int64_t grow = row_base + rr;
+                const float v = stage[rr * 32 + ((((lane >> 2) ^ (rr & 7)) << 2) | swz)];
+                if (grow < d.rows && gc < d.cols) __stcs(static_cast<float *>(d.base) + grow * d.ld + gc, v);
+            }
+            __syncwarp();
+            continue;
+        }
         // Coalesced, predicated stores: 8 lanes cover one 128-byte row segment.
         const int64_t gcol = col_base + ch * 32 + jj * 4;
         // Epilogue inputs, loaded before any store of this block: the bias of this lane's 4

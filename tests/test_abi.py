@@ -258,7 +258,7 @@ def test_work_items_cover_every_k_block_once(tct_lib, shape, opts):
 
 STREAM_K_PLANS = [
     ((1792, 1792, 1792), {"stream_k": 3}), ((2048, 2048, 2048), {"stream_k": 3}),
-    ((1793, 1793, 1793), {"stream_k": 3}), ((3072, 3072, 3072), {"stream_k": 3}),
+    ((1792, 1796, 1793), {"stream_k": 3}), ((3072, 3072, 3072), {"stream_k": 3}),
     ((4096, 4096, 4096), {"stream_k": 3}), ((8192, 8192, 8192), {"stream_k": 3}),
     ((128, 16384, 16384), {"stream_k": 3}), ((128, 16384, 16384), {"stream_k": 3, "cta_group": 2}),
     ((256, 256, 4096), {"stream_k": 3}), ((300, 200, 150), {"stream_k": 3}),
