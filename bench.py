@@ -3,6 +3,7 @@
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
                   [--workload {gemm,softmax}] [--configs] [--sustained SECONDS]
                   [--sustained-leg SECONDS]
+  python bench.py --splits [--steps S]
   python bench.py --case M N K [--launches L] [--warmup W] [--cta-group G] [--tile-n T]
                   [--stages S] [--group-m G] [--max-ctas C] [--stream-k 0|1|2] [--flush-l2]
 
@@ -92,6 +93,9 @@ def parse():
     ap.add_argument("--cta-group", type=int, default=0)
     ap.add_argument("--stream-k", type=int, default=0, help="--case: 1 = whole tiles only, 2 = force split tiles")
     ap.add_argument("--flush-l2", action="store_true", help="--case: write 512 MiB before each launch")
+    ap.add_argument("--splits", action="store_true",
+                    help="instead of the benchmark line, time each work-split form (whole tiles, two-part split "
+                         "tail, stream-K) against the planner's choice on shapes where they differ")
     return ap.parse_args()
 
 
@@ -667,6 +671,21 @@ def run_configs(args):
             b.record()
         torch.cuda.synchronize()
         ms = statistics.median([a.elapsed_time(b) for a, b in pairs])
+        # the vendor library on the same operands and the same timing (FP16 in, FP32 out)
+        cublas_ms = None
+        try:
+            for _ in range(3):
+                torch.mm(A, B, out_dtype=torch.float32)
+            for a, b in pairs:
+                if fits:
+                    flush.fill_(1.0)
+                a.record()
+                torch.mm(A, B, out_dtype=torch.float32)
+                b.record()
+            torch.cuda.synchronize()
+            cublas_ms = statistics.median([a.elapsed_time(b) for a, b in pairs])
+        except (TypeError, RuntimeError):
+            pass
         pl = tct.gemm_f16_f32_plan(M, N, K, lda=K, ldb=N)
         tiles = pl["tiles"]
         slots = sms // pl["cta_group"]
@@ -678,7 +697,8 @@ def run_configs(args):
                 "tiles": tiles, "units": pl["units"], "sm_slots": slots,
                 "waves": -(-tiles // slots), "page_wave_utilization": tiles / (-(-tiles // slots) * slots),
                 "split_tiles": pl["stream_k_tiles"], "effective_waves": pl["effective_waves"],
-                "l2_flushed": fits, "repack": bool(pl["pack_a"] or pl["pack_b"])}
+                "l2_flushed": fits, "repack": bool(pl["pack_a"] or pl["pack_b"]), "split_form": pl["split_form"],
+                "cublas_us": cublas_ms * 1e3 if cublas_ms else None}
         print(json.dumps(line), flush=True)
         del A, B, C
     # operand storage and type at 8192^3: the four layouts of gemm_f32acc, FP16 then BF16
@@ -998,6 +1018,60 @@ def run_softmax(args):
     return 0
 
 
+SPLIT_SHAPES = [(256, 256, 65536), (128, 512, 32768), (512, 512, 16384), (1024, 1024, 32768), (1024, 1024, 8192),
+                (128, 4096, 8192), (256, 256, 4096), (1792, 1792, 1792), (2048, 2048, 2048), (4096, 4096, 4096),
+                (8192, 8192, 8192), (128, 16384, 16384)]
+SPLIT_FORMS = (("whole tiles", {"stream_k": 1}), ("two-part split tail", {"stream_k": 2}),
+               ("stream-K", {"stream_k": 3}), ("planner's choice", {}))
+
+
+def run_splits(args):
+    """Each work-split form on shapes where they differ: median device time over launches (L2
+    flushed before each launch when the operands fit in L2), with the plan's form, the units
+    sharing the stream-K k-blocks and the most pieces one tile is cut into."""
+    import torch
+
+    import tensor_core_tiled_gb300 as tct
+    from tensor_core_tiled_gb300 import build as lib_build
+
+    lib_build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for M, N, K in SPLIT_SHAPES:
+        g = torch.Generator(device=dev).manual_seed(0)
+        A = torch.randn(M, K, device=dev, generator=g).half()
+        B = torch.randn(K, N, device=dev, generator=g).half()
+        C = torch.empty(M, N, device=dev)
+        fits = (A.numel() + B.numel()) * 2 < 100e6
+        for name, opts in SPLIT_FORMS:
+            try:
+                pl = tct.gemm_f16_f32_plan(M, N, K, **opts)
+            except tct.GemmError as e:
+                print(json.dumps({"M": M, "N": N, "K": K, "form": name, "unavailable": str(e)}), flush=True)
+                continue
+            for _ in range(3):
+                tct.matmul(A, B, C, **opts)
+            reps = max(5, min(args.steps, 30))
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for a, b in pairs:
+                if fits:
+                    flush.fill_(1.0)
+                a.record()
+                tct.matmul(A, B, C, **opts)
+                b.record()
+            torch.cuda.synchronize()
+            ms = statistics.median([a.elapsed_time(b) for a, b in pairs])
+            print(json.dumps({"M": M, "N": N, "K": K, "form": name, "us": ms * 1e3,
+                              "tflops": 2 * M * N * K / ms / 1e9, "cta_group": pl["cta_group"],
+                              "tile": [pl["tile_m"], pl["tile_n"]], "split_form": pl["split_form"],
+                              "split_tiles": pl["stream_k_tiles"], "sk_units": pl["sk_units"],
+                              "pieces_or_parts": pl["split_parts_per_unit"], "l2_flushed": fits}), flush=True)
+        del A, B, C
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    return 0
+
+
 def run_sustained(args):
     """4096^3 and 8192^3 launched back to back for args.sustained seconds each (after a
     second of warm-up): whole-loop TFLOP/s by CUDA events, with the median SM clock, the
@@ -1090,6 +1164,8 @@ def main():
         return run_reference(args)
     if args.case:
         return run_case(args)
+    if args.splits:
+        return run_splits(args)
     if args.configs:
         return run_configs(args)
     if args.sustained > 0:
