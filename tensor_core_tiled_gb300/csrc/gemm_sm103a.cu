@@ -414,109 +414,78 @@ __device__ __forceinline__ bool bulk_accumulator(uint32_t t_row, const void *tma
             ++cphase;
         }
     }
-    // The accumulator is read 32 columns at a time (a wide block takes two reads).  With
-    // kOwnBlocks every block has its own staging area, so kBatch reads are issued before one
-    // wait and their blocks go out together: the tensor-memory latency and the proxy fence
-    // are paid BN / 32 / kBatch times instead of BN / 32 (measured: the last tile's stores
-    // took 0.35-0.4 us per 32-column block one at a time).
-    constexpr int kReads = BN / 32;
-    constexpr int kBatch = kOwnBlocks ? (kReads < 4 ? kReads : 4) : 1;
-    for (int sb0 = 0; sb0 < kReads; sb0 += kBatch) {
-        if constexpr (!kOwnBlocks) {
-            const int blk = kWide ? sb0 >> 1 : sb0;
-            const int half = kWide ? sb0 & 1 : 0;
-            if (half == 0) {
-                if (blk > 0) {  // the previous block has been read out of the staging buffer
-                    if (lane == 0) bulk_wait_read_all();
-                    __syncwarp();
-                }
-                if (read_c && block_in(blk)) {
-                    if (lane == 0 && !skip_c_load) {
-                        mbar_arrive_expect_tx(cbar, 4096u);
-                        load_c(blk, stage);
-                    }
+    // The accumulator is read 32 columns at a time (a wide block takes two reads).
+    for (int sb = 0; sb < BN / 32; ++sb) {
+        const int blk = kWide ? sb >> 1 : sb;
+        const int half = kWide ? sb & 1 : 0;
+        const int64_t c0 = col0 + blk * kCols;  // first column of the staged block
+        float *block = kOwnBlocks ? stage + blk * 32 * 32 : stage;
+        if (!kOwnBlocks && half == 0) {
+            if (blk > 0) {  // the previous block has been read out of the staging buffer
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+            }
+            if (read_c && block_in(blk)) {
+                if (lane == 0 && !skip_c_load) {
+                    mbar_arrive_expect_tx(cbar, 4096u);
+                    load_c(blk, block);
                 }
             }
         }
-        uint32_t r[kBatch][32];
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) tmem_ld_32x32b_x32(t_row + (sb0 + b) * 32, r[b]);
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + sb * 32, r);
         tmem_wait_ld();
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) tmem_regs_ready(r[b]);
-        if (sb0 + kBatch == kReads) {
+        if (sb == BN / 32 - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) release();
         }
-        if constexpr (!kOwnBlocks) {
-            const int blk = kWide ? sb0 >> 1 : sb0;
-            const int half = kWide ? sb0 & 1 : 0;
-            if (half == 0 && read_c && block_in(blk)) {
-                ok = wait_or_abort<false>(cbar, cphase & 1u, limit, abort_flag, SITE_EPI_PARTS) && ok;
-                ++cphase;
-            }
+        if (!kOwnBlocks && half == 0 && read_c && block_in(blk)) {
+            ok = wait_or_abort<false>(cbar, cphase & 1u, limit, abort_flag, SITE_EPI_PARTS) && ok;
+            ++cphase;
         }
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        uint4 *srow = reinterpret_cast<uint4 *>(block + lane * 32);
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            const int sb = sb0 + b;
-            const int blk = kWide ? sb >> 1 : sb;
-            const int half = kWide ? sb & 1 : 0;
-            float *block = kOwnBlocks ? stage + blk * 32 * 32 : stage;
-            uint4 *srow = reinterpret_cast<uint4 *>(block + lane * 32);
-#pragma unroll
-            for (int u = 0; u < kUnits; ++u) {
-                const int j = half * kUnits + u;  // 16-byte unit of the staged row
-                const float *bj = sbias + blk * kCols + j * kChunk;  // bias of the unit's columns
-                const uint4 craw = read_c ? srow[j ^ (lane & 7)] : make_uint4(0u, 0u, 0u, 0u);
-                uint4 out;
-                if constexpr (!kWide) {
-                    float4 v = make_float4(__uint_as_float(r[b][4 * u + 0]), __uint_as_float(r[b][4 * u + 1]),
-                                           __uint_as_float(r[b][4 * u + 2]), __uint_as_float(r[b][4 * u + 3]));
-                    if (d.epi) {
-                        const float4 bb = d.bias ? *reinterpret_cast<const float4 *>(bj) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v = apply_epilogue(d, v, raw_to_float4(craw, 2, false), bb);
-                    }
-                    out = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
-                                     __float_as_uint(v.w));
-                } else {
-                    float4 lo = make_float4(__uint_as_float(r[b][8 * u + 0]), __uint_as_float(r[b][8 * u + 1]),
-                                            __uint_as_float(r[b][8 * u + 2]), __uint_as_float(r[b][8 * u + 3]));
-                    float4 hi = make_float4(__uint_as_float(r[b][8 * u + 4]), __uint_as_float(r[b][8 * u + 5]),
-                                            __uint_as_float(r[b][8 * u + 6]), __uint_as_float(r[b][8 * u + 7]));
-                    if (d.epi) {
-                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                        const float4 b_lo = d.bias ? *reinterpret_cast<const float4 *>(bj) : z;
-                        const float4 b_hi = d.bias ? *reinterpret_cast<const float4 *>(bj + 4) : z;
-                        lo = apply_epilogue(d, lo, raw_to_float4(make_uint4(craw.x, craw.y, 0u, 0u), d.out_type, true),
-                                            b_lo);
-                        hi = apply_epilogue(d, hi, raw_to_float4(make_uint4(craw.z, craw.w, 0u, 0u), d.out_type, true),
-                                            b_hi);
-                    }
-                    out = make_uint4(pack_16bit(lo.x, lo.y, d.out_type), pack_16bit(lo.z, lo.w, d.out_type),
-                                     pack_16bit(hi.x, hi.y, d.out_type), pack_16bit(hi.z, hi.w, d.out_type));
+        for (int u = 0; u < kUnits; ++u) {
+            const int j = half * kUnits + u;  // 16-byte unit of the staged row
+            const float *bj = sbias + blk * kCols + j * kChunk;  // bias of the unit's columns
+            const uint4 craw = read_c ? srow[j ^ (lane & 7)] : make_uint4(0u, 0u, 0u, 0u);
+            uint4 out;
+            if constexpr (!kWide) {
+                float4 v = make_float4(__uint_as_float(r[4 * u + 0]), __uint_as_float(r[4 * u + 1]),
+                                       __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+                if (d.epi) {
+                    const float4 b = d.bias ? *reinterpret_cast<const float4 *>(bj) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v = apply_epilogue(d, v, raw_to_float4(craw, 2, false), b);
                 }
-                srow[j ^ (lane & 7)] = out;
+                out = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
+            } else {
+                float4 lo = make_float4(__uint_as_float(r[8 * u + 0]), __uint_as_float(r[8 * u + 1]),
+                                        __uint_as_float(r[8 * u + 2]), __uint_as_float(r[8 * u + 3]));
+                float4 hi = make_float4(__uint_as_float(r[8 * u + 4]), __uint_as_float(r[8 * u + 5]),
+                                        __uint_as_float(r[8 * u + 6]), __uint_as_float(r[8 * u + 7]));
+                if (d.epi) {
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 b_lo = d.bias ? *reinterpret_cast<const float4 *>(bj) : z;
+                    const float4 b_hi = d.bias ? *reinterpret_cast<const float4 *>(bj + 4) : z;
+                    lo = apply_epilogue(d, lo, raw_to_float4(make_uint4(craw.x, craw.y, 0u, 0u), d.out_type, true), b_lo);
+                    hi = apply_epilogue(d, hi, raw_to_float4(make_uint4(craw.z, craw.w, 0u, 0u), d.out_type, true), b_hi);
+                }
+                out = make_uint4(pack_16bit(lo.x, lo.y, d.out_type), pack_16bit(lo.z, lo.w, d.out_type),
+                                 pack_16bit(hi.x, hi.y, d.out_type), pack_16bit(hi.z, hi.w, d.out_type));
             }
+            srow[j ^ (lane & 7)] = out;
         }
-        // The blocks completed by this batch (a wide block is complete after its second half).
-        const int done_lo = kWide ? sb0 >> 1 : sb0;
-        const int done_hi = kWide ? (sb0 + kBatch) >> 1 : sb0 + kBatch;
-        if (done_hi == done_lo) continue;
-        fence_proxy_async_smem();  // this lane's generic writes before the async-proxy read
+        if (kWide && half == 0) continue;  // the block's second half is still to come
+        fence_proxy_async_smem();          // this lane's generic writes before the async-proxy read
         __syncwarp();
-        if (lane == 0) {
-            for (int blk = done_lo; blk < done_hi; ++blk) {
-                if (!block_in(blk)) continue;
-                float *block = kOwnBlocks ? stage + blk * 32 * 32 : stage;
-                const int64_t c0 = col0 + blk * kCols;  // first column of the staged block
-                if constexpr (kReduce)
-                    tma_reduce_add_2d(tmap_c, static_cast<int32_t>(c0), static_cast<int32_t>(row0), smem_u32(block));
-                else
-                    tma_store_2d(tmap_c, static_cast<int32_t>(c0), static_cast<int32_t>(row0), smem_u32(block));
-            }
+        if (lane == 0 && block_in(blk)) {
+            if constexpr (kReduce)
+                tma_reduce_add_2d(tmap_c, static_cast<int32_t>(c0), static_cast<int32_t>(row0), smem_u32(block));
+            else
+                tma_store_2d(tmap_c, static_cast<int32_t>(c0), static_cast<int32_t>(row0), smem_u32(block));
             bulk_commit_group();
         }
     }

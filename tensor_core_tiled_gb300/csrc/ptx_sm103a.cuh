@@ -178,18 +178,6 @@ __device__ __forceinline__ void tmem_wait_ld()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Placed after tmem_wait_ld: ties every later use of r to this point, so that the compiler
-// cannot move arithmetic on the loaded registers above the wait.
-__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32])
-{
-    asm volatile(""
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
-                   "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
-                   "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
-}
-
 // 2-D TMA reduce-add of a shared-memory box into global memory (element type and box from the
 // tensor map; boxes reaching past the tensor are clipped).  Completion is tracked by the
 // thread's bulk-async groups.
