@@ -183,6 +183,21 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUte
                         const KernelParams &p, int layout, int cta_group, int tile_n, int stages, int grid,
                         cudaStream_t stream);
 
+// One matrix of a row copy: rows x cols elements of esz bytes (2 or 4), leading dimensions
+// in elements; a NULL src skips it.
+struct RowCopy {
+    const void *src;
+    int64_t ld_src;
+    void *dst;
+    int64_t ld_dst;
+    int64_t rows, cols;
+    int32_t esz;
+};
+
+// Copies up to two matrices in one launch between layouts whose rows may start on any element
+// boundary (programmatic dependent launch: it waits for the kernel before it).
+cudaError_t launch_copy_rows(const RowCopy &m0, const RowCopy &m1, cudaStream_t stream);
+
 // Copies up to two FP16 operands (a NULL src skips one) into buffers with 16-byte aligned rows,
 // in one launch.
 cudaError_t launch_pack2(const void *src0, int64_t ld_src0, void *dst0, int64_t ld_dst0, int64_t rows0, int64_t cols0,

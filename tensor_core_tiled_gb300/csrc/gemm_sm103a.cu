@@ -949,35 +949,39 @@ __global__ void __launch_bounds__(192, 1)
 
 // ---------------------------------------------------------------- helper kernels
 
-// Row copy into buffers whose rows start on 16-byte boundaries (TMA's stride rule), for up
-// to two operands in one launch: blocks [0, j0.blocks) copy rows of operand 0, the rest rows
-// of operand 1.  A row is copied by a group of g lanes of one warp (g a power of two, the
-// smallest that covers the row's 16-byte units, at most 32), so a warp copies 32 / g short
-// rows at once and a block of kPackWarps warps copies 8 * 32 / g rows; nothing idles on
-// rows much narrower than a block.  Each lane moves 8 consecutive elements (16 bytes) at a
-// time, up to kPackUnroll units loaded before any is stored.  A source row may start on any
-// 2-byte boundary, so 16 bytes generally straddle two aligned 16-byte blocks: both are
-// loaded whole and the bytes realigned with funnel shifts.  Each of the two blocks holds at
-// least one byte of the 8 elements, so no load reaches outside the 16-byte blocks the row
-// occupies.  A row's last, partial group of elements is copied element by element.
-constexpr int kPackWarps = 8;
-constexpr int kPackUnroll = 4;
+// Row copy between two layouts whose rows may start on any element boundary, for up to two
+// matrices in one launch: blocks [0, j0.blocks) copy rows of matrix 0, the rest rows of
+// matrix 1.  It repacks operands into rows that start on 16-byte boundaries (TMA's stride
+// rule) and moves a product from an aligned temporary into a C that TMA cannot write.  A
+// row is copied by a group of g lanes of one warp (g a power of two, the smallest that
+// covers the row's 16-byte units, at most 32), so a warp copies 32 / g short rows at once
+// and a block of kCopyWarps warps 8 * 32 / g rows; nothing idles on rows much narrower than a
+// block.  The destination row is written in whole, aligned 16-byte units, up to kCopyUnroll
+// loaded before any is stored; the few elements before its first and after its last
+// aligned unit are copied one by one.  The 16 source bytes of a unit may straddle two
+// aligned 16-byte blocks: both are loaded whole and the bytes realigned with funnel shifts.
+// Each of the two blocks holds at least one byte of the unit, which lies inside the source
+// row, so no load reaches outside the 16-byte blocks the row occupies.
+constexpr int kCopyWarps = 8;
+constexpr int kCopyUnroll = 4;
 
-struct PackJob {
-    const uint16_t *src;
-    int64_t ld_src;
-    uint16_t *dst;
-    int64_t ld_dst;
-    int64_t rows, cols;
+struct CopyJob {
+    const uint8_t *src;
+    int64_t ld_src;  // bytes between rows
+    uint8_t *dst;
+    int64_t ld_dst;  // bytes between rows
+    int64_t rows;
+    int64_t row_bytes;
+    int32_t esz;            // element size: 2 or 4 bytes
     int32_t lanes_per_row;  // g
     int64_t blocks;
 };
 
-// Elements [8u, 8u + 8) of a source row starting at `s` (2-byte aligned), realigned.
-__device__ __forceinline__ uint4 load_unit_realigned(const uint16_t *__restrict__ s, int64_t u)
+// 16 bytes starting at any byte address p, realigned from the two aligned blocks they touch.
+__device__ __forceinline__ uint4 load16_realigned(const uint8_t *p)
 {
-    const uintptr_t addr = reinterpret_cast<uintptr_t>(s + 8 * u);
-    const uint32_t off = static_cast<uint32_t>(addr & 15u);  // 0, 2, ..., 14
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(p);
+    const uint32_t off = static_cast<uint32_t>(addr & 15u);
     const uint4 *blk = reinterpret_cast<const uint4 *>(addr - off);
     const uint4 lo = __ldg(blk);
     const uint4 hi = off ? __ldg(blk + 1) : make_uint4(0u, 0u, 0u, 0u);
@@ -993,32 +997,55 @@ __device__ __forceinline__ uint4 load_unit_realigned(const uint16_t *__restrict_
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__global__ void __launch_bounds__(kPackWarps * 32) pack_rows_f16(const PackJob j0, const PackJob j1)
+// Elements [e0, e1) of a row, one at a time, e0 + sub, e0 + sub + g, ...
+__device__ __forceinline__ void copy_elements(const uint8_t *s, uint8_t *d, int64_t e0, int64_t e1, int esz, int sub,
+                                              int g)
 {
-    // The next kernel (the GEMM) may start its set-up; it reads these rows only after its
-    // dependency wait, i.e. after this grid has completed.
+    for (int64_t e = e0 + sub; e < e1; e += g) {
+        if (esz == 4)
+            reinterpret_cast<uint32_t *>(d)[e] = reinterpret_cast<const uint32_t *>(s)[e];
+        else
+            reinterpret_cast<uint16_t *>(d)[e] = reinterpret_cast<const uint16_t *>(s)[e];
+    }
+}
+
+__global__ void __launch_bounds__(kCopyWarps * 32) copy_rows(const CopyJob j0, const CopyJob j1)
+{
+    // Launched as a programmatic dependent launch: wait for the kernel before it (which may
+    // write the source), then let the next kernel start its set-up; that kernel reads these
+    // rows only after its own dependency wait, i.e. after this grid has completed.
+    griddep_wait();
     griddep_launch_dependents();
     const bool first = blockIdx.x < j0.blocks;
-    const PackJob &j = first ? j0 : j1;
+    const CopyJob &j = first ? j0 : j1;
     const int64_t blk = first ? blockIdx.x : blockIdx.x - j0.blocks;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = j.lanes_per_row;
-    const int64_t r = (blk * kPackWarps + warp) * (32 / g) + lane / g;
+    const int64_t r = (blk * kCopyWarps + warp) * (32 / g) + lane / g;
     if (r >= j.rows) return;
     const int sub = lane & (g - 1);
-    const uint16_t *__restrict__ s = j.src + r * j.ld_src;
-    uint16_t *__restrict__ d = j.dst + r * j.ld_dst;
-    const int64_t units = j.cols / 8;
-    for (int64_t u0 = sub; u0 < units; u0 += kPackUnroll * g) {
-        uint4 v[kPackUnroll];
-#pragma unroll
-        for (int t = 0; t < kPackUnroll; ++t)
-            if (u0 + t * g < units) v[t] = load_unit_realigned(s, u0 + t * g);
-#pragma unroll
-        for (int t = 0; t < kPackUnroll; ++t)
-            if (u0 + t * g < units) *reinterpret_cast<uint4 *>(d + 8 * (u0 + t * g)) = v[t];
+    const uint8_t *s = j.src + r * j.ld_src;
+    uint8_t *d = j.dst + r * j.ld_dst;
+    const int64_t n = j.row_bytes / j.esz;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(d), d1 = d0 + static_cast<uintptr_t>(j.row_bytes);
+    const uintptr_t a0 = (d0 + 15u) & ~uintptr_t(15), a1 = d1 & ~uintptr_t(15);
+    if (a0 >= a1) {  // no whole aligned unit in the destination row
+        copy_elements(s, d, 0, n, j.esz, sub, g);
+        return;
     }
-    for (int64_t i = units * 8 + sub; i < j.cols; i += g) d[i] = s[i];
+    const int64_t head = static_cast<int64_t>(a0 - d0);  // bytes before the first aligned unit
+    const int64_t units = static_cast<int64_t>(a1 - a0) >> 4;
+    copy_elements(s, d, 0, head / j.esz, j.esz, sub, g);
+    for (int64_t u0 = sub; u0 < units; u0 += kCopyUnroll * g) {
+        uint4 v[kCopyUnroll];
+#pragma unroll
+        for (int t = 0; t < kCopyUnroll; ++t)
+            if (u0 + t * g < units) v[t] = load16_realigned(s + head + 16 * (u0 + t * g));
+#pragma unroll
+        for (int t = 0; t < kCopyUnroll; ++t)
+            if (u0 + t * g < units) *reinterpret_cast<uint4 *>(d + head + 16 * (u0 + t * g)) = v[t];
+    }
+    copy_elements(s, d, (head + 16 * units) / j.esz, n, j.esz, sub, g);
 }
 
 // K == 0: the empty sum, through the epilogue (C = beta * C + bias[col], or zeros).
@@ -1176,34 +1203,50 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUte
     }
 }
 
-// Lanes per row for a row of `cols` elements: the smallest power of two that covers its
+// Lanes per row for a row of `bytes` bytes: the smallest power of two that covers its
 // 16-byte units, at most a warp.
-static int pack_lanes_per_row(int64_t cols)
+static int copy_lanes_per_row(int64_t bytes)
 {
-    const int64_t units = (cols + 7) / 8;
+    const int64_t units = (bytes + 15) / 16;
     int g = 1;
     while (g < 32 && g < units) g *= 2;
     return g;
+}
+
+cudaError_t launch_copy_rows(const RowCopy &m0, const RowCopy &m1, cudaStream_t stream)
+{
+    auto job = [](const RowCopy &m) {
+        CopyJob j{static_cast<const uint8_t *>(m.src), m.ld_src * m.esz, static_cast<uint8_t *>(m.dst),
+                  m.ld_dst * m.esz, m.src ? m.rows : 0, m.cols * m.esz, m.esz, copy_lanes_per_row(m.cols * m.esz), 0};
+        const int64_t rows_per_block = static_cast<int64_t>(kCopyWarps) * (32 / j.lanes_per_row);
+        j.blocks = (j.rows + rows_per_block - 1) / rows_per_block;
+        return j;
+    };
+    if ((m0.src && m0.esz != 2 && m0.esz != 4) || (m1.src && m1.esz != 2 && m1.esz != 4)) return cudaErrorInvalidValue;
+    const CopyJob j0 = job(m0);
+    const CopyJob j1 = job(m1);
+    const int64_t blocks = j0.blocks + j1.blocks;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 2147483647ll) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kCopyWarps * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, copy_rows, j0, j1);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_pack2(const void *src0, int64_t ld_src0, void *dst0, int64_t ld_dst0, int64_t rows0, int64_t cols0,
                          const void *src1, int64_t ld_src1, void *dst1, int64_t ld_dst1, int64_t rows1, int64_t cols1,
                          cudaStream_t stream)
 {
-    auto job = [](const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows, int64_t cols) {
-        PackJob j{static_cast<const uint16_t *>(src), ld_src, static_cast<uint16_t *>(dst), ld_dst,
-                  src ? rows : 0, cols, pack_lanes_per_row(cols), 0};
-        const int64_t rows_per_block = static_cast<int64_t>(kPackWarps) * (32 / j.lanes_per_row);
-        j.blocks = (j.rows + rows_per_block - 1) / rows_per_block;
-        return j;
-    };
-    const PackJob j0 = job(src0, ld_src0, dst0, ld_dst0, rows0, cols0);
-    const PackJob j1 = job(src1, ld_src1, dst1, ld_dst1, rows1, cols1);
-    const int64_t blocks = j0.blocks + j1.blocks;
-    if (blocks <= 0) return cudaSuccess;
-    if (blocks > 2147483647ll) return cudaErrorInvalidValue;
-    pack_rows_f16<<<static_cast<unsigned>(blocks), kPackWarps * 32, 0, stream>>>(j0, j1);
-    return cudaGetLastError();
+    return launch_copy_rows(RowCopy{src0, ld_src0, dst0, ld_dst0, rows0, cols0, 2},
+                            RowCopy{src1, ld_src1, dst1, ld_dst1, rows1, cols1, 2}, stream);
 }
 
 cudaError_t launch_fill_epilogue(const KernelParams &p, int num_sms, cudaStream_t stream)

@@ -143,8 +143,10 @@ def _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt, offset, ldc, **op
 def test_tma_and_lane_store_paths_agree(ct, alpha, beta, bt, opts):
     """The same problem with C where TMA can write it (16-byte aligned base and pitch, rows of
     whole 16-byte units: the tile goes out through swizzled staging and TMA stores, C read by
-    TMA when beta != 0) and one element off that alignment (per-lane stores): the same bits,
-    since both paths apply the same operations; nothing outside the M x N block changes."""
+    TMA when beta != 0), and one element off that alignment, written either through the
+    aligned temporary (TMA stores, then the row copy; C copied in first when beta != 0) or
+    directly by per-lane stores (c_direct): the same bits, since every path applies the same
+    operations; nothing outside the M x N block changes."""
     rng = np.random.default_rng(75)
     M, N, K = 333, 520, 200
     A, B = inputs.pair_ex(rng, M, N, K, dtype="f16")
@@ -152,9 +154,10 @@ def test_tma_and_lane_store_paths_agree(ct, alpha, beta, bt, opts):
     bias = _typed_random(rng, (N,), bt) if bt else None
     ldc = N + 8
     tma, rest_t = _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt or "f32", 0, ldc, **opts)
-    lane, rest_l = _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt or "f32", 1, ldc, **opts)
-    assert np.all(rest_t == -1) and np.all(rest_l == -1)
-    assert np.array_equal(tma, lane)
+    temp, rest_m = _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt or "f32", 1, ldc, **opts)
+    lane, rest_l = _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt or "f32", 1, ldc, c_direct=1, **opts)
+    assert np.all(rest_t == -1) and np.all(rest_m == -1) and np.all(rest_l == -1)
+    assert np.array_equal(tma, lane) and np.array_equal(tma, temp)
     want = run_ref(A, B, "f16", False, False, ct, alpha, beta, Cin, bias, bt or "f32")
     S = np.abs(oracle.gemm_ex_f32(A, B))
     got = tma if ct == "f32" else tma.view(np.uint16)
@@ -239,3 +242,46 @@ def test_torch_helper():
     got16 = out16.cpu().view(torch.int16).numpy().view(np.uint16)
     want16 = run_ref(A, B, "f16", False, False, "bf16", 1.0, 0.0, None, None, "f32")
     assert close(got16, want16, "bf16", K, 1.0, S)
+
+
+@pytest.mark.parametrize("ct", ["f32", "f16", "bf16"])
+def test_beta_with_unaligned_c(ct):
+    """beta != 0 on a C that TMA cannot write: C's current values are copied into the aligned
+    temporary before the product, the epilogue reads them there, and the result is copied
+    back; gap columns and the elements around C keep their bits."""
+    rng = np.random.default_rng(77)
+    M, N, K, pad = 301, 203, 160, 3
+    A, B = inputs.pair_ex(rng, M, N, K, dtype="f16")
+    Cin = _typed_random(rng, (M, N + pad), ct)
+    bias = _typed_random(rng, (N,), "f32")
+    esz = 4 if ct == "f32" else 2
+    off = 1  # one element past an aligned address
+    total = off + M * (N + pad) + 8
+    if ct == "f32":
+        buf = torch.full((total,), float("nan"), dtype=torch.float32, device="cuda")
+        buf[off:off + M * (N + pad)] = torch.from_numpy(np.ascontiguousarray(Cin).reshape(-1)).cuda()
+    else:
+        tt = torch.float16 if ct == "f16" else torch.bfloat16
+        buf = torch.full((total,), float("nan"), dtype=tt, device="cuda")
+        buf[off:off + M * (N + pad)] = torch.from_numpy(np.ascontiguousarray(Cin).view(np.int16).reshape(-1)).cuda().view(tt)
+    before = buf.clone()
+    dA, dB = _dev(A, "f16"), _dev(B, "f16")
+    dbias = _dev(bias, "f32")
+    st = tct.gemm_ex(TYPES["f16"][1], 0, 0, dA.data_ptr(), dB.data_ptr(), buf.data_ptr() + off * esz, TYPES[ct][1],
+                     M, N, K, K, N, N + pad, alpha=0.75, beta=-1.5, bias=dbias.data_ptr(), bias_type=TYPES["f32"][1],
+                     stream=torch.cuda.current_stream().cuda_stream)
+    assert st == tct.GEMM_OK
+    torch.cuda.synchronize()
+    if ct == "f32":
+        got_all = buf.cpu().numpy()
+        was = before.cpu().numpy()
+    else:
+        got_all = buf.cpu().view(torch.int16).numpy().view(np.uint16)
+        was = before.cpu().view(torch.int16).numpy().view(np.uint16)
+    body = got_all[off:off + M * (N + pad)].reshape(M, N + pad)
+    assert np.array_equal(got_all[:off].view(np.uint8), was[:off].view(np.uint8))
+    assert np.array_equal(got_all[off + M * (N + pad):].view(np.uint8), was[off + M * (N + pad):].view(np.uint8))
+    assert np.array_equal(body[:, N:].view(np.uint8), np.ascontiguousarray(Cin)[:, N:].view(np.uint8))
+    want = run_ref(A, B, "f16", False, False, ct, 0.75, -1.5, np.ascontiguousarray(Cin[:, :N]), bias, "f32")
+    S = np.abs(oracle.gemm_ex_f32(A, B, dtype=oracle.F16))
+    assert close(body[:, :N], want, ct, K, 0.75, S + 1.5 * np.abs(_as_float(Cin[:, :N], ct)) + 4)
