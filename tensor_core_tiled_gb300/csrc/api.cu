@@ -636,10 +636,10 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
         // the operands' repack, and C's current values when the epilogue reads them
         cudaError_t e = tct::launch_copy_rows(
             tct::RowCopy{pl.pack_a ? A : nullptr, lda, w, lda_p, a_rows, a_cols, 2},
-            tct::RowCopy{pl.pack_b ? B : nullptr, ldb, w + a_bytes, ldb_p, b_rows, b_cols, 2}, s);
+            tct::RowCopy{pl.pack_b ? B : nullptr, ldb, w + a_bytes, ldb_p, b_rows, b_cols, 2}, s, dev.sms);
         if (e == cudaSuccess && c_temp && read_c)
             e = tct::launch_copy_rows(tct::RowCopy{C, ldc, c_use, ldt, M, N, esz_c},
-                                      tct::RowCopy{nullptr, 0, nullptr, 0, 0, 0, esz_c}, s);
+                                      tct::RowCopy{nullptr, 0, nullptr, 0, 0, 0, esz_c}, s, dev.sms);
         if (e == cudaSuccess && f_bytes)  // the split tiles' flags start lowered
             e = cudaMemsetAsync(w + a_bytes + b_bytes + w_bytes, 0, static_cast<size_t>(f_bytes), s);
         if (e != cudaSuccess) {
@@ -683,7 +683,7 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
             st = to_status(tct::launch_gemm(ta, tb, tp, tc, p, layout, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
         if (st == GEMM_OK && c_temp)  // the product into C, element-aligned rows
             st = to_status(tct::launch_copy_rows(tct::RowCopy{c_use, ldt, C, ldc, M, N, esz_c},
-                                                 tct::RowCopy{nullptr, 0, nullptr, 0, 0, 0, esz_c}, s));
+                                                 tct::RowCopy{nullptr, 0, nullptr, 0, 0, 0, esz_c}, s, dev.sms));
     }
     if (ws) {
         if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;

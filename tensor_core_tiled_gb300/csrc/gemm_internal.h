@@ -196,7 +196,7 @@ struct RowCopy {
 
 // Copies up to two matrices in one launch between layouts whose rows may start on any element
 // boundary (programmatic dependent launch: it waits for the kernel before it).
-cudaError_t launch_copy_rows(const RowCopy &m0, const RowCopy &m1, cudaStream_t stream);
+cudaError_t launch_copy_rows(const RowCopy &m0, const RowCopy &m1, cudaStream_t stream, int num_sms);
 
 // Copies up to two FP16 operands (a NULL src skips one) into buffers with 16-byte aligned rows,
 // in one launch.

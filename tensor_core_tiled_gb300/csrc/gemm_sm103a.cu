@@ -40,6 +40,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <type_traits>
 
@@ -950,20 +951,19 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------- helper kernels
 
 // Row copy between two layouts whose rows may start on any element boundary, for up to two
-// matrices in one launch: blocks [0, j0.blocks) copy rows of matrix 0, the rest rows of
-// matrix 1.  It repacks operands into rows that start on 16-byte boundaries (TMA's stride
-// rule) and moves a product from an aligned temporary into a C that TMA cannot write.  A
-// row is copied by a group of g lanes of one warp (g a power of two, the smallest that
-// covers the row's 16-byte units, at most 32), so a warp copies 32 / g short rows at once
-// and a block of kCopyWarps warps 8 * 32 / g rows; nothing idles on rows much narrower than a
-// block.  The destination row is written in whole, aligned 16-byte units, up to kCopyUnroll
-// loaded before any is stored; the few elements before its first and after its last
-// aligned unit are copied one by one.  The 16 source bytes of a unit may straddle two
-// aligned 16-byte blocks: both are loaded whole and the bytes realigned with funnel shifts.
-// Each of the two blocks holds at least one byte of the unit, which lies inside the source
-// row, so no load reaches outside the 16-byte blocks the row occupies.
-constexpr int kCopyWarps = 8;
-constexpr int kCopyUnroll = 4;
+// matrices in one launch.  It repacks operands into rows that start on 16-byte boundaries
+// (TMA's stride rule) and moves a product from an aligned temporary into a C that TMA cannot
+// write.  Each destination row is written in whole, aligned 16-byte units; the few elements
+// before its first and after its last aligned unit are copied one by one.  The work is
+// flattened: index u of row r (u < units_max, one more than the most whole units a row of
+// this length can hold) is one thread's work -- aligned unit u when the row has that many,
+// else, for the first index past the row's units, the row's loose elements -- so every
+// thread has a single, independent copy in flight and the grid strides over all rows of
+// both matrices.  The 16 source bytes of a unit may straddle two aligned 16-byte blocks: both
+// are loaded whole and the bytes realigned with funnel shifts.  Each of the two blocks holds
+// at least one byte of the unit, which lies inside the source row, so no load reaches
+// outside the 16-byte blocks the row occupies.
+constexpr int kCopyThreads = 256;
 
 struct CopyJob {
     const uint8_t *src;
@@ -972,9 +972,8 @@ struct CopyJob {
     int64_t ld_dst;  // bytes between rows
     int64_t rows;
     int64_t row_bytes;
-    int32_t esz;            // element size: 2 or 4 bytes
-    int32_t lanes_per_row;  // g
-    int64_t blocks;
+    int32_t esz;        // element size: 2 or 4 bytes
+    int64_t units_max;  // work indices per row
 };
 
 // 16 bytes starting at any byte address p, realigned from the two aligned blocks they touch.
@@ -997,11 +996,10 @@ __device__ __forceinline__ uint4 load16_realigned(const uint8_t *p)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Elements [e0, e1) of a row, one at a time, e0 + sub, e0 + sub + g, ...
-__device__ __forceinline__ void copy_elements(const uint8_t *s, uint8_t *d, int64_t e0, int64_t e1, int esz, int sub,
-                                              int g)
+// Elements [e0, e1) of a row, one at a time.
+__device__ __forceinline__ void copy_elements(const uint8_t *s, uint8_t *d, int64_t e0, int64_t e1, int esz)
 {
-    for (int64_t e = e0 + sub; e < e1; e += g) {
+    for (int64_t e = e0; e < e1; ++e) {
         if (esz == 4)
             reinterpret_cast<uint32_t *>(d)[e] = reinterpret_cast<const uint32_t *>(s)[e];
         else
@@ -1009,43 +1007,44 @@ __device__ __forceinline__ void copy_elements(const uint8_t *s, uint8_t *d, int6
     }
 }
 
-__global__ void __launch_bounds__(kCopyWarps * 32) copy_rows(const CopyJob j0, const CopyJob j1)
+// Work index u of row r of job j.
+__device__ __forceinline__ void copy_unit(const CopyJob &j, int64_t r, int64_t u)
+{
+    const uint8_t *s = j.src + r * j.ld_src;
+    uint8_t *d = j.dst + r * j.ld_dst;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(d), d1 = d0 + static_cast<uintptr_t>(j.row_bytes);
+    const uintptr_t a0 = (d0 + 15u) & ~uintptr_t(15), a1 = d1 & ~uintptr_t(15);
+    const int64_t units = a1 > a0 ? static_cast<int64_t>(a1 - a0) >> 4 : 0;
+    const int64_t head = units > 0 ? static_cast<int64_t>(a0 - d0) : 0;  // bytes before the first aligned unit
+    if (u < units) {
+        *reinterpret_cast<uint4 *>(d + head + 16 * u) = load16_realigned(s + head + 16 * u);
+    } else if (u == units) {  // the loose elements: all of a row without a whole aligned unit
+        const int64_t n = j.row_bytes / j.esz;
+        if (units == 0) {
+            copy_elements(s, d, 0, n, j.esz);
+        } else {
+            copy_elements(s, d, 0, head / j.esz, j.esz);
+            copy_elements(s, d, (head + 16 * units) / j.esz, n, j.esz);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kCopyThreads) copy_rows(const CopyJob j0, const CopyJob j1)
 {
     // Launched as a programmatic dependent launch: wait for the kernel before it (which may
     // write the source), then let the next kernel start its set-up; that kernel reads these
     // rows only after its own dependency wait, i.e. after this grid has completed.
     griddep_wait();
     griddep_launch_dependents();
-    const bool first = blockIdx.x < j0.blocks;
-    const CopyJob &j = first ? j0 : j1;
-    const int64_t blk = first ? blockIdx.x : blockIdx.x - j0.blocks;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = j.lanes_per_row;
-    const int64_t r = (blk * kCopyWarps + warp) * (32 / g) + lane / g;
-    if (r >= j.rows) return;
-    const int sub = lane & (g - 1);
-    const uint8_t *s = j.src + r * j.ld_src;
-    uint8_t *d = j.dst + r * j.ld_dst;
-    const int64_t n = j.row_bytes / j.esz;
-    const uintptr_t d0 = reinterpret_cast<uintptr_t>(d), d1 = d0 + static_cast<uintptr_t>(j.row_bytes);
-    const uintptr_t a0 = (d0 + 15u) & ~uintptr_t(15), a1 = d1 & ~uintptr_t(15);
-    if (a0 >= a1) {  // no whole aligned unit in the destination row
-        copy_elements(s, d, 0, n, j.esz, sub, g);
-        return;
+    const int64_t t0 = j0.rows * j0.units_max, total = t0 + j1.rows * j1.units_max;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total; g += stride) {
+        const bool first = g < t0;
+        const CopyJob &j = first ? j0 : j1;
+        const int64_t x = first ? g : g - t0;
+        const int64_t r = x / j.units_max;
+        copy_unit(j, r, x - r * j.units_max);
     }
-    const int64_t head = static_cast<int64_t>(a0 - d0);  // bytes before the first aligned unit
-    const int64_t units = static_cast<int64_t>(a1 - a0) >> 4;
-    copy_elements(s, d, 0, head / j.esz, j.esz, sub, g);
-    for (int64_t u0 = sub; u0 < units; u0 += kCopyUnroll * g) {
-        uint4 v[kCopyUnroll];
-#pragma unroll
-        for (int t = 0; t < kCopyUnroll; ++t)
-            if (u0 + t * g < units) v[t] = load16_realigned(s + head + 16 * (u0 + t * g));
-#pragma unroll
-        for (int t = 0; t < kCopyUnroll; ++t)
-            if (u0 + t * g < units) *reinterpret_cast<uint4 *>(d + head + 16 * (u0 + t * g)) = v[t];
-    }
-    copy_elements(s, d, (head + 16 * units) / j.esz, n, j.esz, sub, g);
 }
 
 // K == 0: the empty sum, through the epilogue (C = beta * C + bias[col], or zeros).
@@ -1203,34 +1202,24 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUte
     }
 }
 
-// Lanes per row for a row of `bytes` bytes: the smallest power of two that covers its
-// 16-byte units, at most a warp.
-static int copy_lanes_per_row(int64_t bytes)
-{
-    const int64_t units = (bytes + 15) / 16;
-    int g = 1;
-    while (g < 32 && g < units) g *= 2;
-    return g;
-}
-
-cudaError_t launch_copy_rows(const RowCopy &m0, const RowCopy &m1, cudaStream_t stream)
+cudaError_t launch_copy_rows(const RowCopy &m0, const RowCopy &m1, cudaStream_t stream, int num_sms)
 {
     auto job = [](const RowCopy &m) {
-        CopyJob j{static_cast<const uint8_t *>(m.src), m.ld_src * m.esz, static_cast<uint8_t *>(m.dst),
-                  m.ld_dst * m.esz, m.src ? m.rows : 0, m.cols * m.esz, m.esz, copy_lanes_per_row(m.cols * m.esz), 0};
-        const int64_t rows_per_block = static_cast<int64_t>(kCopyWarps) * (32 / j.lanes_per_row);
-        j.blocks = (j.rows + rows_per_block - 1) / rows_per_block;
-        return j;
+        const int64_t bytes = m.cols * m.esz;
+        return CopyJob{static_cast<const uint8_t *>(m.src), m.ld_src * m.esz, static_cast<uint8_t *>(m.dst),
+                       m.ld_dst * m.esz, m.src ? m.rows : 0, bytes, m.esz, bytes / 16 + 1};
     };
     if ((m0.src && m0.esz != 2 && m0.esz != 4) || (m1.src && m1.esz != 2 && m1.esz != 4)) return cudaErrorInvalidValue;
     const CopyJob j0 = job(m0);
     const CopyJob j1 = job(m1);
-    const int64_t blocks = j0.blocks + j1.blocks;
-    if (blocks <= 0) return cudaSuccess;
-    if (blocks > 2147483647ll) return cudaErrorInvalidValue;
+    const int64_t total = j0.rows * j0.units_max + j1.rows * j1.units_max;
+    if (total <= 0) return cudaSuccess;
+    // enough threads for one unit each, up to 16 blocks of 256 per SM (the grid strides beyond)
+    const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 152) * 16;
+    const int64_t blocks = std::min<int64_t>((total + kCopyThreads - 1) / kCopyThreads, cap);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-    cfg.blockDim = dim3(kCopyWarps * 32);
+    cfg.blockDim = dim3(kCopyThreads);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1246,7 +1235,7 @@ cudaError_t launch_pack2(const void *src0, int64_t ld_src0, void *dst0, int64_t 
                          cudaStream_t stream)
 {
     return launch_copy_rows(RowCopy{src0, ld_src0, dst0, ld_dst0, rows0, cols0, 2},
-                            RowCopy{src1, ld_src1, dst1, ld_dst1, rows1, cols1, 2}, stream);
+                            RowCopy{src1, ld_src1, dst1, ld_dst1, rows1, cols1, 2}, stream, 0);
 }
 
 cudaError_t launch_fill_epilogue(const KernelParams &p, int num_sms, cudaStream_t stream)

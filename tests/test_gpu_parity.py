@@ -445,7 +445,8 @@ def test_unaligned_c_through_aligned_temporary(M, N, K, off, pad):
     assert np.all(np.isnan(body[:, N:]))
     assert within_tol(body[:, :N], oracle.gemm_f32(A, B), K)
     Ai, Bi = inputs.integer_pair(rng, M, N, K)
-    st = tct.gemm_f16_f32(dev16(Ai).data_ptr(), dev16(Bi).data_ptr(), c_base, M, N, K, K, N, ldc,
+    dAi, dBi = dev16(Ai), dev16(Bi)  # kept alive until the call has run
+    st = tct.gemm_f16_f32(dAi.data_ptr(), dBi.data_ptr(), c_base, M, N, K, K, N, ldc,
                           torch.cuda.current_stream().cuda_stream)
     assert st == tct.GEMM_OK
     torch.cuda.synchronize()
