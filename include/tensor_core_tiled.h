@@ -106,12 +106,6 @@ TCT_API gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t
  *               writes): the epilogue never loads C's blocks, so its waits for them run out
  *               the same way and no tile is stored.  Nothing faults, traps or hangs; later
  *               calls are unaffected.  Values above 3 are rejected.
- *   c_direct  : a C that TMA cannot write (base or row pitch not 16-byte aligned, or rows
- *               ending inside a 16-byte unit) of at most 64 MiB is by default produced in an
- *               aligned stream-ordered temporary by TMA stores and then copied into C (its
- *               current values copied in first when beta != 0); 1 = store such a C directly
- *               with the epilogue's per-lane stores, as is always done above 64 MiB.  The
- *               result is the same bit for bit.  0 or 1.
  */
 typedef struct gemm_options {
     int32_t group_m;
@@ -122,7 +116,6 @@ typedef struct gemm_options {
     int32_t cta_group;
     int32_t stream_k;
     int32_t fault_inject;
-    int32_t c_direct;
 } gemm_options;
 
 /* gemm_f16_f32 with explicit tuning options (opt may be NULL = all defaults). */

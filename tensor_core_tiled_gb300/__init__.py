@@ -51,7 +51,7 @@ class GemmError(RuntimeError):
 class GemmOptions(ctypes.Structure):
     _fields_ = [("group_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32), ("cta_group", ctypes.c_int32),
-                ("stream_k", ctypes.c_int32), ("fault_inject", ctypes.c_int32), ("c_direct", ctypes.c_int32)]
+                ("stream_k", ctypes.c_int32), ("fault_inject", ctypes.c_int32)]
 
 
 class GemmPlan(ctypes.Structure):
@@ -142,11 +142,10 @@ def version():
     return load().gemm_version().decode()
 
 
-def _options(group_m=0, tile_n=0, stages=0, max_ctas=0, timeout_ms=0, cta_group=0, stream_k=0, fault_inject=0,
-             c_direct=0):
+def _options(group_m=0, tile_n=0, stages=0, max_ctas=0, timeout_ms=0, cta_group=0, stream_k=0, fault_inject=0):
     o = GemmOptions()
     o.group_m, o.tile_n, o.stages, o.max_ctas, o.timeout_ms = group_m, tile_n, stages, max_ctas, timeout_ms
-    o.cta_group, o.stream_k, o.fault_inject, o.c_direct = cta_group, stream_k, fault_inject, c_direct
+    o.cta_group, o.stream_k, o.fault_inject = cta_group, stream_k, fault_inject
     return o
 
 

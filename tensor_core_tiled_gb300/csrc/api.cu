@@ -21,8 +21,6 @@ constexpr int kTileK = 64;
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 constexpr int kDefaultGroupM = 8;
 constexpr int kDefaultTimeoutMs = 2000;
-// Largest C (bytes) produced through an aligned temporary when TMA cannot write C itself.
-constexpr int64_t kCTempMaxBytes = int64_t{64} << 20;
 constexpr int kMaxDevices = 64;
 
 // Kernel variants the planner chooses between, with the relative per-tile throughput
@@ -167,7 +165,6 @@ gemm_status check_options(const gemm_options *opt)
 {
     if (!opt) return GEMM_OK;
     if (opt->fault_inject < 0 || opt->fault_inject > 3) return GEMM_ERR_INVALID_ARG;
-    if (opt->c_direct < 0 || opt->c_direct > 1) return GEMM_ERR_INVALID_ARG;
     if (opt->stream_k < 0 || opt->stream_k > 3) return GEMM_ERR_INVALID_ARG;
     if (opt->group_m < 0 || opt->group_m > 256) return GEMM_ERR_INVALID_ARG;
     if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return GEMM_ERR_INVALID_ARG;
@@ -583,16 +580,7 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
     // epilogue warps, and split tiles combine through workspace.
     const bool plain = !epi || (epi->alpha == 1.0f && epi->beta == 0.0f && !epi->bias);
     const bool c_tma = c_tma_ok(C, c_type, N, ldc);
-    // A C that TMA cannot write (rows not on 16-byte boundaries, or ending inside a 16-byte
-    // unit) and small enough to stay in L2 is produced in an aligned temporary that TMA writes,
-    // then copied into C by the row-copy kernel: the epilogue's per-lane stores of such rows
-    // cost more than that extra pass (1793^3: about 10 us of exposed stores on one wave).
-    const int esz_c = type_bytes(c_type);
-    const bool c_temp = !c_tma && !(opt && opt->c_direct) && M <= kCTempMaxBytes / (N * esz_c);
-    const int64_t ldt = c_temp ? round_up(N, 16 / esz_c) : 0;
-    const int64_t t_bytes = c_temp ? round_up(M * ldt * esz_c, 256) : 0;
-    const bool read_c = epi && epi->beta != 0.0f;
-    const bool reduce_ok = plain && c_type == GEMM_DTYPE_F32 && (c_tma || c_temp);
+    const bool reduce_ok = plain && c_type == GEMM_DTYPE_F32 && c_tma;
     gemm_plan pl;
     st = make_plan(M, N, K, lda, ldb, dev.sms, device_pair_slots(&dev), opt, A, B, &pl, true, layout, reduce_ok);
     if (st != GEMM_OK) return st;
@@ -611,14 +599,12 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
     const int64_t b_bytes = pl.pack_b ? round_up(b_rows * ldb_p * 2, 256) : 0;
     const int64_t w_bytes = reduce_ok ? 0 : split_parts_bytes(pl), f_bytes = split_flags_bytes(pl);
     void *ws = nullptr;
-    void *c_use = C;
-    int64_t ldc_use = ldc;
-    if (a_bytes + b_bytes + w_bytes + f_bytes + t_bytes > 0) {
+    if (a_bytes + b_bytes + w_bytes + f_bytes > 0) {
         cudaMemPool_t pool = nullptr;
         st = device_pool(&pool);
         if (st != GEMM_OK) return st;
-        if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes + w_bytes + f_bytes + t_bytes), pool,
-                                    s) != cudaSuccess)
+        if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes + w_bytes + f_bytes), pool, s) !=
+            cudaSuccess)
             return GEMM_ERR_CUDA;
         uint8_t *w = static_cast<uint8_t *>(ws);
         if (pl.pack_a) {
@@ -629,17 +615,9 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
             b_use = w + a_bytes;
             ldb_use = ldb_p;
         }
-        if (c_temp) {
-            c_use = w + a_bytes + b_bytes + w_bytes + f_bytes;
-            ldc_use = ldt;
-        }
-        // the operands' repack, and C's current values when the epilogue reads them
         cudaError_t e = tct::launch_copy_rows(
             tct::RowCopy{pl.pack_a ? A : nullptr, lda, w, lda_p, a_rows, a_cols, 2},
             tct::RowCopy{pl.pack_b ? B : nullptr, ldb, w + a_bytes, ldb_p, b_rows, b_cols, 2}, s, dev.sms);
-        if (e == cudaSuccess && c_temp && read_c)
-            e = tct::launch_copy_rows(tct::RowCopy{C, ldc, c_use, ldt, M, N, esz_c},
-                                      tct::RowCopy{nullptr, 0, nullptr, 0, 0, 0, esz_c}, s, dev.sms);
         if (e == cudaSuccess && f_bytes)  // the split tiles' flags start lowered
             e = cudaMemsetAsync(w + a_bytes + b_bytes + w_bytes, 0, static_cast<size_t>(f_bytes), s);
         if (e != cudaSuccess) {
@@ -657,15 +635,15 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
                              b_t(layout) ? static_cast<uint32_t>(pl.tile_n / pl.cta_group) : kTileK, is_bf16(layout));
     if (st == GEMM_OK) {
         const int tmo = opt && opt->timeout_ms ? opt->timeout_ms : kDefaultTimeoutMs;
-        tct::KernelParams p = make_params(pl, nullptr, M, N, K, ldc_use, tmo);
-        set_epilogue(p, c_use, c_type, ldc_use, epi);
+        tct::KernelParams p = make_params(pl, nullptr, M, N, K, ldc, tmo);
+        set_epilogue(p, C, c_type, ldc, epi);
         p.fault_inject = opt ? opt->fault_inject : 0;
         CUtensorMap tp, tc;
         std::memset(&tp, 0, sizeof(tp));
         std::memset(&tc, 0, sizeof(tc));
-        if (c_tma || c_temp) {
+        if (c_tma) {
             p.c_tma = 1;
-            st = encode_c_map(&tc, c_use, c_type, M, N, ldc_use);
+            st = encode_c_map(&tc, C, c_type, M, N, ldc);
         }
         if (pl.stream_k_tiles > 0 && st == GEMM_OK) {
             uint8_t *w = static_cast<uint8_t *>(ws) + a_bytes + b_bytes;
@@ -681,9 +659,6 @@ gemm_status run_gemm(int layout, const void *A, const void *B, void *C, int c_ty
         }
         if (st == GEMM_OK)
             st = to_status(tct::launch_gemm(ta, tb, tp, tc, p, layout, pl.cta_group, pl.tile_n, pl.stages, pl.grid, s));
-        if (st == GEMM_OK && c_temp)  // the product into C, element-aligned rows
-            st = to_status(tct::launch_copy_rows(tct::RowCopy{c_use, ldt, C, ldc, M, N, esz_c},
-                                                 tct::RowCopy{nullptr, 0, nullptr, 0, 0, 0, esz_c}, s, dev.sms));
     }
     if (ws) {
         if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;

@@ -143,10 +143,8 @@ def _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt, offset, ldc, **op
 def test_tma_and_lane_store_paths_agree(ct, alpha, beta, bt, opts):
     """The same problem with C where TMA can write it (16-byte aligned base and pitch, rows of
     whole 16-byte units: the tile goes out through swizzled staging and TMA stores, C read by
-    TMA when beta != 0), and one element off that alignment, written either through the
-    aligned temporary (TMA stores, then the row copy; C copied in first when beta != 0) or
-    directly by per-lane stores (c_direct): the same bits, since every path applies the same
-    operations; nothing outside the M x N block changes."""
+    TMA when beta != 0) and one element off that alignment (per-lane stores): the same bits,
+    since both paths apply the same operations; nothing outside the M x N block changes."""
     rng = np.random.default_rng(75)
     M, N, K = 333, 520, 200
     A, B = inputs.pair_ex(rng, M, N, K, dtype="f16")
@@ -154,10 +152,9 @@ def test_tma_and_lane_store_paths_agree(ct, alpha, beta, bt, opts):
     bias = _typed_random(rng, (N,), bt) if bt else None
     ldc = N + 8
     tma, rest_t = _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt or "f32", 0, ldc, **opts)
-    temp, rest_m = _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt or "f32", 1, ldc, **opts)
-    lane, rest_l = _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt or "f32", 1, ldc, c_direct=1, **opts)
-    assert np.all(rest_t == -1) and np.all(rest_m == -1) and np.all(rest_l == -1)
-    assert np.array_equal(tma, lane) and np.array_equal(tma, temp)
+    lane, rest_l = _gemm_ex_at(A, B, M, N, K, ct, alpha, beta, Cin, bias, bt or "f32", 1, ldc, **opts)
+    assert np.all(rest_t == -1) and np.all(rest_l == -1)
+    assert np.array_equal(tma, lane)
     want = run_ref(A, B, "f16", False, False, ct, alpha, beta, Cin, bias, bt or "f32")
     S = np.abs(oracle.gemm_ex_f32(A, B))
     got = tma if ct == "f32" else tma.view(np.uint16)
@@ -246,9 +243,9 @@ def test_torch_helper():
 
 @pytest.mark.parametrize("ct", ["f32", "f16", "bf16"])
 def test_beta_with_unaligned_c(ct):
-    """beta != 0 on a C that TMA cannot write: C's current values are copied into the aligned
-    temporary before the product, the epilogue reads them there, and the result is copied
-    back; gap columns and the elements around C keep their bits."""
+    """beta != 0 on a C that TMA cannot write (one element off a 16-byte boundary, a row pitch
+    that is not a 16-byte multiple): the per-lane epilogue reads C's current values and stores
+    the result; gap columns and the elements around C keep their bits."""
     rng = np.random.default_rng(77)
     M, N, K, pad = 301, 203, 160, 3
     A, B = inputs.pair_ex(rng, M, N, K, dtype="f16")
