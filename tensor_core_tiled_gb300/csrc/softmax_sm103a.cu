@@ -18,8 +18,9 @@
 //     rescales its slice by exp(max_slice - max_row) / sum_row.
 // The team kernels launch as programmatic dependent launches: their barrier set-up may
 // overlap the previous kernel on the stream, and X and Y are touched only after waiting for it.
-// Other layouts (and rows beyond 16 slices of 96 KB) take the plain kernels below: a warp per
-// row held in registers, a CTA per row staged in shared memory, or two passes over the row.
+// Rows whose 16 slices each exceed the 112 KB ring are streamed twice by the same cluster
+// kernel.  Other layouts take the plain kernels below: a warp per row held in registers, a
+// CTA per row staged in shared memory, or two passes over the row.
 // exp(-inf) = 0; a row holding a NaN, whose maximum is +inf, or that is all -inf has no
 // finite softmax and is written as NaN.
 #include <cuda_runtime.h>
@@ -242,7 +243,10 @@ constexpr int kStagedThreads = kComputeThreads + 32;  // + one producer warp
 constexpr int kMaxRing = 32;                          // ring slots (one mbarrier pair each)
 constexpr uint32_t kRingBytes = 32 * 1024;            // staging ring per CTA (at least two slots)
 constexpr uint32_t kMaxSmemBytes = 200 * 1024;        // dynamic shared memory opt-in of the staged kernels
-constexpr uint32_t kLongRingBytes = 96 * 1024;        // ring of the long-slice cluster kernel
+// Ring of the long-slice cluster kernel: 7 slots, so that a slice of up to 5 slots leaves 2
+// for the next row's first chunks (measured on GB300 against 6 slots: 131072-column rows
+// 0.75 -> 0.78 of the copy bandwidth, 262144 columns 0.62 -> 0.64; two CTAs still fit per SM).
+constexpr uint32_t kLongRingBytes = 112 * 1024;
 constexpr int kCtasPerSm = 2;
 constexpr uint32_t kHeaderBytes = 1024;               // barriers and reduction scratch
 constexpr uint32_t kChunkBytes = 16 * 1024;           // slot size of the CTA kernel for long slices
@@ -898,7 +902,7 @@ cudaError_t launch_softmax_rows(const float *X, float *Y, int64_t M, int64_t N, 
 
     // A cluster per row: up to kTeamClusterMax CTAs holding slices of at most kTeamMaxCols
     // columns in registers; longer rows in slices of about kLongSliceCols columns staged in
-    // shared memory (at most 5 of the 6 ring slots, so the next row's first slot streams in
+    // shared memory (at most 5 of the 7 ring slots, so the next row's first slots stream in
     // meanwhile), at most kMaxCluster CTAs.  Measured on GB300: clusters of 7 CTAs stream
     // markedly slower than clusters of 8, so 7 becomes 8.
     const bool team = N <= static_cast<int64_t>(kTeamClusterMax) * kTeamMaxCols;
@@ -919,7 +923,7 @@ cudaError_t launch_softmax_rows(const float *X, float *Y, int64_t M, int64_t N, 
     } else {
         kernel = kClusterLong;
         p.slot_bytes = kChunkBytes;
-        p.ring = static_cast<int32_t>(kLongRingBytes / kChunkBytes);  // a slice up to 96 KB is read once
+        p.ring = static_cast<int32_t>(kLongRingBytes / kChunkBytes);  // a slice up to 112 KB is read once
         p.tiles = M;
         smem = kHeaderBytes + static_cast<size_t>(p.ring) * p.slot_bytes;
     }

@@ -3,7 +3,7 @@
 The workload is the one of "06_triton_style.py" demo 3: N(0,1) rows, softmax along each
 row.  Rows whose base and leading dimension are multiples of 16 bytes take the staged
 kernels (a team of threads per row up to 8192 columns, a cluster of CTAs per row beyond,
-reading long slices twice past 16 x 24576 columns); other rows take the plain kernels
+reading long slices twice past 16 x 28672 columns); other rows take the plain kernels
 (a warp per row up to 2048 columns, a CTA per row in shared memory up to 51200, two passes
 beyond).  Shapes sit on each boundary, with ragged lengths, padded and unaligned rows,
 in-place use, special values and empty shapes.
@@ -82,14 +82,15 @@ def _run(x, inplace=False):
 # holds a row in registers (several rows staged per ring slot); up to 8 * 8192 columns a
 # cluster of ceil(N / 8192) CTAs splits each row the same way; beyond, a cluster of
 # ceil(N / 20480) CTAs (7 taken as 8, at most 16) stages each slice in 16 KB shared-memory
-# slots, and reads it twice when it exceeds the 6-slot ring (past 16 * 24576 columns).
+# slots, and reads it twice when it exceeds the 7-slot ring (past 16 * 28672 columns).
 # The tall shapes wrap every CTA's slot ring several times.
 SHAPES = [(1, 1, 10), (7, 1, 11), (33, 5, 12), (300, 37, 13), (129, 128, 14), (64, 129, 15), (257, 256, 16),
           (100, 511, 17), (65, 1000, 18), (40, 1024, 19), (80000, 100, 40), (31, 1025, 20), (17, 2048, 21),
           (9, 2049, 22), (20, 3000, 23), (5, 4096, 24), (5, 4097, 25), (3, 8192, 26), (8000, 2000, 41),
           (3, 8193, 27), (2, 51200, 28), (2, 51201, 29), (1000, 30000, 42), (2, 65536, 45), (2, 65537, 46), (2, 131072, 43),
           (2, 131073, 44), (2, 143360, 47), (3, 163841, 48), (2, 327680, 49), (2, 327681, 50),
-          (2, 200003, 30), (2, 393216, 31), (2, 393217, 32), (3, 1 << 20, 33), (2, 1000003, 34)]
+          (2, 200003, 30), (2, 393216, 31), (2, 393217, 32), (2, 458752, 35), (2, 458753, 36), (3, 1 << 20, 33),
+          (2, 1000003, 34)]
 
 
 @pytest.mark.parametrize("M,N,seed", SHAPES)
