@@ -454,6 +454,7 @@ tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t 
     p.fault_inject = 0;
     p.split_mode = pl.split_form == 2 ? 2 : 0;
     p.sk_units = pl.split_form == 2 ? pl.sk_units : 0;
+    p.b_stream = p.num_m == 1 ? 1 : 0;
     p.c_tma = 0;
     return p;
 }

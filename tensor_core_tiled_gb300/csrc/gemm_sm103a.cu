@@ -384,13 +384,17 @@ __device__ __forceinline__ uint32_t pack_16bit(float a, float b, int type)
 // out.  Returns false if a C load did not arrive in time (after recording the timeout);
 // else once the copies have read shared memory, and with kOwnBlocks once they have completed.
 // `release` is called by lane 0 once every column has been read from TMEM.
-template <int BN, bool kReduce, bool kOwnBlocks, bool kWide, typename Release>
+// With kStageOnly (kOwnBlocks, FP32, no epilogue inputs) the blocks are only staged: nothing
+// is issued, and issue_staged_blocks sends them later (a stream-K piece stages its
+// accumulator while it waits for the next piece to reach C).
+template <int BN, bool kReduce, bool kOwnBlocks, bool kWide, typename Release, bool kStageOnly = false>
 __device__ __forceinline__ bool bulk_accumulator(uint32_t t_row, const void *tmap_c, int64_t row0, int64_t col0,
                                                  const TileDst &d, const float *sbias, float *stage, int lane,
                                                  uint32_t cbar, uint32_t &cphase, uint64_t limit,
                                                  volatile int *abort_flag, bool skip_c_load, Release release)
 {
     static_assert(!(kReduce && kWide), "reduce-add of FP32 only");
+    static_assert(!kStageOnly || (kOwnBlocks && !kWide), "staging alone needs a block per 32 FP32 columns");
     constexpr int kCols = kWide ? 64 : 32;  // columns per staged block (128-byte rows)
     constexpr int kChunk = kWide ? 8 : 4;   // columns per 16-byte unit
     constexpr int kUnits = 32 / kChunk;     // 16-byte units per 32 accumulator columns
@@ -480,6 +484,7 @@ __device__ __forceinline__ bool bulk_accumulator(uint32_t t_row, const void *tma
             srow[j ^ (lane & 7)] = out;
         }
         if (kWide && half == 0) continue;  // the block's second half is still to come
+        if constexpr (kStageOnly) continue;
         fence_proxy_async_smem();          // this lane's generic writes before the async-proxy read
         __syncwarp();
         if (lane == 0 && block_in(blk)) {
@@ -490,6 +495,11 @@ __device__ __forceinline__ bool bulk_accumulator(uint32_t t_row, const void *tma
             bulk_commit_group();
         }
     }
+    if constexpr (kStageOnly) {
+        fence_proxy_async_smem();  // every block's generic writes before the later async-proxy reads
+        __syncwarp();
+        return ok;
+    }
     if (lane == 0) {
         if constexpr (kOwnBlocks)
             bulk_wait_all();
@@ -498,6 +508,27 @@ __device__ __forceinline__ bool bulk_accumulator(uint32_t t_row, const void *tma
     }
     __syncwarp();
     return ok;
+}
+
+// The blocks bulk_accumulator<..., kStageOnly> staged (FP32, one 4 KB block per 32 columns),
+// added into C by TMA reduce-add back to back; returns once the writes have completed.
+template <int BN>
+__device__ __forceinline__ void issue_staged_blocks(const void *tmap_c, int64_t row0, int64_t col0, const TileDst &d,
+                                                    const float *stage, int lane)
+{
+    if (lane == 0) {
+        if (row0 < d.rows) {
+            for (int blk = 0; blk < BN / 32; ++blk) {
+                const int64_t c0 = col0 + blk * 32;
+                if (c0 < d.cols)
+                    tma_reduce_add_2d(tmap_c, static_cast<int32_t>(c0), static_cast<int32_t>(row0),
+                                      smem_u32(stage + blk * 32 * 32));
+            }
+        }
+        bulk_commit_group();
+        bulk_wait_all();
+    }
+    __syncwarp();
 }
 
 // Waits until *flag is raised (by another CTA), bounded like the pipeline waits.
@@ -604,6 +635,8 @@ __global__ void __launch_bounds__(192, 1)
             for (int i = 0; i < STAGES; ++i) issued[i] = false, issued_parity[i] = 0;
             bool ok = true;
             WorkItem w;
+            const bool b_first_out = !kPair && p.b_stream != 0;  // B read by one tile only
+            const uint64_t b_policy = l2_policy_evict_first();
             for (int idx = 0; ok && work_item(p, unit, idx, w); ++idx) {
                 const TileCoord c = tile_coord(w.tile, p.num_m, p.num_n, p.group_m);
                 const int32_t m0 = c.m * (Cf::BM * CG) + static_cast<int32_t>(rank) * Cf::BM;
@@ -643,10 +676,11 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int j = 0; j < Cf::B_BOXES; ++j) {
                         const uint32_t dst = smem_u32(sB + s * Cf::B_STAGE + j * Cf::B_SUB);
-                        if constexpr (BT)
-                            load(dst, &tmB, k0, n0);
+                        const int32_t bc0 = BT ? k0 : n0 + 64 * j, bc1 = BT ? n0 : k0;
+                        if (b_first_out)
+                            tma_load_2d_hint(dst, &tmB, bc0, bc1, fb, b_policy);
                         else
-                            load(dst, &tmB, n0 + 64 * j, k0);
+                            load(dst, &tmB, bc0, bc1);
                     }
                     issued[s] = true;
                     issued_parity[s] = ph;
@@ -845,14 +879,28 @@ __global__ void __launch_bounds__(192, 1)
                 // inside the tile waits for the next unit's piece, then adds itself; the piece
                 // that reaches the tile's end is the first and is stored.
                 const bool add = w.kb1 < p.num_kb;
-                if (add) {
-                    ok = wait_flag(p.flags + (unit + 1) * CG + rank, limit, abort_flag);
+                if (add && own_blocks) {
+                    // The unit's last item (a piece that ends inside its tile always is): stage
+                    // the whole accumulator in the idle stage buffers while the next piece is on
+                    // its way, then add it into C in one burst once the flag is seen.
+                    ok = bulk_accumulator<BN, true, true, false, decltype(release), true>(
+                        t_row0, &tmC, row_base, col_base, d, sbias, blocks, lane, cb, cphase, limit, abort_flag, skip_c,
+                        release);
+                    ok = ok && wait_flag(p.flags + (unit + 1) * CG + rank, limit, abort_flag);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     fence_proxy_async_all();  // the flag seen before the reduce reads C
+                    issue_staged_blocks<BN>(&tmC, row_base, col_base, d, blocks, lane);
+                } else {
+                    if (add) {
+                        ok = wait_flag(p.flags + (unit + 1) * CG + rank, limit, abort_flag);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        fence_proxy_async_all();  // the flag seen before the reduce reads C
+                    }
+                    ok = add ? bulk(std::true_type{}, std::false_type{}) : bulk(std::false_type{}, std::false_type{});
+                    if (!ok) break;
                 }
-                ok = add ? bulk(std::true_type{}, std::false_type{}) : bulk(std::false_type{}, std::false_type{});
-                if (!ok) break;
                 if (w.kb0 > 0) {
                     // A unit's only piece that starts inside a tile (its first): publish it to
                     // the previous unit once all four warps' rows are in C.
