@@ -39,6 +39,7 @@ struct Candidate {
 constexpr double kSmFlops = 8192.0 * 1.9e9;
 constexpr double kHbmBytesPerSec = 6.5e12;
 constexpr double kL2BytesPerSec = 20e12;
+constexpr double kL2Bytes = 128.0 * 1024 * 1024;  // about the L2 capacity
 // Measured on GB300: the second half's write, its transfer to the owner and the owner's
 // store are serial after the halves finish, about two tile epilogues plus a flag handoff.
 constexpr double kFixupSec = 12e-6;       // split tile combined through workspace (measured)
@@ -230,6 +231,8 @@ struct Split {
     double compute;  // the compute part of `time` (tile time x effective waves)
     int form;        // 0 whole tiles, 1 two-part split tail, 2 stream-K
     int64_t sk_units;
+    bool mem_bound;  // the memory term sets `time`
+    double l2_bytes; // operand bytes the tiles' TMA loads move from L2 into shared memory
 };
 
 // Work split and modelled time of one variant.  Whole waves of tiles go data-parallel; the
@@ -264,6 +267,8 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
     sp.time = t_dp;
     sp.eff_waves = static_cast<double>(waves);
     sp.compute = waves * tile_sec;
+    sp.mem_bound = t_dp > waves * tile_sec;
+    sp.l2_bytes = 2.0 * static_cast<double>(tiles) * (tile_m + tile_n) * static_cast<double>(kb * kTileK);
     const int64_t full = tiles / units, rest = tiles - full * units;
     const int64_t helpers = units - rest;
     const int64_t p = helpers > 0 ? tct::ceil_div(rest, helpers) : 0;
@@ -292,6 +297,7 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
             sp.eff_waves = ew;
             sp.compute = ew * tile_sec;
             sp.form = 1;
+            sp.mem_bound = t_tail_mem > ew * tile_sec;
         }
     }
     // Stream-K ("02_gpu_execution_model.py" part 5: rather than leave a partial wave's SMs
@@ -336,6 +342,7 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
                     best.compute = ew * tile_sec;
                     best.form = 2;
                     best.sk_units = sku;
+                    best.mem_bound = t_mem > ew * tile_sec;
                 }
             }
         }
@@ -374,9 +381,18 @@ gemm_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
         // Within 1% (e.g. every candidate bound by the same HBM time) the one with less compute
         // time wins: it has the most slack (measured: 1-CTA 128x128 tiles stream the skinny
         // 128 x 16384 x 16384 shape 5% faster than CTA-pair 256x256 tiles, half of whose rows
-        // are empty).
+        // are empty).  Between two bandwidth-bound plans within 5%, the one whose tiles move
+        // fewer operand bytes from L2 into shared memory wins first (measured at 128 x 16384 x
+        // 16384: 1-CTA 128x256 tiles, each split in two k-halves, 4-5% faster than whole
+        // 128x128 tiles, which re-read A twice as often); only for operands larger than L2,
+        // which stream from HBM.
         const bool tie = best && sp.time <= best_sp.time * 1.01 && best_sp.time <= sp.time * 1.01;
-        if (!best || (tie ? sp.compute < best_sp.compute : sp.time < best_sp.time)) {
+        const bool streaming = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N) > kL2Bytes;
+        const bool mem_tie = best && streaming && sp.mem_bound && best_sp.mem_bound && sp.time <= best_sp.time * 1.05 &&
+                             best_sp.time <= sp.time * 1.05 &&
+                             (sp.l2_bytes < best_sp.l2_bytes * 0.9 || best_sp.l2_bytes < sp.l2_bytes * 0.9);
+        if (!best || (mem_tie ? sp.l2_bytes < best_sp.l2_bytes
+                              : (tie ? sp.compute < best_sp.compute : sp.time < best_sp.time))) {
             best = &c;
             best_sp = sp;
         }
