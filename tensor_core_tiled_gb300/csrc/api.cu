@@ -55,7 +55,9 @@ constexpr int64_t kMinSplitIters = 4;
 constexpr double kLinkFixedSec = 1.5e-6;
 constexpr double kLinkBytesPerSecPerSm = 33e9;
 // Pieces one tile may be cut into (bounds the chain's length); the planner tries each cap.
-constexpr int64_t kStreamKPieceCaps[] = {2, 3, 4, 6};
+// Cap 1 asks for ranges of at least a tile less one k-block, so that no tile has more than two
+// pieces: those add into C in either order with no chain (split_mode 3).
+constexpr int64_t kStreamKPieceCaps[] = {1, 2, 3, 4, 6};
 
 constexpr Candidate kCandidates[] = {
     {2, 256, 6, 1.00},
@@ -318,16 +320,19 @@ Split model_split(int64_t M, int64_t N, int64_t K, int cg, int tile_n, int stage
             if (skt <= 0) continue;
             const int64_t iters = skt * kb;
             for (const int64_t cap : kStreamKPieceCaps) {
-                const int64_t qmin = std::max<int64_t>(want_sk == 3 ? 1 : kMinSplitIters, tct::ceil_div(kb, cap));
+                const int64_t qmin = std::max<int64_t>(want_sk == 3 ? 1 : kMinSplitIters,
+                                                       cap == 1 ? kb - 1 : tct::ceil_div(kb, cap));
                 const int64_t sku = std::min<int64_t>(units, iters / qmin);
-                if (sku < 2 || (want_sk != 3 && sku <= skt)) continue;  // no finer than whole tiles
+                if (sku < 2 || (want_sk != 3 && iters % (sku * kb) == 0)) continue;  // whole tiles only
                 const int64_t q = iters / sku, qmax = tct::ceil_div(iters, sku);
                 const int64_t pieces = std::min<int64_t>(tct::ceil_div(kb - 1, q) + 1, sku);
                 const double ew = dpw + static_cast<double>(qmax) / kb;
                 const double busy_sk = static_cast<double>(sku) / units;
                 const double t_mem = (dpw > 0 ? bytes * dpw * units / tiles / kHbmBytesPerSec : 0.0) +
                                      bytes * skt / tiles / (kHbmBytesPerSec * hbm_share(busy_sk));
-                const double t = std::max(ew * tile_sec, t_mem) + (pieces - 1) * link_sec;
+                // at most two pieces per tile: one reduce-add pass, no chain
+                const double comb = pieces <= 2 ? fixup_sec : (pieces - 1) * link_sec;
+                const double t = std::max(ew * tile_sec, t_mem) + comb;
                 if (!found || t < best.time) {
                     found = true;
                     best = sp;
@@ -468,7 +473,8 @@ tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t 
     p.workspace = nullptr;
     p.flags = nullptr;
     p.fault_inject = 0;
-    p.split_mode = pl.split_form == 2 ? 2 : 0;
+    // stream-K: tiles of at most two pieces add in either order; longer ones chain
+    p.split_mode = pl.split_form == 2 ? (pl.split_parts_per_unit <= 2 ? 3 : 2) : 0;
     p.sk_units = pl.split_form == 2 ? pl.sk_units : 0;
     p.b_stream = p.num_m == 1 ? 1 : 0;
     p.c_tma = 0;
@@ -486,7 +492,8 @@ int64_t split_parts_bytes(const gemm_plan &pl)
 int64_t split_flags_bytes(const gemm_plan &pl)
 {
     if (pl.stream_k_tiles <= 0) return 0;
-    if (pl.split_form == 2) return round_up(static_cast<int64_t>(pl.sk_units) * pl.cta_group * 4, 256);
+    if (pl.split_form == 2)  // a flag per unit (chains) or per stream-K tile (pairs)
+        return round_up(std::max<int64_t>(pl.sk_units, pl.stream_k_tiles) * pl.cta_group * 4, 256);
     return round_up(static_cast<int64_t>(pl.stream_k_tiles) * pl.cta_group * 4, 256);
 }
 

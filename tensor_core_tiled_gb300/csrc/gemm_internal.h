@@ -63,6 +63,11 @@ struct KernelParams {
     // rank]) and adds itself by TMA reduce-add; a piece that starts inside the tile raises
     // flag[u * cta_group + rank] once its rows are in C.  C = ((p_last + ...) + p_1) + p_0,
     // the same bits on every run.
+    // split_mode 3: the same ranges when every range is at least a tile long less one k-block,
+    // so that no tile has more than two pieces: the piece that starts the tile zeroes its
+    // rows of C at kernel start and raises flag[(tile - dp_tiles) * cta_group + rank]; both
+    // pieces add into C by TMA reduce-add once they see it, in either order, since
+    // (0 + a) + b = (0 + b) + a.
     int32_t sk_units;
     // 1 when every B element is read by one tile only (a single row of tiles, num_m == 1):
     // B's TMA loads then mark their L2 lines evict-first, so that the stream of B does not
@@ -75,7 +80,7 @@ enum WorkMode : int32_t {
     WORK_STORE = 0,    // store the accumulator to C
     WORK_FIXUP = 1,    // add the part in workspace slot `part`, then store to C
     WORK_PARTIAL = 2,  // store the accumulator to workspace slot `part`, raise its flag
-    WORK_CHAIN = 3,    // stream-K piece of a tile (split_mode 2); `part` is the unit
+    WORK_CHAIN = 3,    // stream-K piece of a tile (split_mode 2 or 3); `part` is the unit
 };
 
 // One piece of work of a unit: k-blocks [kb0, kb1) of linear tile `tile`.
@@ -102,7 +107,7 @@ inline bool work_item(const KernelParams &p, int32_t u, int32_t idx, WorkItem &i
         it.mode = WORK_STORE;
         return true;
     }
-    if (p.split_mode == 2) {
+    if (p.split_mode == 2 || p.split_mode == 3) {
         // Stream-K: the idx - waves-th tile piece of this unit's range [a, b) of iterations.
         if (u >= p.sk_units || p.split_tiles <= 0) return false;
         const int64_t iters = static_cast<int64_t>(p.split_tiles) * p.num_kb;

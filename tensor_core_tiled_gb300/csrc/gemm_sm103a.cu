@@ -788,14 +788,17 @@ __global__ void __launch_bounds__(192, 1)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         float *stage = sEpi + (warp - 2) * 32 * 32;
         float *sbias = sBias + (warp - 2) * BN;  // the current tile's bias columns (TMA path)
-        if (p.split_mode == 1 && !(p.fault_inject & 1)) {
-            // The owner of a split tile zeroes its rows of the tile in C while the first tile's
-            // k-loop runs, then raises the tile's flag for this CTA rank; both halves add into
-            // C once they see it.  (A unit owns at most one split tile.)  Fault injection skips
-            // this, so that both halves' waits run out and C keeps its old contents there.
+        if ((p.split_mode == 1 || p.split_mode == 3) && !(p.fault_inject & 1)) {
+            // The owner of a split tile (the piece that starts it) zeroes its rows of the tile
+            // in C while the first tile's k-loop runs, then raises the tile's flag for this CTA
+            // rank; both pieces add into C once they see it.  (A unit owns at most one split
+            // tile.)  Fault injection skips this, so that both pieces' waits run out and C keeps
+            // its old contents there.
             WorkItem z;
             for (int i = 0; work_item(p, unit, i, z); ++i) {
-                if (z.mode != WORK_FIXUP) continue;
+                const bool owned = p.split_mode == 1 ? z.mode == WORK_FIXUP : (z.mode == WORK_CHAIN && z.kb0 == 0);
+                if (!owned) continue;
+                const int32_t slot = p.split_mode == 1 ? z.part : z.tile - p.dp_tiles;
                 const TileCoord c = tile_coord(z.tile, p.num_m, p.num_n, p.group_m);
                 const int64_t r0 = static_cast<int64_t>(c.m) * (Cf::BM * CG) + rank * Cf::BM + q * 32;
                 const int64_t c0 = static_cast<int64_t>(c.n) * BN;
@@ -816,7 +819,7 @@ __global__ void __launch_bounds__(192, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(part_bar);
                 if (warp == 2 && lane == 0 && wait_or_abort<false>(part_bar, 0u, limit, abort_flag, SITE_EPI_PARTS))
-                    flag_release_gpu(p.flags + z.part * CG + rank, 1u);
+                    flag_release_gpu(p.flags + slot * CG + rank, 1u);
                 break;
             }
         }
@@ -874,6 +877,16 @@ __global__ void __launch_bounds__(192, 1)
                                                                                stage, lane, cb, cphase, limit, abort_flag,
                                                                                skip_c, release);
             };
+            if (w.mode == WORK_CHAIN && p.split_mode == 3) {
+                // Stream-K piece of a tile cut in at most two: add into C, zeroed by the tile's
+                // first piece, whichever piece comes first.
+                ok = wait_flag(p.flags + (w.tile - p.dp_tiles) * CG + rank, limit, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                fence_proxy_async_all();  // the owner's zeros (generic writes) before the reduce
+                if (!bulk(std::true_type{}, std::false_type{})) break;
+                continue;
+            }
             if (w.mode == WORK_CHAIN) {
                 // Stream-K piece: the tile's pieces reach C last-first.  A piece that ends
                 // inside the tile waits for the next unit's piece, then adds itself; the piece
@@ -1146,7 +1159,7 @@ static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, 
     // split tiles combined through workspace or reduce-add need room for a part in the stage
     // buffers; stream-K pieces (split_mode 2) need none
     if (p.split_tiles > 0 && p.split_mode != 2 && !Cfg<CG, BN, STAGES>::SPLIT_OK) return cudaErrorInvalidValue;
-    if (p.split_mode == 2 && !p.c_tma) return cudaErrorInvalidValue;
+    if ((p.split_mode == 2 || p.split_mode == 3) && !p.c_tma) return cudaErrorInvalidValue;
     e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tp, tc, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
