@@ -355,3 +355,10 @@ def test_stream_k_needs_the_reduce_add_path(tct_lib):
     assert tct.gemm_f16_f32_plan(2048, 2048, 2048, num_sms=sms, stream_k=3)["split_form"] == 2
     with pytest.raises(tct.GemmError):
         tct.gemm_f16_f32_plan(2048, 2046, 2048, num_sms=sms, stream_k=3)
+
+
+def test_stream_k_plans_cover_both_combinations(tct_lib):
+    """The stream-K plans above include tiles of at most two pieces (added into C in either
+    order) and longer chains (added in a fixed order), so both combinations are exercised."""
+    pieces = {tct.gemm_f16_f32_plan(*shape, num_sms=152, **opts)["split_parts_per_unit"] for shape, opts in STREAM_K_PLANS}
+    assert min(pieces) <= 2 < max(pieces)

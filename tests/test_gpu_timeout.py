@@ -99,16 +99,19 @@ def test_missing_c_load_times_out_and_context_survives(c_dtype):
     assert np.all(np.abs(got - want) <= tol)
 
 
-def test_unpublished_stream_k_piece_times_out_and_context_survives():
-    """Stream-K with fault_inject bit 0: a piece that starts inside a tile never raises its
-    flag, so the unit before it, whose piece of that tile waits to add into C, runs out of
-    time.  The status is read on the host, the tiles computed whole are correct, and the next
-    call on the same context is correct everywhere."""
-    M, N, K = 4096, 4096, 1024
+@pytest.mark.parametrize("M,N,K,chained", [(4096, 4096, 1024, False), (1024, 1024, 16384, True)])
+def test_unpublished_stream_k_piece_times_out_and_context_survives(M, N, K, chained):
+    """Stream-K with fault_inject bit 0.  Tiles of two pieces: the piece that starts a tile
+    never zeroes and flags its rows of C, so both pieces' waits run out.  Longer chains: a
+    piece that starts inside a tile never raises its flag, so the unit before it, whose piece
+    of that tile waits to add into C, runs out of time.  The status is read on the host, the
+    tiles computed whole are correct, and the next call on the same context is correct
+    everywhere."""
     opts = dict(stream_k=3)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     plan = tct.gemm_f16_f32_plan(M, N, K, num_sms=sms, **opts)
-    assert plan["split_form"] == 2 and 0 < plan["stream_k_tiles"] < plan["tiles"]
+    assert plan["split_form"] == 2 and 0 < plan["stream_k_tiles"] <= plan["tiles"]
+    assert (plan["split_parts_per_unit"] > 2) == chained
     rng = np.random.default_rng(57)
     A, B = inputs.normal_pair(rng, M, N, K)
     dA, dB = _dev16(A), _dev16(B)
@@ -123,6 +126,9 @@ def test_unpublished_stream_k_piece_times_out_and_context_survives():
     R = oracle.gemm_f32(A, B)
     tm, tn = plan["tile_m"], plan["tile_n"]
     num_m, num_n = -(-M // tm), -(-N // tn)
+    # the whole tiles every unit computes before its stream-K range (a unit whose wait ran out
+    # stops there, so whole tiles inside the stream-K region may be left unwritten)
+    dp_tiles = plan["tiles"] - plan["stream_k_tiles"]
     whole = []
     for u in range(plan["units"]):
         idx = 0
@@ -130,10 +136,9 @@ def test_unpublished_stream_k_piece_times_out_and_context_survives():
             it = tct.gemm_f16_f32_work_item(M, N, K, sms, u, idx, **opts)
             if it is None:
                 break
-            if it["mode"] == tct.WORK_STORE:
+            if it["mode"] == tct.WORK_STORE and it["tile"] < dp_tiles:
                 whole.append(it["tile"])
             idx += 1
-    assert whole
     for t in whole:
         r, c = tct.gemm_tile_coord(t, num_m, num_n, plan["group_m"])
         blk = (slice(r * tm, min(M, (r + 1) * tm)), slice(c * tn, min(N, (c + 1) * tn)))
