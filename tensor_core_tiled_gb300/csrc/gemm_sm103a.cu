@@ -77,6 +77,10 @@ struct Cfg {
     // A split tile's part (32 rows x BN FP32 per epilogue warp) is loaded into the stage
     // buffers, which are idle by then; only variants with room for it split tiles.
     static constexpr bool SPLIT_OK = STAGES * (A_STAGE + B_STAGE) >= EPI_WARPS * 32 * BN * 4;
+    // The last tile of a unit, for a C that TMA cannot write, is staged as whole rows (32 per
+    // epilogue warp, BN + 4 floats apart) in the idle stage buffers.
+    static constexpr int ROW_PITCH = BN + 4;
+    static constexpr bool ROWS_OK = STAGES * (A_STAGE + B_STAGE) >= EPI_WARPS * 32 * ROW_PITCH * 4;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM_BYTES =
         1024 + STAGES * (A_STAGE + B_STAGE) + EPI_BYTES + BIAS_BYTES + NUM_BARS * 8 + 16;
@@ -358,6 +362,53 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const TileDst 
         }
         __syncwarp();
     }
+}
+
+// One accumulator buffer to an FP32 C whose rows TMA cannot address (a row pitch or base
+// off the 16-byte grid), plain epilogue: lane l's row of the tile goes whole into
+// rows + l * PITCH, shifted by the row's offset from the 16-byte grid in C, so that its
+// elements sit at the same address modulo 16 in shared and global memory.  The row's body
+// between its first and last 16-byte boundaries in C then goes out as one bulk copy
+// (cp.async.bulk, issued by the lane), the at most three elements on either side by plain
+// stores.  `rows` is 16-byte aligned with room for 32 x PITCH floats.  Returns once the
+// copies have completed.  `release` is called by lane 0 once every column has been read
+// from TMEM.
+template <int BN, int PITCH, typename Release>
+__device__ __forceinline__ void store_rows_bulk(uint32_t t_row, const TileDst &d, int64_t row_base, int64_t col_base,
+                                                float *rows, int lane, Release release)
+{
+    static_assert(PITCH % 4 == 0 && PITCH >= BN + 3, "rows of whole 16-byte units with room for the shift");
+    const int64_t grow = row_base + lane;
+    const bool row_in = grow < d.rows;
+    float *gdst = static_cast<float *>(d.base) + (row_in ? grow : 0) * d.ld + col_base;
+    const int shift = static_cast<int>((reinterpret_cast<uintptr_t>(gdst) >> 2) & 3u);
+    float *srow = rows + lane * PITCH + shift;
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + ch * 32, r);
+        tmem_wait_ld();
+        if (ch == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release();
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) srow[ch * 32 + j] = __uint_as_float(r[j]);
+    }
+    const int64_t ncols = d.cols - col_base < BN ? d.cols - col_base : BN;
+    if (row_in && ncols > 0) {
+        const int64_t head = ((4 - shift) & 3) < ncols ? ((4 - shift) & 3) : ncols;
+        const int64_t body = (ncols - head) & ~int64_t(3);
+        if (body > 0) {
+            fence_proxy_async_smem();  // this lane's generic writes before the async-proxy read
+            bulk_store(gdst + head, smem_u32(srow + head), static_cast<uint32_t>(body * 4));
+            bulk_commit_group();
+        }
+        for (int64_t c = 0; c < head; ++c) __stcs(gdst + c, srow[c]);
+        for (int64_t c = head + body; c < ncols; ++c) __stcs(gdst + c, srow[c]);
+        if (body > 0) bulk_wait_all();
+    }
+    __syncwarp();
 }
 
 // Two floats rounded to the 16-bit type (FP16 0, BF16 1) and packed, the first in the low half.
@@ -972,6 +1023,21 @@ __global__ void __launch_bounds__(192, 1)
             }
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(b * BN);
+            if constexpr (Cf::ROWS_OK) {
+                if (own_blocks && w.mode == WORK_STORE && !p.c_tma && !d.epi && d.out_type == 2) {
+                    float *rows = reinterpret_cast<float *>(sA) + (warp - 2) * 32 * Cf::ROW_PITCH;
+                    if constexpr (kPair) {
+                        const uint32_t te = map_to_cta(tempty_bar(b), 0);
+                        store_rows_bulk<BN, Cf::ROW_PITCH>(t_row, d, row_base, col_base, rows, lane,
+                                                           [&] { mbar_arrive_cluster(te); });
+                    } else {
+                        const uint32_t te = tempty_bar(b);
+                        store_rows_bulk<BN, Cf::ROW_PITCH>(t_row, d, row_base, col_base, rows, lane,
+                                                           [&] { mbar_arrive(te); });
+                    }
+                    continue;
+                }
+            }
             if constexpr (kPair) {
                 const uint32_t te = map_to_cta(tempty_bar(b), 0);
                 store_accumulator<BN>(t_row, d, row_base, col_base, stage, lane, [&] { mbar_arrive_cluster(te); });

@@ -219,6 +219,16 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, int32_t c0, int32
                  : "memory");
 }
 
+// Bulk (non-tensor) copy of `bytes` contiguous bytes from this CTA's shared memory to global
+// memory, in this thread's current bulk group.  Both addresses must be 16-byte aligned and
+// `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until the shared-memory sources of this thread's committed bulk groups have been read.

@@ -121,6 +121,33 @@ def test_k_zero_and_empty_outputs():
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("cta_group,tile_n", [(1, 128), (1, 256), (2, 128), (2, 256)])
+@pytest.mark.parametrize("off", [1, 2, 3])
+def test_unaligned_c_every_variant(cta_group, tile_n, off):
+    """Every tile shape writing a C whose rows start 4 * off bytes past a 16-byte boundary
+    (row pitch 1001 floats, so consecutive rows shift by one more element): the oracle's
+    result bit for bit on integer inputs, with units of one and of several tiles, and the NaN
+    guard zones around and between the rows untouched."""
+    M, N, K, ldc = 1000, 1000, 320, 1001
+    rng = np.random.default_rng(62 + off)
+    Ai, Bi = inputs.integer_pair(rng, M, N, K)
+    guard = 4096
+    for max_ctas in (0, 16):
+        c_buf = torch.full((guard + off + M * ldc + guard,), float("nan"), dtype=torch.float32, device="cuda")
+        c_base = c_buf.data_ptr() + (guard + off) * 4
+        dAi, dBi = dev16(Ai), dev16(Bi)  # kept alive until the call has run
+        st = tct.gemm_f16_f32_ex(dAi.data_ptr(), dBi.data_ptr(), c_base, M, N, K, K, N, ldc,
+                                 torch.cuda.current_stream().cuda_stream, cta_group=cta_group, tile_n=tile_n,
+                                 max_ctas=max_ctas)
+        assert st == tct.GEMM_OK
+        torch.cuda.synchronize()
+        host = c_buf.cpu().numpy()
+        assert np.all(np.isnan(host[:guard + off])) and np.all(np.isnan(host[guard + off + M * ldc:]))
+        body = host[guard + off:guard + off + M * ldc].reshape(M, ldc)
+        assert np.all(np.isnan(body[:, N:]))
+        assert bit_exact(body[:, :N], oracle.gemm_f32(Ai, Bi))
+
+
 @pytest.mark.parametrize("M,N,K,pad_a,pad_b,pad_c,off", [
     (300, 200, 150, 7, 5, 3, 0),
     (129, 65, 33, 0, 0, 0, 1),
@@ -422,11 +449,12 @@ def test_square_integer_bit_exact_whole(n, seed):
 # ---- C that TMA cannot write ------------------------------------------------------------
 
 @pytest.mark.parametrize("M,N,K,off,pad", [(1793, 1793, 1793, 0, 0), (300, 201, 150, 1, 2), (129, 65, 700, 3, 0),
-                                           (1000, 1100, 2000, 1, 1), (17, 4097, 31, 2, 5)])
+                                           (1000, 1100, 2000, 1, 1), (17, 4097, 31, 2, 5), (2048, 4097, 256, 1, 0)])
 def test_unaligned_c_guard_zones(M, N, K, off, pad):
-    """C whose rows do not start on 16-byte boundaries or end inside a 16-byte unit (stored by
-    the epilogue's per-lane stores): the oracle's result in the M x N block, bit for bit on
-    integer inputs, and NaN guard zones before, after and between the rows untouched."""
+    """C whose rows do not start on 16-byte boundaries or end inside a 16-byte unit (a unit's
+    last tile staged as whole rows and bulk-copied, its other tiles by per-lane stores): the
+    oracle's result in the M x N block, bit for bit on integer inputs, and NaN guard zones
+    before, after and between the rows untouched."""
     rng = np.random.default_rng(61)
     A, B = inputs.normal_pair(rng, M, N, K)
     ldc = N + pad
