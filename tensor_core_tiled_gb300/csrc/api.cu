@@ -482,6 +482,11 @@ tct::KernelParams make_params(const gemm_plan &pl, float *C, int64_t M, int64_t 
     p.split_mode = pl.split_form == 2 ? (pl.split_parts_per_unit <= 2 ? 3 : 2) : 0;
     p.sk_units = pl.split_form == 2 ? pl.sk_units : 0;
     p.b_stream = p.num_m == 1 ? 1 : 0;
+    p.a_keep = (p.num_m > 1 && p.num_n > 1 &&
+                2.0 * (static_cast<double>(M) * static_cast<double>(K) + static_cast<double>(K) * static_cast<double>(N)) >
+                    kL2Bytes)
+                   ? 1
+                   : 0;
     p.c_tma = 0;
     return p;
 }

@@ -74,6 +74,11 @@ struct KernelParams {
     // push out the A rows every tile re-reads (measured on GB300 at 128 x 16384 x 16384:
     // 94.3 -> 90.6 us).
     int32_t b_stream;
+    // 1 when the operands do not fit in L2 and A's rows are re-read by several column tiles:
+    // A's TMA loads then mark three quarters of their L2 lines evict-last, so that a GROUP_M
+    // group's A rows survive the B columns streaming past them across its waves (measured on
+    // GB300: DRAM reads -5 to -10% at 8192^3, 6144^3 and 16384 x 16384 x 4096, time unchanged).
+    int32_t a_keep;
 };
 
 enum WorkMode : int32_t {

@@ -688,6 +688,8 @@ __global__ void __launch_bounds__(192, 1)
             WorkItem w;
             const bool b_first_out = !kPair && p.b_stream != 0;  // B read by one tile only
             const uint64_t b_policy = l2_policy_evict_first();
+            const bool a_keep = p.a_keep != 0;  // A rows re-read across a group's waves
+            const uint64_t a_policy = l2_policy_evict_last(0.75f);
             for (int idx = 0; ok && work_item(p, unit, idx, w); ++idx) {
                 const TileCoord c = tile_coord(w.tile, p.num_m, p.num_n, p.group_m);
                 const int32_t m0 = c.m * (Cf::BM * CG) + static_cast<int32_t>(rank) * Cf::BM;
@@ -716,20 +718,27 @@ __global__ void __launch_bounds__(192, 1)
                         else
                             tma_load_2d(dst, tm, c0, c1, fb);
                     };
+                    auto load_hint = [&](uint32_t dst, const CUtensorMap *tm, int32_t c0, int32_t c1, uint64_t pol) {
+                        if constexpr (kPair)
+                            tma_load_2d_pair_hint(dst, tm, c0, c1, fb, pol);
+                        else
+                            tma_load_2d_hint(dst, tm, c0, c1, fb, pol);
+                    };
 #pragma unroll
                     for (int j = 0; j < Cf::A_BOXES; ++j) {
                         const uint32_t dst = smem_u32(sA + s * Cf::A_STAGE + j * Cf::B_SUB);
-                        if constexpr (AT)
-                            load(dst, &tmA, m0 + 64 * j, k0);
+                        const int32_t ac0 = AT ? m0 + 64 * j : k0, ac1 = AT ? k0 : m0;
+                        if (a_keep)
+                            load_hint(dst, &tmA, ac0, ac1, a_policy);
                         else
-                            load(dst, &tmA, k0, m0);
+                            load(dst, &tmA, ac0, ac1);
                     }
 #pragma unroll
                     for (int j = 0; j < Cf::B_BOXES; ++j) {
                         const uint32_t dst = smem_u32(sB + s * Cf::B_STAGE + j * Cf::B_SUB);
                         const int32_t bc0 = BT ? k0 : n0 + 64 * j, bc1 = BT ? n0 : k0;
                         if (b_first_out)
-                            tma_load_2d_hint(dst, &tmB, bc0, bc1, fb, b_policy);
+                            load_hint(dst, &tmB, bc0, bc1, b_policy);
                         else
                             load(dst, &tmB, bc0, bc1);
                     }

@@ -114,7 +114,16 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return pol;
 }
 
-// tma_load_2d with an L2 cache policy (from l2_policy_evict_first).
+// An L2 cache policy that marks the given fraction (0..1] of the lines a load brings in as the
+// last to evict; the others keep their priority.
+__device__ __forceinline__ uint64_t l2_policy_evict_last(float fraction)
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, %1;" : "=l"(pol) : "f"(fraction));
+    return pol;
+}
+
+// tma_load_2d with an L2 cache policy (from l2_policy_evict_first or l2_policy_evict_last).
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap, int32_t c0, int32_t c1,
                                                  uint32_t bar, uint64_t policy)
 {
@@ -337,6 +346,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+
+// tma_load_2d_pair with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void *tmap, int32_t c0, int32_t c1,
+                                                      uint32_t bar_cluster, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar_cluster), "l"(policy)
         : "memory");
 }
 
