@@ -4,7 +4,7 @@ Every case draws, from its own seed: a shape (log-uniform sizes, occasionally K 
 operand type and storage (gemm_f32acc's four layouts, FP16 or BF16), padded leading
 dimensions and element offsets of the bases (so some operands are repacked and some C
 matrices are stored without 16-byte vectors), and planner options (tile width, CTA pairs,
-grid caps, GROUP_M, forced or forbidden split tails).  A quarter of the GEMM cases use
+grid caps, GROUP_M, forced or forbidden split tails, stream-K where a plan for it exists).  A quarter of the GEMM cases use
 integer inputs and must match bit for bit; the rest must meet the parity tolerance.  Every
 case also checks that nothing outside the M x N block of C was written.  The epilogue cases
 add random alpha, beta, bias and output types (gemm_ex); the softmax cases draw row lengths
@@ -65,7 +65,7 @@ def _draw_gemm(seed):
                 pad_c=int(rng.choice([0, 0, 1, 4])), off_c=int(rng.choice([0, 0, 0, 1, 4])))
     opts = {}
     if rng.random() < 0.5:
-        opts["stream_k"] = int(rng.choice([1, 2]))
+        opts["stream_k"] = int(rng.choice([1, 2, 3]))
     if rng.random() < 0.3:
         opts["cta_group"] = int(rng.choice([1, 2]))
     if rng.random() < 0.3:
@@ -74,8 +74,24 @@ def _draw_gemm(seed):
         opts["max_ctas"] = int(rng.integers(2, 153))
     if rng.random() < 0.3:
         opts["group_m"] = int(rng.integers(1, 17))
+    if opts.get("stream_k") == 3:
+        # stream-K adds pieces into C by TMA reduce-add: give it a C that TMA can write (rows of
+        # whole 16-byte units on a 16-byte grid), so that most of these cases run it
+        case["N"] = -(-N // 4) * 4
+        case["pad_c"] = case["pad_c"] // 4 * 4
+        case["off_c"] = case["off_c"] // 4 * 4
     case["opts"] = opts
     return rng, case
+
+
+def _call(fn, opts):
+    """fn(**opts); stream-K asked for (stream_k 3) is rejected with GEMM_ERR_INVALID_ARG where no
+    stream-K plan exists (C not TMA-writable, an epilogue other than the plain FP32 one, too
+    few k-blocks): then the call is repeated with the planner's own choice."""
+    st = fn(**opts)
+    if st == tct.GEMM_ERR_INVALID_ARG and opts.get("stream_k") == 3:
+        st = fn(**{k: v for k, v in opts.items() if k != "stream_k"})
+    return st
 
 
 def _operands(rng, c):
@@ -102,8 +118,8 @@ def test_gemm_fuzz(seed):
     ldc = N + c["pad_c"]
     C = torch.full((c["off_c"] + M * ldc + 8,), float("nan"), device="cuda")
     pC = C.data_ptr() + 4 * c["off_c"]
-    st = tct.gemm_f32acc(TYPES[c["dt"]][1], int(c["ta"]), int(c["tb"]), pA, pB, pC, M, N, K, lda, ldb, ldc,
-                         torch.cuda.current_stream().cuda_stream, **c["opts"])
+    st = _call(lambda **o: tct.gemm_f32acc(TYPES[c["dt"]][1], int(c["ta"]), int(c["tb"]), pA, pB, pC, M, N, K, lda,
+                                           ldb, ldc, torch.cuda.current_stream().cuda_stream, **o), c["opts"])
     assert st == tct.GEMM_OK, c
     torch.cuda.synchronize()
     host = C.cpu().numpy()
@@ -145,9 +161,10 @@ def test_gemm_ex_fuzz(seed):
         bias = (b.astype(np.float32) if bt == "f32" else b.astype(np.float16).view(np.uint16) if bt == "f16"
                 else inputs.to_bf16_bits(b))
         dbias = torch.from_numpy(bias.view(np.int32 if bt == "f32" else np.int16)).cuda()
-    st = tct.gemm_ex(TYPES[c["dt"]][1], int(c["ta"]), int(c["tb"]), pA, pB, dC.data_ptr(), TYPES[ct][1], M, N, K,
-                     lda, ldb, N, alpha=alpha, beta=beta, bias=dbias.data_ptr() if bt else 0,
-                     bias_type=TYPES[bt or "f32"][1], stream=torch.cuda.current_stream().cuda_stream, **c["opts"])
+    st = _call(lambda **o: tct.gemm_ex(TYPES[c["dt"]][1], int(c["ta"]), int(c["tb"]), pA, pB, dC.data_ptr(),
+                                       TYPES[ct][1], M, N, K, lda, ldb, N, alpha=alpha, beta=beta,
+                                       bias=dbias.data_ptr() if bt else 0, bias_type=TYPES[bt or "f32"][1],
+                                       stream=torch.cuda.current_stream().cuda_stream, **o), c["opts"])
     assert st == tct.GEMM_OK, c
     torch.cuda.synchronize()
     got = dC.cpu().numpy()
