@@ -61,6 +61,7 @@ constexpr int64_t kStreamKPieceCaps[] = {1, 2, 3, 4, 6};
 
 constexpr Candidate kCandidates[] = {
     {2, 256, 6, 1.00},
+    {2, 192, 6, 0.82},
     {1, 256, 4, 0.85},
     {1, 128, 6, 0.70},
     {2, 128, 8, 0.57},
@@ -170,14 +171,14 @@ gemm_status check_options(const gemm_options *opt)
     if (opt->fault_inject < 0 || opt->fault_inject > 3) return GEMM_ERR_INVALID_ARG;
     if (opt->stream_k < 0 || opt->stream_k > 3) return GEMM_ERR_INVALID_ARG;
     if (opt->group_m < 0 || opt->group_m > 256) return GEMM_ERR_INVALID_ARG;
-    if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return GEMM_ERR_INVALID_ARG;
+    if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 192 && opt->tile_n != 256) return GEMM_ERR_INVALID_ARG;
     if (opt->cta_group < 0 || opt->cta_group > 2) return GEMM_ERR_INVALID_ARG;
     if (opt->stages < 0 || opt->max_ctas < 0 || opt->timeout_ms < 0) return GEMM_ERR_INVALID_ARG;
     if (opt->stages != 0) {
         // some compiled variant must match every field that is set
         bool any = false;
         for (int cg = 1; cg <= 2; ++cg)
-            for (int tn = 128; tn <= 256; tn += 128) {
+            for (int tn = 128; tn <= 256; tn += 64) {
                 if ((opt->cta_group && opt->cta_group != cg) || (opt->tile_n && opt->tile_n != tn)) continue;
                 if (tct::variant_smem_bytes(cg, tn, opt->stages) > 0) any = true;
             }

@@ -160,6 +160,7 @@ inline bool work_item(const KernelParams &p, int32_t u, int32_t idx, WorkItem &i
 // 256 x tile_n tiles on a CTA pair; per CTA and stage 16 KB of A + tile_n * 64 B of B.
 // The epilogue staging takes 16 KB more.
 #define TCT_VARIANTS(X) \
+    X(2, 192, 6)        \
     X(1, 256, 2)        \
     X(1, 256, 3)        \
     X(1, 256, 4)        \

@@ -66,9 +66,12 @@ struct Cfg {
     static constexpr int UMMA_K = 16;         // K of one kind::f16 MMA
     static constexpr int A_STAGE = BM * BK * 2;
     static constexpr int B_SUB = BK * 64 * 2;  // one 64-column TMA box of B
-    static constexpr int B_BOXES = BT_ ? 1 : BN_CTA / 64;  // TMA boxes of B per stage
+    // TMA boxes of B per stage: B as K x N arrives in 64-column boxes (a CTA of a 192-column
+    // pair tile holds 96 columns: two boxes, the second one's last 32 columns unused); B as
+    // N x K arrives as one K-major box of BN_CTA rows.
+    static constexpr int B_BOXES = BT_ ? 1 : (BN_CTA + 63) / 64;
     static constexpr int A_BOXES = AT_ ? 2 : 1;            // TMA boxes of A per stage
-    static constexpr int B_STAGE = BK * BN_CTA * 2;
+    static constexpr int B_STAGE = BT_ ? BK * BN_CTA * 2 : B_BOXES * B_SUB;
     static constexpr int STAGE_TX = CG * (A_STAGE + B_STAGE);  // bytes counted on one full barrier
     static constexpr int EPI_WARPS = 4;
     static constexpr int EPI_BYTES = EPI_WARPS * 32 * 32 * 4;
@@ -81,11 +84,13 @@ struct Cfg {
     // epilogue warp, BN + 4 floats apart) in the idle stage buffers.
     static constexpr int ROW_PITCH = BN + 4;
     static constexpr bool ROWS_OK = STAGES * (A_STAGE + B_STAGE) >= EPI_WARPS * 32 * ROW_PITCH * 4;
-    static constexpr int TMEM_COLS = 2 * BN;
+    // two accumulator buffers of BN columns; the allocation is a power of two of at least 32
+    static constexpr int TMEM_COLS = 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
     static constexpr int SMEM_BYTES =
         1024 + STAGES * (A_STAGE + B_STAGE) + EPI_BYTES + BIAS_BYTES + NUM_BARS * 8 + 16;
     static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per tile");
-    static_assert(BN_CTA % 64 == 0 && BN <= 256, "B columns per CTA must be whole 64-column boxes");
+    static_assert(BN_CTA % 32 == 0 && BN % 64 == 0 && BN <= 256, "B columns per CTA: a multiple of 32");
+    static_assert(B_STAGE % 1024 == 0, "each stage's B starts on a 1024-byte swizzle boundary");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory");
 };

@@ -190,6 +190,13 @@ def test_planner_on_gb300_shapes(tct_lib):
         assert tct.gemm_f16_f32_plan(*shape, num_sms=sms)["split_form"] == 2, shape
     for shape in ((1792, 1792, 1792), (2048, 2048, 2048), (16384, 16384, 4096)):
         assert tct.gemm_f16_f32_plan(*shape, num_sms=sms)["split_form"] == 0, shape
+    # wave quantisation decides the tile width: 1792^3 fills one wave better with 70 pair tiles
+    # of 256x192 than with 49 of 256x256 (measured 19.5 against 20.5 us); 1793^3 (80 tiles of
+    # 192 columns, more than the 76 pairs) and 2048^3 (64 tiles of 256) keep 256 columns
+    assert (tct.gemm_f16_f32_plan(1792, 1792, 1792, num_sms=sms)["tile_n"],
+            tct.gemm_f16_f32_plan(1792, 1792, 1792, num_sms=sms)["tiles"]) == (192, 70)
+    for shape in ((1793, 1793, 1793), (2048, 2048, 2048), (4096, 4096, 4096), (8192, 8192, 8192)):
+        assert tct.gemm_f16_f32_plan(*shape, num_sms=sms)["tile_n"] == 256, shape
     # the skinny, bandwidth-bound shape: among plans within 5% of the HBM time, the one whose
     # tiles move the fewest operand bytes from L2 (1-CTA 128x256 tiles, split in k-halves)
     p = tct.gemm_f16_f32_plan(128, 16384, 16384, num_sms=sms)
@@ -207,7 +214,7 @@ def test_planner_on_gb300_shapes(tct_lib):
     p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, cta_group=1, tile_n=256)
     assert (p["cta_group"], p["tile_m"], p["stages"], p["grid"]) == (1, 128, 4, 152)
     # every compiled variant's shared-memory ring fits the 227 KB limit
-    for cg, tn, st in ((1, 256, 2), (1, 256, 3), (1, 256, 4), (1, 128, 4), (1, 128, 6),
+    for cg, tn, st in ((1, 256, 2), (1, 256, 3), (1, 256, 4), (1, 128, 4), (1, 128, 6), (2, 192, 6),
                        (2, 256, 3), (2, 256, 4), (2, 256, 5), (2, 256, 6), (2, 128, 6), (2, 128, 8)):
         p = tct.gemm_f16_f32_plan(4096, 4096, 4096, num_sms=sms, cta_group=cg, tile_n=tn, stages=st)
         assert (p["cta_group"], p["tile_n"], p["stages"]) == (cg, tn, st)

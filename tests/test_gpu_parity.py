@@ -121,7 +121,7 @@ def test_k_zero_and_empty_outputs():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("cta_group,tile_n", [(1, 128), (1, 256), (2, 128), (2, 256)])
+@pytest.mark.parametrize("cta_group,tile_n", [(1, 128), (1, 256), (2, 128), (2, 192), (2, 256)])
 @pytest.mark.parametrize("off", [1, 2, 3])
 def test_unaligned_c_every_variant(cta_group, tile_n, off):
     """Every tile shape writing a C whose rows start 4 * off bytes past a 16-byte boundary
@@ -243,6 +243,7 @@ VARIANT_OPTS = [
     dict(cta_group=2, tile_n=256, stages=5), dict(cta_group=2, tile_n=256, stages=6, group_m=1),
     dict(cta_group=2, tile_n=128, stages=6), dict(cta_group=2, tile_n=128, stages=8, group_m=4),
     dict(cta_group=2, tile_n=256, max_ctas=6), dict(cta_group=2, tile_n=128, max_ctas=2),
+    dict(cta_group=2, tile_n=192), dict(cta_group=2, tile_n=192, group_m=5, max_ctas=10),
 ]
 
 
@@ -274,7 +275,7 @@ def test_pair_and_single_cta_tiles_agree():
     assert within_tol(one.cpu().numpy(), R, K) and within_tol(two.cpu().numpy(), R, K)
 
 
-@pytest.mark.parametrize("cta_group,tile_n", [(1, 128), (1, 256), (2, 128), (2, 256)])
+@pytest.mark.parametrize("cta_group,tile_n", [(1, 128), (1, 256), (2, 128), (2, 192), (2, 256)])
 def test_every_variant_on_ragged_and_integer_inputs(cta_group, tile_n):
     for (M, N, K), A, B in inputs.workload("ragged"):
         C = gpu_gemm(A, B, cta_group=cta_group, tile_n=tile_n)
@@ -302,6 +303,7 @@ STREAM_K_CASES = [
     ((2048, 2048, 2048), dict(stream_k=2)),
     ((3072, 3072, 1024), dict(stream_k=2)),
     ((1500, 5000, 777), dict(stream_k=2, cta_group=1, tile_n=128)),
+    ((3000, 4000, 1000), dict(stream_k=2, cta_group=2, tile_n=192)),
 ]
 
 
@@ -337,6 +339,7 @@ STREAM_K_CHAIN_CASES = [
     ((4096, 4096, 1024), {}),
     ((777, 1500, 515), {"max_ctas": 40}),
     ((129, 68, 64 * 33), {"cta_group": 1, "tile_n": 128}),
+    ((1000, 1000, 3000), {"cta_group": 2, "tile_n": 192}),
 ]
 
 
