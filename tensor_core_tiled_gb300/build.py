@@ -16,7 +16,12 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libtensor_core_tiled.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["gemm_sm103a.cu", "api.cu", "softmax_sm103a.cu", "probe_sm103a.cu"]
+# (source, object, extra flags): the GEMM kernel source compiles as two objects in parallel,
+# each holding the kernels of a share of the operand layouts (TCT_PART 0 and 1).
+SOURCES = [("gemm_sm103a.cu", "gemm_sm103a_part0.o", ["-DTCT_PART=0"]),
+           ("gemm_sm103a.cu", "gemm_sm103a_part1.o", ["-DTCT_PART=1"]),
+           ("api.cu", "api.o", []), ("softmax_sm103a.cu", "softmax_sm103a.o", []),
+           ("probe_sm103a.cu", "probe_sm103a.o", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -49,9 +54,10 @@ def build(force=False, verbose=False, extra_flags=()):
     if verbose:
         common += ["-Xptxas", "-v"]
 
-    def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-        cmd = common + ["-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job):
+        src, obj_name, flags = job
+        obj = os.path.join(BUILD_DIR, obj_name)
+        cmd = common + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")

@@ -198,6 +198,10 @@ int variant_max_clusters(int cta_group, int tile_n, int stages);
 cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const CUtensorMap &tc,
                         const KernelParams &p, int layout, int cta_group, int tile_n, int stages, int grid,
                         cudaStream_t stream);
+// The layouts 3..7 of launch_gemm, compiled in the second object of the kernel source.
+cudaError_t launch_gemm_part1(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp,
+                              const CUtensorMap &tc, const KernelParams &p, int layout, int cta_group, int tile_n,
+                              int stages, int grid, cudaStream_t stream);
 
 // One matrix of a row copy: rows x cols elements of esz bytes (2 or 4), leading dimensions
 // in elements; a NULL src skips it.
@@ -224,6 +228,8 @@ cudaError_t launch_pack2(const void *src0, int64_t ld_src0, void *dst0, int64_t 
 cudaError_t launch_fill_epilogue(const KernelParams &p, int num_sms, cudaStream_t stream);
 
 cudaError_t read_and_clear_error(unsigned *out);
+// The second object's error word, read and cleared (read_and_clear_error reads both).
+cudaError_t read_and_clear_error_part1(unsigned *out);
 
 // Device address of the library's error word (code | wait site << 8) on the current device.
 cudaError_t error_word_address(unsigned **out);

@@ -48,9 +48,17 @@
 #include "ptx_sm103a.cuh"
 #include "tile_sched.h"
 
+// The file compiles as two objects that run in parallel: TCT_PART 0 holds the kernels of the
+// row-major and single-transpose FP16 layouts and every host-side function, TCT_PART 1 the
+// kernels of the other layouts (each object keeps its own device error word; the host reads
+// and clears both).
+#ifndef TCT_PART
+#define TCT_PART 0
+#endif
+
 namespace tct {
 
-__device__ unsigned int g_error_word;
+static __device__ unsigned int g_error_word;
 
 template <int CG_, int BN_, int STAGES_, bool AT_ = false, bool BT_ = false, bool BF16_ = false>
 struct Cfg {
@@ -1170,6 +1178,7 @@ __device__ __forceinline__ void copy_unit(const CopyJob &j, int64_t r, int64_t u
     }
 }
 
+#if TCT_PART == 0
 __global__ void __launch_bounds__(kCopyThreads) copy_rows(const CopyJob j0, const CopyJob j1)
 {
     // Launched as a programmatic dependent launch: wait for the kernel before it (which may
@@ -1202,6 +1211,8 @@ __global__ void fill_epilogue(const KernelParams p)
         store_general(d, r, c, make_float4(0.f, 0.f, 0.f, 0.f));
     }
 }
+
+#endif  // TCT_PART == 0
 
 // ---------------------------------------------------------------- host side
 
@@ -1265,6 +1276,7 @@ static int max_clusters_variant()
     return n;
 }
 
+#if TCT_PART == 0
 int variant_smem_bytes(int cta_group, int tile_n, int stages)
 {
 #define TCT_CASE(CG_, BN_, ST_) \
@@ -1309,6 +1321,8 @@ int variant_exists(int layout, int cta_group, int tile_n, int stages)
     return 0;
 }
 
+#endif  // TCT_PART == 0
+
 template <bool AT, bool BT, bool BF16>
 static cudaError_t launch_layout(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp,
                                  const CUtensorMap &tc, const KernelParams &p, int cta_group, int tile_n, int stages,
@@ -1326,6 +1340,29 @@ static cudaError_t launch_layout(const CUtensorMap &ta, const CUtensorMap &tb, c
     return cudaErrorInvalidValue;
 }
 
+#if TCT_PART == 1
+cudaError_t launch_gemm_part1(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp,
+                              const CUtensorMap &tc, const KernelParams &p, int layout, int cta_group, int tile_n,
+                              int stages, int grid, cudaStream_t stream)
+{
+    switch (layout) {
+    case 3: return launch_layout<true, true, false>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 4: return launch_layout<false, false, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 5: return launch_layout<true, false, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 6: return launch_layout<false, true, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    case 7: return launch_layout<true, true, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t read_and_clear_error_part1(unsigned *out)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_error_word, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned));
+}
+#else
 cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tp, const CUtensorMap &tc,
                         const KernelParams &p, int layout, int cta_group, int tile_n, int stages, int grid,
                         cudaStream_t stream)
@@ -1334,12 +1371,7 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUte
     case 0: return launch_layout<false, false, false>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
     case 1: return launch_layout<true, false, false>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
     case 2: return launch_layout<false, true, false>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
-    case 3: return launch_layout<true, true, false>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
-    case 4: return launch_layout<false, false, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
-    case 5: return launch_layout<true, false, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
-    case 6: return launch_layout<false, true, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
-    case 7: return launch_layout<true, true, true>(ta, tb, tp, tc, p, cta_group, tile_n, stages, grid, stream);
-    default: return cudaErrorInvalidValue;
+    default: return launch_gemm_part1(ta, tb, tp, tc, p, layout, cta_group, tile_n, stages, grid, stream);
     }
 }
 
@@ -1405,7 +1437,13 @@ cudaError_t read_and_clear_error(unsigned *out)
     e = cudaMemcpyFromSymbol(out, g_error_word, sizeof(unsigned));
     if (e != cudaSuccess) return e;
     const unsigned zero = 0;
-    return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned));
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    unsigned other = 0;  // the word of the other object's kernels: the first error recorded wins
+    e = read_and_clear_error_part1(&other);
+    if (e == cudaSuccess && *out == 0) *out = other;
+    return e;
 }
+#endif  // TCT_PART
 
 }  // namespace tct
