@@ -147,3 +147,33 @@ def test_unpublished_stream_k_piece_times_out_and_context_survives(M, N, K, chai
     C2 = tct.matmul(dA, dB, **opts)
     assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
     assert within_tol(C2.cpu().numpy(), R, K)
+
+
+@pytest.mark.parametrize("dt,ta,tb", [("bf16", False, False), ("f16", True, True), ("f16", True, False)])
+def test_timeout_in_every_kernel_object_is_reported(dt, ta, tb):
+    """The kernels of BF16 and of both-transposed operands are built in a second object with
+    its own device error word; a wait that runs out there is reported by the same status call
+    and cleared by it, like one in the first object's kernels (A transposed, FP16); the next
+    call then gives the oracle's result."""
+    M, N, K = 2000, 3000, 1000
+    rng = np.random.default_rng(53)
+    A, B = inputs.pair_ex(rng, M, N, K, dtype=dt, trans_a=ta, trans_b=tb)
+    tdt = torch.float16 if dt == "f16" else torch.bfloat16
+    dA = torch.from_numpy(np.ascontiguousarray(A).view(np.int16)).cuda().view(tdt)
+    dB = torch.from_numpy(np.ascontiguousarray(B).view(np.int16)).cuda().view(tdt)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    ab = tct.GEMM_DTYPE_F16 if dt == "f16" else tct.GEMM_DTYPE_BF16
+    opts = dict(stream_k=2, cta_group=2, tile_n=256, max_ctas=150)
+
+    def call(**extra):
+        return tct.gemm_f32acc(ab, int(ta), int(tb), dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K,
+                               A.shape[1], B.shape[1], N, torch.cuda.current_stream().cuda_stream, **opts, **extra)
+
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    assert call(timeout_ms=50, fault_inject=1) == tct.GEMM_OK
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_ERR_DEVICE_TIMEOUT
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    assert call() == tct.GEMM_OK
+    assert tct.gemm_f16_f32_get_error() == tct.GEMM_OK
+    R = oracle.gemm_ex_f32(A, B, dtype=oracle.F16 if dt == "f16" else oracle.BF16, trans_a=ta, trans_b=tb)
+    assert within_tol(C.cpu().numpy(), R, K)
