@@ -72,8 +72,7 @@ TCT_API gemm_status gemm_f16_f32(const void *A, const void *B, float *C, int64_t
  *   group_m   : output tile rows per launch-order group ("06_triton_style.py",
  *               matmul_kernel and demo 2: GROUP_M program order for L2 reuse); 1 gives
  *               row-major tile order.  Range 1..256.
- *   tile_n    : output tile width in columns: 128 or 256, or 192 (CTA pairs only, FP16
- *               operands stored as given).
+ *   tile_n    : output tile width in columns: 128 or 256, or 192 (CTA pairs only).
  *   stages    : shared-memory pipeline depth (a compiled depth for the chosen tile).
  *   max_ctas  : cap on the persistent grid in CTAs (default: every co-resident CTA).
  *   timeout_ms: limit on any single device pipeline wait (default 2000 ms).

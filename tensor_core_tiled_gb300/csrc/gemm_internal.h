@@ -176,6 +176,7 @@ inline bool work_item(const KernelParams &p, int32_t u, int32_t idx, WorkItem &i
 // Variants compiled for the other operand layouts and BF16 (the planner's candidates).
 #define TCT_VARIANTS_EX(X) \
     X(2, 256, 6)           \
+    X(2, 192, 6)           \
     X(1, 256, 4)           \
     X(1, 128, 6)           \
     X(2, 128, 8)

@@ -74,8 +74,8 @@ def _draw_gemm(seed):
         opts["max_ctas"] = int(rng.integers(2, 153))
     if rng.random() < 0.3:
         opts["group_m"] = int(rng.integers(1, 17))
-    if opts.get("tile_n") == 192 and (case["ta"] or case["tb"] or case["dt"] != "f16" or opts.get("cta_group") == 1):
-        opts["tile_n"] = 256  # 192-column tiles: CTA pairs on FP16 operands stored as given
+    if opts.get("tile_n") == 192 and opts.get("cta_group") == 1:
+        opts["tile_n"] = 256  # 192-column tiles: CTA pairs only
     if opts.get("stream_k") == 3:
         # stream-K adds pieces into C by TMA reduce-add: give it a C that TMA can write (rows of
         # whole 16-byte units on a 16-byte grid), so that most of these cases run it

@@ -67,6 +67,7 @@ def test_integer_inputs_bit_exact(dt, ta, tb):
 @pytest.mark.parametrize("dt,ta,tb", LAYOUTS)
 @pytest.mark.parametrize("opts", [dict(cta_group=2, tile_n=256), dict(cta_group=1, tile_n=256),
                                   dict(cta_group=1, tile_n=128), dict(cta_group=2, tile_n=128),
+                                  dict(cta_group=2, tile_n=192),
                                   dict(stream_k=2, cta_group=2, tile_n=256)])
 def test_every_planner_variant(dt, ta, tb, opts):
     rng = np.random.default_rng(63)
