@@ -25,10 +25,12 @@ constexpr int kMaxDevices = 64;
 
 // Kernel variants the planner chooses between, with the relative per-tile throughput
 // each reached on GB300 with every SM busy (8192^3 and 4096^3, same clocks): the pair
-// 256 x 256 tile moves the fewest operand bytes into shared memory per FLOP; the
-// 128-column tiles are much slower per tile and only pay off when they fill SMs that a
-// wider tile would leave idle (skinny M or N).  The planner weighs these against wave
-// quantisation.
+// 256 x 256 tile moves the fewest operand bytes into shared memory per FLOP; the pair
+// 256 x 192 tile loads the same stage bytes for three quarters of the MMAs (measured 0.80
+// of the 256-column rate at 8192^3, 0.86 at 1792^3) and pays off where it fills a wave
+// better (1792^3: 70 tiles on 76 pairs instead of 49); the 128-column tiles are much slower
+// per tile and only pay off when they fill SMs that a wider tile would leave idle (skinny
+// M or N).  The planner weighs these against wave quantisation.
 struct Candidate {
     int cta_group, tile_n, stages;
     double rate;
